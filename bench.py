@@ -1,0 +1,557 @@
+#!/usr/bin/env python
+"""Benchmark of the row-wise LayerNorm / RMSNorm hot path on one GB300.
+
+One step = one pass of the whole path over the bf16 workload with N = 8192
+rows and H in {1024, 5120}: for each H, LayerNorm forward + backward, RMSNorm
+forward + backward and the fused residual-add + RMSNorm forward (10 calls, 14
+kernel launches).  Each call is timed on the device with CUDA events on the
+launching stream, with L2 flushed (a write larger than twice the L2 size)
+before every call, as in training where the forward's outputs are long gone
+from L2 when the backward runs.
+
+Metric: achieved HBM GB/s = algorithmic bytes of the step / summed device
+time of its calls.  Algorithmic bytes per call (e = 2 bytes, bf16):
+  LN fwd 2NHe + 2He + 8N,  RMS fwd 2NHe + He + 4N,  fused 4NHe + He + 4N,
+  LN bwd 3NHe + 3He + 8N,  RMS bwd 3NHe + 2He + 4N.
+
+The JSON line also carries: per-call microseconds (the backward per shape
+included), a roofline object for the call with the largest share of the step,
+the SM clocks sampled during the timed region, an end-to-end figure through
+the public API with pinned host buffers and the copies inside the timed
+region, and the fp64 CPU oracle timed on the host as a reported baseline.
+
+``--impl reference`` times the CPU oracle alone on a bounded row sample of the
+same workload (there is no other implementation of this path to run).
+Under torchrun (N > 1) every rank runs an independent replica of the step
+(rows are independent; nothing is exchanged) and rank 0 prints the aggregate.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "LN+RMSNorm fwd+bwd and fused add+RMSNorm fwd, bf16, N=8192, H in {1024, 5120}"
+SHAPES = [(8192, 1024), (8192, 5120)]
+EPS, EPS_FUSED = 1e-5, 1e-6
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "LN/RMSNorm fwd+bwd achieved HBM GB/s and % of GB300 peak; bwd µs per shape (bf16)"
+OPS = ("ln_fwd", "ln_bwd", "rms_fwd", "rms_bwd", "fused_fwd")
+LAUNCHES = {"ln_fwd": 1, "rms_fwd": 1, "fused_fwd": 1, "ln_bwd": 2, "rms_bwd": 2}
+
+
+def alg_bytes(op: str, N: int, H: int, e: int = 2, ew: int = 2) -> int:
+    """Algorithmic HBM bytes of one call (each tensor byte read or written once)."""
+    nh = N * H * e
+    return {
+        "ln_fwd": 2 * nh + 2 * H * ew + 8 * N,
+        "rms_fwd": 2 * nh + H * ew + 4 * N,
+        "fused_fwd": 4 * nh + H * ew + 4 * N,
+        "ln_bwd": 3 * nh + 8 * N + H * ew + 2 * H * ew,
+        "rms_bwd": 3 * nh + 4 * N + H * ew + H * ew,
+    }[op]
+
+
+# ---------------------------------------------------------------------------
+# environment
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def src_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rmsnorm_ln_fwd_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(op_key: str):
+    """dram read+write bytes per launch of `op_key` from the committed ncu
+    summary, or None when absent or taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
+    try:
+        with open(path) as f:
+            kv = dict(line.strip().split("=", 1) for line in f if "=" in line and not line.startswith("#"))
+    except OSError:
+        return None
+    if kv.get("src_digest") != src_digest():
+        return None
+    v = kv.get(op_key)
+    return float(v) if v else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and os.path.getsize(self.path) == 0:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the workload on the GPU
+# ---------------------------------------------------------------------------
+
+class Shape:
+    """Device tensors of one (N, H) shape and argument tuples for the C ABI."""
+
+    def __init__(self, N, H, dev, seed, lib):
+        import torch
+        from rmsnorm_ln_fwd_gb300 import synth, ops
+        self.N, self.H, self.lib, self.dev = N, H, lib, dev
+        host = synth.norm_inputs(N, H, "bf16", seed=seed, with_residual=True)
+        self.host = host
+        t = {k: v.to(dev) for k, v in host.items()}
+        self.t = t
+        e = torch.empty
+        bf = torch.bfloat16
+        self.y = e(N, H, dtype=bf, device=dev)
+        self.yr = e(N, H, dtype=bf, device=dev)
+        self.yf = e(N, H, dtype=bf, device=dev)
+        self.h = e(N, H, dtype=bf, device=dev)
+        self.dx = e(N, H, dtype=bf, device=dev)
+        self.dxr = e(N, H, dtype=bf, device=dev)
+        self.mean = e(N, dtype=torch.float32, device=dev)
+        self.rstd = e(N, dtype=torch.float32, device=dev)
+        self.rstd_r = e(N, dtype=torch.float32, device=dev)
+        self.rstd_f = e(N, dtype=torch.float32, device=dev)
+        self.dg = e(H, dtype=bf, device=dev)
+        self.db = e(H, dtype=bf, device=dev)
+        self.dgr = e(H, dtype=bf, device=dev)
+        self.wsb = ops.bwd_workspace_bytes(H, dev)
+        self.ws = e((self.wsb + 3) // 4, dtype=torch.float32, device=dev)
+        self.bytes = {op: alg_bytes(op, N, H) for op in OPS}
+
+    def call(self, op, stream):
+        L, t, N, H = self.lib, self.t, self.N, self.H
+        BF = 1
+        if op == "ln_fwd":
+            st = L.ln_forward(t["x"].data_ptr(), H, t["gamma"].data_ptr(), t["beta"].data_ptr(), self.y.data_ptr(),
+                              H, self.mean.data_ptr(), self.rstd.data_ptr(), N, H, EPS, BF, BF, stream)
+        elif op == "ln_bwd":
+            st = L.ln_backward(t["dy"].data_ptr(), H, t["x"].data_ptr(), H, self.mean.data_ptr(),
+                               self.rstd.data_ptr(), t["gamma"].data_ptr(), self.dx.data_ptr(), H,
+                               self.dg.data_ptr(), self.db.data_ptr(), self.ws.data_ptr(), self.wsb, N, H, BF, BF,
+                               stream)
+        elif op == "rms_fwd":
+            st = L.rms_forward(t["x"].data_ptr(), H, t["gamma"].data_ptr(), self.yr.data_ptr(), H,
+                               self.rstd_r.data_ptr(), N, H, EPS, BF, BF, stream)
+        elif op == "rms_bwd":
+            st = L.rms_backward(t["dy"].data_ptr(), H, t["x"].data_ptr(), H, self.rstd_r.data_ptr(),
+                                t["gamma"].data_ptr(), self.dxr.data_ptr(), H, self.dgr.data_ptr(),
+                                self.ws.data_ptr(), self.wsb, N, H, BF, BF, stream)
+        else:
+            st = L.fused_add_rms_forward(t["x"].data_ptr(), H, t["residual"].data_ptr(), H, t["gamma"].data_ptr(),
+                                         self.yf.data_ptr(), H, self.h.data_ptr(), H, self.rstd_f.data_ptr(), N, H,
+                                         EPS_FUSED, BF, BF, stream)
+        if st != 0:
+            raise RuntimeError(f"{op} {N}x{H}: status {st}")
+
+
+def step_calls(shapes):
+    return [(s, op) for s in shapes for op in OPS]
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from rmsnorm_ln_fwd_gb300 import _build
+    _build.build()
+    import rmsnorm_ln_fwd_gb300 as nl
+    lib = nl.load_library()
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    shapes = [Shape(N, H, dev, seed=rank * 100 + i, lib=lib) for i, (N, H) in enumerate(SHAPES)]
+    calls = step_calls(shapes)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    for _ in range(args.warmup):
+        for s, op in calls:
+            flush.zero_()
+            s.call(op, sh)
+    torch.cuda.synchronize()
+
+    n = len(calls)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+          for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for k in range(args.steps):
+        for i, (s, op) in enumerate(calls):
+            flush.zero_()
+            ev[k][i][0].record(stream)
+            s.call(op, sh)
+            ev[k][i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+
+    per_call = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)] for i in range(n)]
+    step_ms = sum(sum(c) for c in per_call) / args.steps
+    step_bytes = sum(s.bytes[op] for s, op in calls)
+    ms_t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    step_ms_max = float(ms_t.item())
+    value = world * step_bytes / (step_ms_max * 1e-3) / 1e9
+
+    peak, peak_kind = measured_peak()
+    breakdown = {}
+    for i, (s, op) in enumerate(calls):
+        us = statistics.median(per_call[i]) * 1e3
+        mean_us = statistics.fmean(per_call[i]) * 1e3
+        gbs = s.bytes[op] / (mean_us * 1e-6) / 1e9
+        breakdown[f"{op}_{s.N}x{s.H}"] = {"us_median": round(us, 2), "us_mean": round(mean_us, 2),
+                                          "gbs": round(gbs, 1), "frac": round(gbs / peak, 3),
+                                          "bytes": s.bytes[op], "launches": LAUNCHES[op]}
+    # the call with the largest share of the step
+    dom_i = max(range(n), key=lambda i: sum(per_call[i]))
+    ds, dop = calls[dom_i]
+    dkey = f"{dop}_{ds.N}x{ds.H}"
+    d_us = statistics.fmean(per_call[dom_i]) * 1e3
+    achieved = ds.bytes[dop] / (d_us * 1e-6) / 1e9
+    traffic = recorded_traffic(dkey)
+
+    e2e = run_e2e(args, shapes, stream, dev, world, dist)
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows": 8192, "widths": [1024, 5120],
+                   "calls_per_step": [op for op in OPS],
+                   "l2": f"flushed before every timed call ({flush.numel() * 4 >> 20} MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "frac_of_peak": round(value / world / peak, 3),
+        "peak_gbs": peak,
+        "peak_kind": peak_kind,
+        "bwd_us": {k.replace("_bwd", ""): v["us_mean"] for k, v in breakdown.items() if "_bwd_" in k},
+        "breakdown": breakdown,
+        "roofline": {"bound": "hbm", "kernel": dkey + (" (main + partial-reduce kernels)" if "bwd" in dop else ""),
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 3), "traffic": traffic,
+                     "algorithmic_bytes": ds.bytes[dop], "peak_kind": f"{peak_kind} (hbm_gbs copy)"},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": args.steps * sum(LAUNCHES[op] for _, op in calls),
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if rank == 0:
+        out["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, shapes, stream, dev, world, dist):
+    """Same step through the public API with pinned host buffers: every step
+    copies its inputs host->device, runs the ten calls and copies every output
+    back, all inside the timed region (no L2 flush: the copies are the traffic)."""
+    import torch
+    import rmsnorm_ln_fwd_gb300 as nl
+    hosts = []
+    for s in shapes:
+        hin = {k: v.pin_memory() for k, v in s.host.items()}
+        hosts.append(hin)
+    h2d = sum(v.numel() * v.element_size() for hin in hosts for v in hin.values())
+    results = []
+
+    def one_step():
+        outs = []
+        for s, hin in zip(shapes, hosts):
+            d = {k: v.to(dev, non_blocking=True) for k, v in hin.items()}
+            y, mean, rstd = nl.ln_forward(d["x"], d["gamma"], d["beta"], EPS)
+            dx, dg, db = nl.ln_backward(d["dy"], d["x"], mean, rstd, d["gamma"], workspace=s.ws)
+            yr, rr = nl.rms_forward(d["x"], d["gamma"], EPS)
+            dxr, dgr = nl.rms_backward(d["dy"], d["x"], rr, d["gamma"], workspace=s.ws)
+            yf, h, rf = nl.fused_add_rms_forward(d["x"], d["residual"], d["gamma"], EPS_FUSED)
+            outs.extend([y, mean, rstd, dx, dg, db, yr, rr, dxr, dgr, yf, h, rf])
+        return [o.to("cpu", non_blocking=True) for o in outs]
+
+    for _ in range(max(1, args.warmup)):
+        one_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        results = one_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / e2e_steps
+    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms = float(ms_t.item())
+    d2h = sum(o.numel() * o.element_size() for o in results)
+    step_bytes = sum(s.bytes[op] for s in shapes for op in OPS)
+    return {"value": round(world * step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
+            "steps": e2e_steps}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle: baseline and reference arm
+# ---------------------------------------------------------------------------
+
+def oracle_step(samples):
+    import oracle as O
+    for x, dy, res, g, b in samples:
+        O.layer_norm_forward(x, g, b, EPS)
+        O.layer_norm_backward(dy, x, g, EPS)
+        O.rms_norm_forward(x, g, EPS)
+        O.rms_norm_backward(dy, x, g, EPS)
+        O.fused_add_rms_norm_forward(x, res, g, EPS_FUSED, "bfloat16")
+
+
+def oracle_samples(rows):
+    from rmsnorm_ln_fwd_gb300 import synth
+    out = []
+    for i, (N, H) in enumerate(SHAPES):
+        c = synth.norm_inputs(rows, H, "bf16", seed=i, with_residual=True)
+        f = {k: v.double().numpy() for k, v in c.items()}
+        out.append((f["x"], f["dy"], f["residual"], f["gamma"], f["beta"]))
+    return out
+
+
+def sample_bytes(rows):
+    return sum(alg_bytes(op, rows, H) for _, H in SHAPES for op in OPS)
+
+
+def cpu_baseline(args, target_s=None):
+    target_s = args.cpu_seconds if target_s is None else target_s
+    rows = args.cpu_rows
+    samples = oracle_samples(rows)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle_step(samples)
+        reps += 1
+        if time.perf_counter() - t0 >= target_s:
+            break
+    dt = time.perf_counter() - t0
+    gbs = reps * sample_bytes(rows) / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of 8192 rows per width, all 10 calls, {reps} repetitions, {dt:.1f} s, "
+                      f"numpy fp64 single-threaded"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    rows = args.ref_rows
+    samples = oracle_samples(rows)
+    for _ in range(args.warmup):
+        oracle_step(samples)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(samples)
+    dt = time.perf_counter() - t0
+    step_ms = dt / args.steps * 1e3
+    gbs = sample_bytes(rows) / (step_ms * 1e-3) / 1e9
+    sample = f"{rows} of 8192 rows per width per step, all 10 calls, numpy fp64 single-threaded"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows_per_step": rows, "widths": [1024, 5120]},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# extra modes: per-config sweep and a single-call loop for profilers
+# ---------------------------------------------------------------------------
+
+SWEEP = [("ln_fwd", 8192, 1024), ("rms_fwd", 8192, 1024), ("ln_bwd", 8192, 1024), ("rms_bwd", 8192, 1024),
+         ("ln_fwd", 8192, 5120), ("rms_fwd", 8192, 5120), ("ln_bwd", 8192, 5120), ("rms_bwd", 8192, 5120),
+         ("fused_fwd", 16384, 4096), ("ln_bwd", 32768, 1024), ("rms_bwd", 32768, 1024), ("ln_bwd", 16384, 2048),
+         ("rms_bwd", 16384, 2048), ("ln_fwd", 2048, 16384), ("rms_fwd", 2048, 16384), ("ln_bwd", 2048, 16384),
+         ("rms_bwd", 2048, 16384), ("ln_fwd", 512, 16384), ("rms_fwd", 512, 16384), ("ln_bwd", 512, 16384),
+         ("rms_bwd", 512, 16384)]
+
+
+def run_sweep(args):
+    import torch
+    from rmsnorm_ln_fwd_gb300 import _build
+    _build.build()
+    import rmsnorm_ln_fwd_gb300 as nl
+    lib = nl.load_library()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    peak, kind = measured_peak()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    cache = {}
+    for op, N, H in SWEEP:
+        if (N, H) not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            cache[(N, H)] = Shape(N, H, dev, seed=7, lib=lib)
+        s = cache[(N, H)]
+        if op.endswith("bwd"):
+            s.call("ln_fwd" if op == "ln_bwd" else "rms_fwd", stream.cuda_stream)
+        for _ in range(5):
+            flush.zero_()
+            s.call(op, stream.cuda_stream)
+        ts = []
+        for _ in range(args.sweep_iters):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            s.call(op, stream.cuda_stream)
+            b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        us = [a.elapsed_time(b) * 1e3 for a, b in ts]
+        byts = alg_bytes(op, N, H)
+        med = statistics.median(us)
+        print(json.dumps({"op": op, "N": N, "H": H, "us_median": round(med, 2), "us_min": round(min(us), 2),
+                          "gbs": round(byts / (med * 1e-6) / 1e9, 1), "frac": round(byts / (med * 1e-6) / 1e9 / peak, 3),
+                          "bytes": byts, "peak": peak, "peak_kind": kind}), flush=True)
+
+
+def run_profile_loop(args):
+    """Run one call `--iters` times (after one untimed forward for a backward):
+    a small, self-terminating target for ncu captures."""
+    import torch
+    from rmsnorm_ln_fwd_gb300 import _build
+    _build.build()
+    import rmsnorm_ln_fwd_gb300 as nl
+    lib = nl.load_library()
+    N, H = (int(v) for v in args.shape.split("x"))
+    dev = torch.device("cuda", 0)
+    s = Shape(N, H, dev, seed=3, lib=lib)
+    sh = torch.cuda.current_stream(dev).cuda_stream
+    op = args.profile_op
+    if op.endswith("bwd"):
+        s.call("ln_fwd" if op == "ln_bwd" else "rms_fwd", sh)
+    for _ in range(args.iters):
+        s.call(op, sh)
+    torch.cuda.synchronize()
+    print(json.dumps({"profiled": op, "N": N, "H": H, "iters": args.iters}))
+
+
+def main():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--cpu-rows", type=int, default=512)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--ref-rows", type=int, default=64)
+    p.add_argument("--sweep", action="store_true", help="per-call timings over every configured shape")
+    p.add_argument("--sweep-iters", type=int, default=50)
+    p.add_argument("--profile-op", choices=list(OPS), default=None)
+    p.add_argument("--shape", default="8192x1024")
+    p.add_argument("--iters", type=int, default=3)
+    args = p.parse_args()
+    if args.impl == "ours" and not (args.sweep or args.profile_op):
+        args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
+    elif args.profile_op:
+        run_profile_loop(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

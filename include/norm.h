@@ -1,0 +1,173 @@
+/*
+ * norm.h -- C ABI of libnorm: row-wise LayerNorm and RMSNorm on one GB300 GPU
+ * (sm_103a): forward, fused residual-add + RMSNorm forward, and the training
+ * backward with gamma/beta gradients.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout.  A "row tensor" is N rows of H elements, row-major, the last
+ *   (normalised) dimension contiguous, consecutive rows `ld` ELEMENTS apart
+ *   (ld >= H).  A (B, T, H) tensor is passed as N = B*T rows.  gamma, beta,
+ *   dgamma and dbeta have shape (H,) and are indexed by column only.  mean and
+ *   rstd have shape (N,), fp32.
+ * Memory.  Every pointer is CUDA device memory owned by the caller (any
+ *   allocator, e.g. PyTorch's).  The library never allocates, frees or keeps a
+ *   pointer after the call returns.
+ * Streams.  Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream) and runs asynchronously; the call returns once the work is
+ *   enqueued.  Outputs are valid after the stream reaches that point.
+ * Dtypes.  `x_dtype` types the row tensors (x, residual, y, h_out, dy, dx);
+ *   `w_dtype` types gamma, beta, dgamma, dbeta and must equal x_dtype or be
+ *   NORM_F32.  All statistics and arithmetic are fp32; stored values are
+ *   rounded to nearest, ties to even.
+ * eps.  Added INSIDE the square root: rstd = 1/sqrt(var + eps).  eps must be
+ *   finite and > 0.
+ * Alignment.  Rows whose pointers and strides are 16-byte aligned take the
+ *   128-bit vector path; anything else is still correct (scalar path).
+ * Errors.  Arguments are validated on the host before anything is enqueued;
+ *   an invalid call returns an error and enqueues nothing.  A failed launch
+ *   returns NORM_ERR_CUDA.  No entry point aborts, throws or prints.
+ * Threads.  Every entry point is thread-safe; the only library state is a
+ *   per-device cache of device attributes.
+ *
+ * Sources: "Skill: Write a Triton LayerNorm Kernel", "Skill: Write CUDA
+ * LayerNorm Kernel", "Skill: Write a Triton Fused Add+RMSNorm Kernel" and the
+ * Fast-LLM pull request "Rewrite Triton normalization backward kernel_1
+ * (#499)".  Each declaration names the section it implements.
+ */
+#ifndef NORM_H_
+#define NORM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* norm_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  NORM_OK = 0,
+  NORM_ERR_INVALID_VALUE = 1, /* bad size, stride, eps, null or overlapping pointer */
+  NORM_ERR_UNSUPPORTED = 2,   /* dtype combination not provided */
+  NORM_ERR_WORKSPACE = 3,     /* backward workspace missing, too small or misaligned */
+  NORM_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
+} norm_status;
+
+typedef enum { NORM_F32 = 0, NORM_BF16 = 1 } norm_dtype;
+
+/*
+ * LayerNorm forward.  "Skill: Write a Triton LayerNorm Kernel", Required
+ * reasoning process steps 1-10; "Skill: Write CUDA LayerNorm Kernel", steps
+ * 1-7 (Welford statistics with the parallel merge, eps inside rsqrt):
+ *   mean = sum_j x_j / H,  var = sum_j (x_j - mean)^2 / H  (biased),
+ *   rstd = 1/sqrt(var + eps),  y_j = (x_j - mean) * rstd * gamma_j + beta_j.
+ * x     [N x ldx]  input rows.
+ * gamma [H] or NULL (= all ones);  beta [H] or NULL (= all zeros).
+ * y     [N x ldy]  output rows.  May be exactly x (same pointer and stride) for
+ *                  an in-place call; any other overlap with x is rejected.
+ * mean, rstd [N] fp32 or NULL: the statistics saved for the backward.
+ * N >= 0, H >= 1.  N == 0 enqueues nothing, and then every row and statistics
+ * pointer may be NULL.
+ */
+norm_status ln_forward(const void* x, int64_t ldx, const void* gamma, const void* beta,
+                       void* y, int64_t ldy, float* mean, float* rstd,
+                       int64_t N, int64_t H, float eps,
+                       norm_dtype x_dtype, norm_dtype w_dtype, norm_stream_t stream);
+
+/*
+ * RMSNorm forward.  "Skill: Write CUDA LayerNorm Kernel", Kernel design rules
+ * (RMSNorm); "Skill: Write a Triton LayerNorm Kernel", step 5:
+ *   rstd = 1/sqrt(sum_j x_j^2 / H + eps),  y_j = x_j * rstd * gamma_j.
+ * No mean subtraction and no beta.  Arguments as in ln_forward; rstd may be
+ * NULL.
+ */
+norm_status rms_forward(const void* x, int64_t ldx, const void* gamma,
+                        void* y, int64_t ldy, float* rstd,
+                        int64_t N, int64_t H, float eps,
+                        norm_dtype x_dtype, norm_dtype w_dtype, norm_stream_t stream);
+
+/*
+ * Fused residual add + RMSNorm forward.  "Skill: Write a Triton Fused
+ * Add+RMSNorm Kernel", Required reasoning process steps 1-9:
+ *   h = x + residual formed in fp32;  h_out = h rounded to x_dtype;
+ *   rstd = 1/sqrt(sum_j h_j^2 / H + eps);  y_j = h_j * rstd * gamma_j, with y
+ *   computed from the fp32 h, not from the rounded h_out.
+ * x [N x ldx], residual [N x ldr]: inputs.
+ * h_out [N x ldh]: the summed residual stream.  It may be exactly x or exactly
+ *   residual (same pointer and stride: in-place update); any other overlap is
+ *   rejected.
+ * y [N x ldy]: must not overlap x, residual or h_out.
+ * rstd [N] fp32 or NULL (saved for training).
+ */
+norm_status fused_add_rms_forward(const void* x, int64_t ldx, const void* residual, int64_t ldr,
+                                  const void* gamma, void* y, int64_t ldy,
+                                  void* h_out, int64_t ldh, float* rstd,
+                                  int64_t N, int64_t H, float eps,
+                                  norm_dtype x_dtype, norm_dtype w_dtype, norm_stream_t stream);
+
+/*
+ * Bytes of device workspace the backward needs for a row width H on CUDA
+ * device `device`: the bounded fp32 partial buffer for dgamma/dbeta of
+ * "Rewrite Triton normalization backward kernel_1 (#499)", Summary item 2
+ * (a fixed number of partial rows tied to the SM count, independent of N).
+ * Returns 0 if H < 1 or the device cannot be queried.
+ */
+size_t norm_bwd_workspace_bytes(int64_t H, int device);
+
+/*
+ * LayerNorm backward.  "Skill: Write CUDA LayerNorm Kernel", step 8, with
+ * g_j = dy_j * gamma_j and x_hat_j = (x_j - mean) * rstd:
+ *   dx_j     = rstd/H * (H*g_j - sum(g) - x_hat_j * sum(g * x_hat)),
+ *   dgamma_j = sum over all N rows of dy_j * x_hat_j,
+ *   dbeta_j  = sum over all N rows of dy_j.
+ * Rows are grid-strided over a CTA count tied to the SM count; each CTA folds
+ * its rows into one fp32 partial row in `workspace`, and a second kernel sums
+ * the partials and casts once to w_dtype ("Rewrite Triton normalization
+ * backward kernel_1 (#499)", Summary items 1-2).
+ * dy [N x lddy], x [N x ldx]: inputs.  mean, rstd [N] fp32: the forward's
+ *   saved statistics (required).
+ * gamma [H] or NULL (= ones).
+ * dx [N x lddx]: output; may be exactly dy (in place); must not overlap x.
+ * dgamma, dbeta [H] in w_dtype, or NULL to skip that gradient.  They are
+ *   overwritten, not accumulated into.  With N == 0 they are set to zero, the
+ *   row and statistics pointers may be NULL and no workspace is needed.
+ * workspace: device memory of at least norm_bwd_workspace_bytes(H, device)
+ *   bytes, 16-byte aligned; needed only when dgamma or dbeta is non-NULL.  Its
+ *   contents need no initialisation and are undefined afterwards.  Calls that
+ *   share one workspace must be ordered on the GPU (e.g. one stream).
+ */
+norm_status ln_backward(const void* dy, int64_t lddy, const void* x, int64_t ldx,
+                        const float* mean, const float* rstd, const void* gamma,
+                        void* dx, int64_t lddx, void* dgamma, void* dbeta,
+                        void* workspace, size_t workspace_bytes,
+                        int64_t N, int64_t H,
+                        norm_dtype x_dtype, norm_dtype w_dtype, norm_stream_t stream);
+
+/*
+ * RMSNorm backward (derived from the RMSNorm forward; no page prints it):
+ * with g_j = dy_j * gamma_j and x_hat_j = x_j * rstd,
+ *   dx_j     = rstd * (g_j - x_hat_j * sum(g * x_hat) / H),
+ *   dgamma_j = sum over all N rows of dy_j * x_hat_j.
+ * Arguments as in ln_backward, without mean and dbeta.
+ */
+norm_status rms_backward(const void* dy, int64_t lddy, const void* x, int64_t ldx,
+                         const float* rstd, const void* gamma,
+                         void* dx, int64_t lddx, void* dgamma,
+                         void* workspace, size_t workspace_bytes,
+                         int64_t N, int64_t H,
+                         norm_dtype x_dtype, norm_dtype w_dtype, norm_stream_t stream);
+
+/* A static, human-readable name for a status code (never NULL). */
+const char* norm_status_str(norm_status status);
+
+/* Version of this ABI: major*10000 + minor*100 + patch. */
+int norm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NORM_H_ */

@@ -1,0 +1,239 @@
+// Device helpers shared by the forward and backward kernels of libnorm.
+//
+// Everything here is bandwidth plumbing: 128-bit global loads/stores, bf16
+// packing, warp-shuffle reductions and the parallel Welford merge.  The
+// normalisation arithmetic itself lives in norm_fwd.cu / norm_bwd.cu.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace normk {
+
+// Element types.  VEC = elements per 16-byte vector.
+struct F32 {
+  using T = float;
+  static constexpr int VEC = 4;
+};
+struct BF16 {
+  using T = __nv_bfloat16;
+  static constexpr int VEC = 8;
+};
+
+// ---------------------------------------------------------------------------
+// 16-byte global memory access.  Streamed row data is read with an L1
+// no-allocate hint (each byte is used once per kernel) and a 256-byte L2
+// prefetch hint; parameters (gamma, beta) use the default cached path because
+// every row reuses them.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ld_cached(const void* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+__device__ __forceinline__ void st_vec(void* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Packing: a 16-byte vector <-> VEC fp32 values (element 0 in the low bits).
+// bf16 -> fp32 is exact (a shift); fp32 -> bf16 rounds to nearest even.
+// ---------------------------------------------------------------------------
+template <typename D>
+__device__ __forceinline__ void unpack(const uint4& u, float* f);
+
+template <>
+__device__ __forceinline__ void unpack<F32>(const uint4& u, float* f) {
+  f[0] = __uint_as_float(u.x);
+  f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z);
+  f[3] = __uint_as_float(u.w);
+}
+
+template <>
+__device__ __forceinline__ void unpack<BF16>(const uint4& u, float* f) {
+  f[0] = __uint_as_float(u.x << 16);
+  f[1] = __uint_as_float(u.x & 0xffff0000u);
+  f[2] = __uint_as_float(u.y << 16);
+  f[3] = __uint_as_float(u.y & 0xffff0000u);
+  f[4] = __uint_as_float(u.z << 16);
+  f[5] = __uint_as_float(u.z & 0xffff0000u);
+  f[6] = __uint_as_float(u.w << 16);
+  f[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+template <typename D>
+__device__ __forceinline__ uint4 pack(const float* f);
+
+template <>
+__device__ __forceinline__ uint4 pack<F32>(const float* f) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                    __float_as_uint(f[3]));
+}
+
+template <>
+__device__ __forceinline__ uint4 pack<BF16>(const float* f) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+// Scalar element access (tails and the unaligned path).
+template <typename D>
+__device__ __forceinline__ float load_elem(const void* base, int64_t i) {
+  if constexpr (sizeof(typename D::T) == 4) {
+    return reinterpret_cast<const float*>(base)[i];
+  } else {
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
+  }
+}
+
+template <typename D>
+__device__ __forceinline__ void store_elem(void* base, int64_t i, float v) {
+  if constexpr (sizeof(typename D::T) == 4) {
+    reinterpret_cast<float*>(base)[i] = v;
+  } else {
+    reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+  }
+}
+
+// Parameter element (gamma/beta): fp32 or the row dtype, chosen at run time.
+template <typename D>
+__device__ __forceinline__ float load_param(const void* p, int i, bool w_f32) {
+  return w_f32 ? reinterpret_cast<const float*>(p)[i] : load_elem<D>(p, i);
+}
+
+// Whole 16-byte vectors of a row (the register path requires H % VEC == 0,
+// so a vector is either entirely inside the row or entirely past its end).
+template <typename D>
+__device__ __forceinline__ uint4 load_vec_or_zero(const void* row, int c, int H) {
+  return c < H ? ld_stream(reinterpret_cast<const typename D::T*>(row) + c) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+template <typename D>
+__device__ __forceinline__ void store_vec(void* row, int c, const float* f) {
+  st_vec(reinterpret_cast<typename D::T*>(row) + c, pack<D>(f));
+}
+
+// gamma/beta for the full vector at column c: p == nullptr gives `fill` (1 for
+// gamma, 0 for beta).  Cached 16-byte loads: every row reuses them.
+template <typename D>
+__device__ __forceinline__ void load_param_vec(const void* p, int c, bool w_f32, float fill, float* f) {
+  constexpr int VEC = D::VEC;
+  if (p == nullptr) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) f[i] = fill;
+  } else if (w_f32) {
+    const float* q = reinterpret_cast<const float*>(p) + c;
+#pragma unroll
+    for (int k = 0; k < VEC / 4; ++k) unpack<F32>(ld_cached(q + 4 * k), f + 4 * k);
+  } else {
+    unpack<D>(ld_cached(reinterpret_cast<const typename D::T*>(p) + c), f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Reductions.  Every lane of a warp (and every thread of a row group) ends
+// with bit-identical results: the butterfly adds are commutative, the Welford
+// merge is evaluated with the lower-indexed partner as its left operand, and
+// cross-warp partials are folded in warp order.
+// ---------------------------------------------------------------------------
+template <int K>
+__device__ __forceinline__ void warp_sum(float (&v)[K]) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], off);
+  }
+}
+
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Sum K values over the `nw` warps of one row group.  `sh` holds 2*nw*K floats
+// private to the group; `parity` alternates per row so one barrier per row is
+// enough (a buffer is rewritten only after the next row's barrier).
+template <int K>
+__device__ __forceinline__ void group_sum(float (&v)[K], float* sh, int nw, int wig, int lane,
+                                          int bar_id, int parity) {
+  warp_sum<K>(v);
+  if (nw == 1) return;
+  float* buf = sh + parity * nw * K;
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) buf[wig * K + k] = v[k];
+  }
+  named_barrier(bar_id, nw * 32);
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    float s = buf[k];
+    for (int w = 1; w < nw; ++w) s += buf[w * K + k];
+    v[k] = s;
+  }
+}
+
+// Welford accumulator (count, mean, M2) and the parallel merge of
+// "Skill: Write CUDA LayerNorm Kernel", Required reasoning process step 3:
+// n = na + nb, delta = mb - ma, mean = ma + delta*nb/n,
+// M2 = M2a + M2b + delta^2*na*nb/n; count 0 is the identity.
+struct Welford {
+  float n, m, m2;
+};
+
+__device__ __forceinline__ Welford welford_merge(const Welford& a, const Welford& b) {
+  const float n = a.n + b.n;
+  if (n == 0.f) return a;
+  const float wb = b.n / n;
+  const float d = b.m - a.m;
+  Welford r;
+  r.n = n;
+  r.m = fmaf(d, wb, a.m);
+  r.m2 = a.m2 + b.m2 + d * d * a.n * wb;
+  return r;
+}
+
+__device__ __forceinline__ Welford warp_welford(Welford w, int lane) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    Welford o;
+    o.n = __shfl_xor_sync(0xffffffffu, w.n, off);
+    o.m = __shfl_xor_sync(0xffffffffu, w.m, off);
+    o.m2 = __shfl_xor_sync(0xffffffffu, w.m2, off);
+    w = (lane & off) ? welford_merge(o, w) : welford_merge(w, o);
+  }
+  return w;
+}
+
+// Welford merge over the warps of a row group, same buffering as group_sum.
+__device__ __forceinline__ Welford group_welford(Welford w, float* sh, int nw, int wig, int lane,
+                                                 int bar_id, int parity) {
+  w = warp_welford(w, lane);
+  if (nw == 1) return w;
+  float* buf = sh + parity * nw * 3;
+  if (lane == 0) {
+    buf[wig * 3 + 0] = w.n;
+    buf[wig * 3 + 1] = w.m;
+    buf[wig * 3 + 2] = w.m2;
+  }
+  named_barrier(bar_id, nw * 32);
+  Welford acc{buf[0], buf[1], buf[2]};
+  for (int k = 1; k < nw; ++k) acc = welford_merge(acc, Welford{buf[3 * k], buf[3 * k + 1], buf[3 * k + 2]});
+  return acc;
+}
+
+}  // namespace normk

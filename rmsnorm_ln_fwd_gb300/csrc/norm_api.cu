@@ -1,0 +1,280 @@
+// The C ABI declared in include/norm.h: host-side argument validation, the
+// per-device attribute cache, and dispatch to the kernel launchers.
+//
+// Validation happens entirely on the host and before anything is enqueued, so
+// an invalid call has no effect on the GPU.  No entry point throws, aborts or
+// allocates.
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "launch.h"
+#include "norm.h"
+
+using normk::BwdArgs;
+using normk::DeviceInfo;
+using normk::FwdArgs;
+
+namespace {
+
+constexpr int64_t kMaxH = int64_t(1) << 24;  // counts stay exact in fp32
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mu;
+DeviceInfo g_info[kMaxDevices];
+bool g_have[kMaxDevices];
+
+bool device_info(int dev, DeviceInfo* out) {
+  if (dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_have[dev]) {
+    DeviceInfo d{};
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaSuccess)
+      return false;
+    if (d.sm_count < 1) return false;
+    g_info[dev] = d;
+    g_have[dev] = true;
+  }
+  *out = g_info[dev];
+  return true;
+}
+
+bool current_device_info(DeviceInfo* out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  return device_info(dev, out);
+}
+
+size_t elem_size(norm_dtype d) { return d == NORM_BF16 ? 2 : 4; }
+
+norm_status check_dtypes(norm_dtype x, norm_dtype w) {
+  const bool xv = x == NORM_F32 || x == NORM_BF16;
+  const bool wv = w == NORM_F32 || w == NORM_BF16;
+  if (!xv || !wv) return NORM_ERR_UNSUPPORTED;
+  if (w != x && w != NORM_F32) return NORM_ERR_UNSUPPORTED;
+  return NORM_OK;
+}
+
+bool shape_ok(int64_t N, int64_t H) { return N >= 0 && H >= 1 && H <= kMaxH; }
+
+bool eps_ok(float eps) { return std::isfinite(eps) && eps > 0.f; }
+
+// The byte range [lo, hi) touched by N rows of H elements, `ld` apart.
+struct Span {
+  uintptr_t lo, hi;
+};
+
+// ld >= H and the extent (N-1)*ld + H elements fits comfortably in 63 bits.
+bool ld_ok(int64_t ld, int64_t N, int64_t H, size_t es) {
+  if (ld < H) return false;
+  if (N <= 1) return true;
+  const int64_t limit = (INT64_MAX / 8) / (int64_t)es;
+  return (N - 1) <= (limit - H) / ld;
+}
+
+Span rows_span(const void* p, int64_t N, int64_t ld, int64_t H, size_t es) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  const uint64_t n = N == 0 ? 0 : (uint64_t)((N - 1) * ld + H) * es;
+  return Span{lo, lo + n};
+}
+
+Span vec_span(const void* p, int64_t n, size_t es) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Span{lo, lo + (uint64_t)n * es};
+}
+
+bool overlap(const Span& a, const Span& b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo; }
+
+// Two row tensors may be the same buffer (same pointer and stride) or
+// disjoint; anything in between is a partial overlap.
+bool same_or_disjoint(const void* p, int64_t ldp, const void* q, int64_t ldq, int64_t N, int64_t H, size_t es) {
+  if (p == q && ldp == ldq) return true;
+  return !overlap(rows_span(p, N, ldp, H, es), rows_span(q, N, ldq, H, es));
+}
+
+bool disjoint_rows(const void* p, int64_t ldp, const void* q, int64_t ldq, int64_t N, int64_t H, size_t es) {
+  return !overlap(rows_span(p, N, ldp, H, es), rows_span(q, N, ldq, H, es));
+}
+
+norm_status launch_result(cudaError_t e) { return e == cudaSuccess ? NORM_OK : NORM_ERR_CUDA; }
+
+normk::Dtype to_dt(norm_dtype d) { return d == NORM_BF16 ? normk::DT_BF16 : normk::DT_F32; }
+
+norm_status forward_common(int kind, const void* x, int64_t ldx, const void* res, int64_t ldr,
+                           const void* gamma, const void* beta, void* y, int64_t ldy, void* h,
+                           int64_t ldh, float* mean, float* rstd, int64_t N, int64_t H, float eps,
+                           norm_dtype xd, norm_dtype wd, norm_stream_t stream) {
+  norm_status st = check_dtypes(xd, wd);
+  if (st != NORM_OK) return st;
+  if (!shape_ok(N, H) || !eps_ok(eps)) return NORM_ERR_INVALID_VALUE;
+  if (N == 0) return NORM_OK;  // nothing to read or write; pointers may be NULL
+  if (x == nullptr || y == nullptr) return NORM_ERR_INVALID_VALUE;
+  const size_t es = elem_size(xd);
+  if (!ld_ok(ldx, N, H, es) || !ld_ok(ldy, N, H, es)) return NORM_ERR_INVALID_VALUE;
+  const bool fused = kind == normk::KIND_FUSED;
+  if (fused) {
+    if (res == nullptr || h == nullptr) return NORM_ERR_INVALID_VALUE;
+    if (!ld_ok(ldr, N, H, es) || !ld_ok(ldh, N, H, es)) return NORM_ERR_INVALID_VALUE;
+    // y is a fresh output: disjoint from every other row tensor.
+    if (!disjoint_rows(y, ldy, x, ldx, N, H, es) || !disjoint_rows(y, ldy, res, ldr, N, H, es) ||
+        !disjoint_rows(y, ldy, h, ldh, N, H, es))
+      return NORM_ERR_INVALID_VALUE;
+    // h may replace x or residual in place; then the other input must be that
+    // same buffer too or stay clear of it.
+    if (!same_or_disjoint(h, ldh, x, ldx, N, H, es) || !same_or_disjoint(h, ldh, res, ldr, N, H, es))
+      return NORM_ERR_INVALID_VALUE;
+  } else {
+    if (!same_or_disjoint(y, ldy, x, ldx, N, H, es)) return NORM_ERR_INVALID_VALUE;
+  }
+  if (mean && rstd && overlap(vec_span(mean, N, 4), vec_span(rstd, N, 4))) return NORM_ERR_INVALID_VALUE;
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return NORM_ERR_CUDA;
+  FwdArgs a{};
+  a.x = x;
+  a.ldx = ldx;
+  a.res = res;
+  a.ldr = ldr;
+  a.gamma = gamma;
+  a.beta = beta;
+  a.y = y;
+  a.ldy = ldy;
+  a.h = h;
+  a.ldh = ldh;
+  a.mean = mean;
+  a.rstd = rstd;
+  a.N = N;
+  a.H = (int)H;
+  a.eps = eps;
+  a.w_f32 = wd == NORM_F32;
+  a.h_alias = fused && ((h == x && ldh == ldx) || (h == res && ldh == ldr));
+  return launch_result(normk::launch_forward(kind, to_dt(xd), a, dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t workspace_bytes_for(int64_t H, const DeviceInfo& dev) {
+  return 2 * (size_t)normk::bwd_max_partials(dev) * (size_t)normk::bwd_partial_stride((int)H) * sizeof(float);
+}
+
+norm_status backward_common(int kind, const void* dy, int64_t lddy, const void* x, int64_t ldx,
+                            const float* mean, const float* rstd, const void* gamma, void* dx,
+                            int64_t lddx, void* dgamma, void* dbeta, void* ws, size_t ws_bytes,
+                            int64_t N, int64_t H, norm_dtype xd, norm_dtype wd, norm_stream_t stream) {
+  norm_status st = check_dtypes(xd, wd);
+  if (st != NORM_OK) return st;
+  if (!shape_ok(N, H)) return NORM_ERR_INVALID_VALUE;
+  const size_t es = elem_size(xd);
+  const size_t wes = elem_size(wd);
+  if (dgamma && dbeta && overlap(vec_span(dgamma, H, wes), vec_span(dbeta, H, wes))) return NORM_ERR_INVALID_VALUE;
+  if (N == 0) {
+    // A sum over no rows: the parameter gradients are zero.  No workspace.
+    DeviceInfo dev;
+    if (!current_device_info(&dev)) return NORM_ERR_CUDA;
+    BwdArgs a{};
+    a.N = 0;
+    a.H = (int)H;
+    a.w_f32 = wd == NORM_F32;
+    return launch_result(normk::launch_backward(kind, to_dt(xd), a, dgamma, dbeta, dev,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+  }
+  if (dy == nullptr || x == nullptr || dx == nullptr || rstd == nullptr) return NORM_ERR_INVALID_VALUE;
+  if (kind == normk::KIND_LN && mean == nullptr) return NORM_ERR_INVALID_VALUE;
+  if (!ld_ok(lddy, N, H, es) || !ld_ok(ldx, N, H, es) || !ld_ok(lddx, N, H, es)) return NORM_ERR_INVALID_VALUE;
+  if (!disjoint_rows(dx, lddx, x, ldx, N, H, es) || !same_or_disjoint(dx, lddx, dy, lddy, N, H, es))
+    return NORM_ERR_INVALID_VALUE;
+  const Span sdx = rows_span(dx, N, lddx, H, es);
+  if (dgamma && overlap(vec_span(dgamma, H, wes), sdx)) return NORM_ERR_INVALID_VALUE;
+  if (dbeta && overlap(vec_span(dbeta, H, wes), sdx)) return NORM_ERR_INVALID_VALUE;
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return NORM_ERR_CUDA;
+  const bool want = dgamma != nullptr || dbeta != nullptr;
+  if (want) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 15u) != 0) return NORM_ERR_WORKSPACE;
+    if (ws_bytes < workspace_bytes_for(H, dev)) return NORM_ERR_WORKSPACE;
+    const Span sws = Span{reinterpret_cast<uintptr_t>(ws), reinterpret_cast<uintptr_t>(ws) + ws_bytes};
+    if (overlap(sws, sdx) || (dgamma && overlap(sws, vec_span(dgamma, H, wes))) ||
+        (dbeta && overlap(sws, vec_span(dbeta, H, wes))))
+      return NORM_ERR_WORKSPACE;
+  }
+  BwdArgs a{};
+  a.dy = dy;
+  a.lddy = lddy;
+  a.x = x;
+  a.ldx = ldx;
+  a.mean = mean;
+  a.rstd = rstd;
+  a.gamma = gamma;
+  a.dx = dx;
+  a.lddx = lddx;
+  a.ws = static_cast<float*>(ws);
+  a.N = N;
+  a.H = (int)H;
+  a.w_f32 = wd == NORM_F32;
+  return launch_result(normk::launch_backward(kind, to_dt(xd), a, dgamma, dbeta, dev,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+norm_status ln_forward(const void* x, int64_t ldx, const void* gamma, const void* beta, void* y, int64_t ldy,
+                       float* mean, float* rstd, int64_t N, int64_t H, float eps, norm_dtype x_dtype,
+                       norm_dtype w_dtype, norm_stream_t stream) {
+  return forward_common(normk::KIND_LN, x, ldx, nullptr, 0, gamma, beta, y, ldy, nullptr, 0, mean, rstd, N, H,
+                        eps, x_dtype, w_dtype, stream);
+}
+
+norm_status rms_forward(const void* x, int64_t ldx, const void* gamma, void* y, int64_t ldy, float* rstd,
+                        int64_t N, int64_t H, float eps, norm_dtype x_dtype, norm_dtype w_dtype,
+                        norm_stream_t stream) {
+  return forward_common(normk::KIND_RMS, x, ldx, nullptr, 0, gamma, nullptr, y, ldy, nullptr, 0, nullptr, rstd,
+                        N, H, eps, x_dtype, w_dtype, stream);
+}
+
+norm_status fused_add_rms_forward(const void* x, int64_t ldx, const void* residual, int64_t ldr,
+                                  const void* gamma, void* y, int64_t ldy, void* h_out, int64_t ldh,
+                                  float* rstd, int64_t N, int64_t H, float eps, norm_dtype x_dtype,
+                                  norm_dtype w_dtype, norm_stream_t stream) {
+  return forward_common(normk::KIND_FUSED, x, ldx, residual, ldr, gamma, nullptr, y, ldy, h_out, ldh, nullptr,
+                        rstd, N, H, eps, x_dtype, w_dtype, stream);
+}
+
+size_t norm_bwd_workspace_bytes(int64_t H, int device) {
+  if (H < 1 || H > kMaxH) return 0;
+  DeviceInfo dev;
+  if (!device_info(device, &dev)) return 0;
+  return workspace_bytes_for(H, dev);
+}
+
+norm_status ln_backward(const void* dy, int64_t lddy, const void* x, int64_t ldx, const float* mean,
+                        const float* rstd, const void* gamma, void* dx, int64_t lddx, void* dgamma, void* dbeta,
+                        void* workspace, size_t workspace_bytes, int64_t N, int64_t H, norm_dtype x_dtype,
+                        norm_dtype w_dtype, norm_stream_t stream) {
+  return backward_common(normk::KIND_LN, dy, lddy, x, ldx, mean, rstd, gamma, dx, lddx, dgamma, dbeta, workspace,
+                         workspace_bytes, N, H, x_dtype, w_dtype, stream);
+}
+
+norm_status rms_backward(const void* dy, int64_t lddy, const void* x, int64_t ldx, const float* rstd,
+                         const void* gamma, void* dx, int64_t lddx, void* dgamma, void* workspace,
+                         size_t workspace_bytes, int64_t N, int64_t H, norm_dtype x_dtype, norm_dtype w_dtype,
+                         norm_stream_t stream) {
+  return backward_common(normk::KIND_RMS, dy, lddy, x, ldx, nullptr, rstd, gamma, dx, lddx, dgamma, nullptr,
+                         workspace, workspace_bytes, N, H, x_dtype, w_dtype, stream);
+}
+
+const char* norm_status_str(norm_status status) {
+  switch (status) {
+    case NORM_OK: return "NORM_OK";
+    case NORM_ERR_INVALID_VALUE: return "NORM_ERR_INVALID_VALUE: bad size, stride, eps, null or overlapping pointer";
+    case NORM_ERR_UNSUPPORTED: return "NORM_ERR_UNSUPPORTED: dtype combination not provided";
+    case NORM_ERR_WORKSPACE: return "NORM_ERR_WORKSPACE: backward workspace missing, too small or misaligned";
+    case NORM_ERR_CUDA: return "NORM_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+  }
+  return "NORM_ERR_UNKNOWN";
+}
+
+int norm_abi_version(void) { return 10000; }
+
+}  // extern "C"

@@ -1,0 +1,387 @@
+// Backward kernels: LayerNorm and RMSNorm grad_input plus the gamma/beta
+// gradients through a bounded fp32 partial reduction.
+//
+// Math ("Skill: Write CUDA LayerNorm Kernel", Required reasoning process
+// step 8; the RMSNorm form is derived from its forward):
+//   g = dy * gamma,  x_hat = (x - mean) * rstd   (RMSNorm: x * rstd)
+//   LayerNorm: dx = rstd * (g - sum(g)/H - x_hat * sum(g*x_hat)/H)
+//   RMSNorm:   dx = rstd * (g - x_hat * sum(g*x_hat)/H)
+//   dgamma = sum over rows of dy * x_hat,  dbeta = sum over rows of dy.
+// The saved fp32 mean can sit half an fp32 ulp away from the true mean; for
+// rows with a large common offset that is a visible constant shift of x_hat.
+// Because mean(x_hat) = 0 exactly, the kernel also sums x_hat and subtracts
+// its row mean, which removes that shift (one extra value in the same
+// reduction).
+//
+// Structure ("Rewrite Triton normalization backward kernel_1 (#499)",
+// Summary items 1-2): a fixed grid of P = 2 x SM-count CTAs grid-strides the
+// rows.  Each thread owns fixed columns, so its dgamma/dbeta accumulators stay
+// in fp32 registers across all rows it visits; at the end each CTA folds its
+// row groups into ONE partial row.  The partial buffer is therefore P x H,
+// independent of N, and a second small kernel sums it column-wise, casting to
+// the parameter dtype once at the store.
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace normk {
+
+int bwd_max_partials(const DeviceInfo& dev) { return 2 * dev.sm_count; }
+
+template <int KIND, typename D, int VPT, int MAXT>
+__global__ void __launch_bounds__(MAXT) bwd_reg_kernel(const BwdArgs a) {
+  using T = typename D::T;
+  constexpr int VEC = D::VEC;
+  constexpr bool LN = KIND == KIND_LN;
+  constexpr int NS = LN ? 3 : 1;  // values per row reduction
+  extern __shared__ __align__(16) float sh_dyn[];
+  const int tpr = a.tpr;
+  const int rpc = blockDim.x / tpr;
+  const int slot = threadIdx.x / tpr;
+  const int t = threadIdx.x - slot * tpr;
+  const int nw = tpr >> 5;
+  const int wig = t >> 5;
+  const int lane = threadIdx.x & 31;
+  const int H = a.H;
+  const float inv_h = 1.f / (float)H;
+  const bool w_f32 = a.w_f32 != 0;
+  float* sh = sh_dyn + slot * (2 * nw * NS);
+  const int bar_id = 1 + slot;
+  const int64_t stride = (int64_t)gridDim.x * rpc;
+  int parity = 0;
+
+  float acc_g[VPT][VEC], acc_b[VPT][VEC];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) acc_g[v][i] = acc_b[v][i] = 0.f;
+
+  for (int64_t row = (int64_t)blockIdx.x * rpc + slot; row < a.N; row += stride) {
+    const T* xrow = reinterpret_cast<const T*>(a.x) + row * a.ldx;
+    const T* dyrow = reinterpret_cast<const T*>(a.dy) + row * a.lddy;
+    // x and dy stay packed in registers between the two passes over the row.
+    uint4 xr[VPT], dr[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = (v * tpr + t) * VEC;
+      xr[v] = load_vec_or_zero<D>(xrow, c, H);
+      dr[v] = load_vec_or_zero<D>(dyrow, c, H);
+    }
+    const float r = a.rstd[row];
+    const float mu = LN ? a.mean[row] : 0.f;
+
+    // Pass 1: sum(g), sum(g*x_hat) and (LayerNorm) sum(x_hat).
+    float S[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) S[k] = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = (v * tpr + t) * VEC;
+      if (c >= H) continue;
+      float xv[VEC], dv[VEC], gm[VEC];
+      unpack<D>(xr[v], xv);
+      unpack<D>(dr[v], dv);
+      load_param_vec<D>(a.gamma, c, w_f32, 1.f, gm);
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const float xh = LN ? (xv[i] - mu) * r : xv[i] * r;
+        const float g = __fmul_rn(dv[i], gm[i]);  // rounded once: both passes see the same g
+        if (LN) {
+          S[0] += g;
+          S[1] = fmaf(g, xh, S[1]);
+          S[2] += xh;
+        } else {
+          S[0] = fmaf(g, xh, S[0]);
+        }
+      }
+    }
+    group_sum<NS>(S, sh, nw, wig, lane, bar_id, parity);
+
+    // Pass 2: dx and the parameter-gradient accumulators.
+    T* dxrow = reinterpret_cast<T*>(a.dx) + row * a.lddx;
+    const float s0 = LN ? S[2] * inv_h : 0.f;  // row mean of x_hat: removes the mean's rounding shift
+    const float c1 = LN ? S[0] * inv_h : 0.f;
+    const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = (v * tpr + t) * VEC;
+      if (c >= H) continue;
+      float xv[VEC], dv[VEC], gm[VEC], out[VEC];
+      unpack<D>(xr[v], xv);
+      unpack<D>(dr[v], dv);
+      load_param_vec<D>(a.gamma, c, w_f32, 1.f, gm);
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const float xc = LN ? (xv[i] - mu) * r - s0 : xv[i] * r;
+        const float g = __fmul_rn(dv[i], gm[i]);  // rounded once: both passes see the same g
+        out[i] = r * (g - c1 - xc * c2);
+        acc_g[v][i] = fmaf(dv[i], xc, acc_g[v][i]);
+        if (LN) acc_b[v][i] += dv[i];
+      }
+      store_vec<D>(dxrow, c, out);
+    }
+    parity ^= 1;
+  }
+
+  if (a.ws == nullptr) return;
+  // Fold the CTA's row groups into partial row blockIdx.x.  Columns a thread
+  // never visited hold zeros.
+  const int Hp = a.Hp;
+  float* pg = a.ws + (size_t)blockIdx.x * Hp;
+  float* pb = a.ws + ((size_t)gridDim.x + blockIdx.x) * Hp;
+  if (rpc == 1) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = (v * tpr + t) * VEC;
+      if (c >= H) continue;
+#pragma unroll
+      for (int k = 0; k < VEC / 4; ++k) {
+        *reinterpret_cast<float4*>(pg + c + 4 * k) =
+            make_float4(acc_g[v][4 * k], acc_g[v][4 * k + 1], acc_g[v][4 * k + 2], acc_g[v][4 * k + 3]);
+        if (LN)
+          *reinterpret_cast<float4*>(pb + c + 4 * k) =
+              make_float4(acc_b[v][4 * k], acc_b[v][4 * k + 1], acc_b[v][4 * k + 2], acc_b[v][4 * k + 3]);
+      }
+    }
+    return;
+  }
+  const int red_off = ((rpc * 2 * nw * NS) + 3) & ~3;
+  float* red_g = sh_dyn + red_off;
+  float* red_b = red_g + Hp;
+  for (int s2 = 0; s2 < rpc; ++s2) {
+    if (slot == s2) {
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int c = (v * tpr + t) * VEC;
+        if (c >= H) continue;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+          red_g[c + i] = s2 == 0 ? acc_g[v][i] : red_g[c + i] + acc_g[v][i];
+          if (LN) red_b[c + i] = s2 == 0 ? acc_b[v][i] : red_b[c + i] + acc_b[v][i];
+        }
+      }
+    }
+    __syncthreads();
+  }
+  for (int k = threadIdx.x * 4; k < H; k += blockDim.x * 4) {
+    *reinterpret_cast<float4*>(pg + k) = *reinterpret_cast<const float4*>(red_g + k);
+    if (LN) *reinterpret_cast<float4*>(pb + k) = *reinterpret_cast<const float4*>(red_b + k);
+  }
+}
+
+constexpr int LOOP_THREADS = 256;
+
+// Any H, any alignment: one row per CTA iteration, two passes over the row.
+// The CTA's partial row lives in the workspace; column j is always handled by
+// thread j % LOOP_THREADS, so its read-modify-writes never race.
+template <int KIND, typename D>
+__global__ void __launch_bounds__(LOOP_THREADS) bwd_loop_kernel(const BwdArgs a) {
+  using T = typename D::T;
+  constexpr bool LN = KIND == KIND_LN;
+  constexpr int NS = LN ? 3 : 1;
+  constexpr int NW = LOOP_THREADS / 32;
+  __shared__ float sh[2 * NW * NS];
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  const int wig = t >> 5;
+  const int H = a.H;
+  const float inv_h = 1.f / (float)H;
+  const bool w_f32 = a.w_f32 != 0;
+  float* pg = a.ws ? a.ws + (size_t)blockIdx.x * a.Hp : nullptr;
+  float* pb = a.ws ? a.ws + ((size_t)gridDim.x + blockIdx.x) * a.Hp : nullptr;
+  if (pg) {
+    for (int j = t; j < a.Hp; j += LOOP_THREADS) {
+      pg[j] = 0.f;
+      if (LN) pb[j] = 0.f;
+    }
+  }
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < a.N; row += gridDim.x) {
+    const T* xrow = reinterpret_cast<const T*>(a.x) + row * a.ldx;
+    const T* dyrow = reinterpret_cast<const T*>(a.dy) + row * a.lddy;
+    const float r = a.rstd[row];
+    const float mu = LN ? a.mean[row] : 0.f;
+    float S[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) S[k] = 0.f;
+    for (int j = t; j < H; j += LOOP_THREADS) {
+      const float xv = load_elem<D>(xrow, j);
+      const float xh = LN ? (xv - mu) * r : xv * r;
+      const float g = __fmul_rn(load_elem<D>(dyrow, j), a.gamma ? load_param<D>(a.gamma, j, w_f32) : 1.f);
+      if (LN) {
+        S[0] += g;
+        S[1] = fmaf(g, xh, S[1]);
+        S[2] += xh;
+      } else {
+        S[0] = fmaf(g, xh, S[0]);
+      }
+    }
+    group_sum<NS>(S, sh, NW, wig, lane, 1, parity);
+    const float s0 = LN ? S[2] * inv_h : 0.f;
+    const float c1 = LN ? S[0] * inv_h : 0.f;
+    const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
+    T* dxrow = reinterpret_cast<T*>(a.dx) + row * a.lddx;
+    for (int j = t; j < H; j += LOOP_THREADS) {
+      const float xv = load_elem<D>(xrow, j);
+      const float dyv = load_elem<D>(dyrow, j);
+      const float xc = LN ? (xv - mu) * r - s0 : xv * r;
+      const float g = __fmul_rn(dyv, a.gamma ? load_param<D>(a.gamma, j, w_f32) : 1.f);
+      store_elem<D>(dxrow, j, r * (g - c1 - xc * c2));
+      if (pg) {
+        pg[j] = fmaf(dyv, xc, pg[j]);
+        if (LN) pb[j] += dyv;
+      }
+    }
+    parity ^= 1;
+  }
+}
+
+// dgamma[j] = sum_p partial[0][p][j], dbeta[j] = sum_p partial[1][p][j]: 8
+// column vectors (32 columns) x 32 row groups per CTA, blockIdx.y picks the
+// parameter.  Fixed summation order, one rounding to the output dtype.
+template <typename D>
+__global__ void __launch_bounds__(256) bwd_param_reduce_kernel(const float* ws, int P, int Hp, int H,
+                                                               void* dg, void* db, int w_f32) {
+  const int which = blockIdx.y;
+  void* out = which ? db : dg;
+  if (out == nullptr) return;
+  const float* src = ws + (size_t)which * P * Hp;
+  const int cl = threadIdx.x & 7;
+  const int rg = threadIdx.x >> 3;
+  const int col = (blockIdx.x * 8 + cl) * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (col < Hp) {
+#pragma unroll 4
+    for (int p = rg; p < P; p += 32) {
+      const float4 v = *reinterpret_cast<const float4*>(src + (size_t)p * Hp + col);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+  }
+  __shared__ float4 sm[32][8];
+  sm[rg][cl] = acc;
+  __syncthreads();
+  if (rg == 0 && col < H) {
+    float4 s = sm[0][cl];
+    for (int k = 1; k < 32; ++k) {
+      const float4 v = sm[k][cl];
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    }
+    const float vals[4] = {s.x, s.y, s.z, s.w};
+    for (int i = 0; i < 4 && col + i < H; ++i) {
+      if (w_f32) {
+        reinterpret_cast<float*>(out)[col + i] = vals[i];
+      } else {
+        store_elem<D>(out, col + i, vals[i]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side configuration.
+// ---------------------------------------------------------------------------
+
+static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <int KIND, typename D, int VPT, int MAXT>
+static cudaError_t run_reg(const BwdArgs& a, int threads, int P, size_t smem, cudaStream_t s) {
+  auto kern = bwd_reg_kernel<KIND, D, VPT, MAXT>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<P, threads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int KIND, typename D>
+static cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& dev,
+                                    cudaStream_t s) {
+  using T = typename D::T;
+  constexpr int VEC = D::VEC;
+  constexpr int VPT_MAX = 16 / VEC;  // 16 elements per thread
+  constexpr int NS = KIND == KIND_LN ? 3 : 1;
+  const size_t es = sizeof(T);
+  const size_t wes = a.w_f32 ? 4 : es;
+  const bool want = dg != nullptr || db != nullptr;
+  if (a.N == 0) {
+    if (dg && cudaMemsetAsync(dg, 0, (size_t)a.H * wes, s) != cudaSuccess) return cudaGetLastError();
+    if (db && cudaMemsetAsync(db, 0, (size_t)a.H * wes, s) != cudaSuccess) return cudaGetLastError();
+    return cudaSuccess;
+  }
+  if (!want) a.ws = nullptr;
+  a.Hp = bwd_partial_stride(a.H);
+  const int p_max = bwd_max_partials(dev);
+  bool aligned = aligned16(a.x) && aligned16(a.dy) && aligned16(a.dx) && (a.ldx * es) % 16 == 0 &&
+                 (a.lddy * es) % 16 == 0 && (a.lddx * es) % 16 == 0;
+  if (a.gamma) aligned = aligned && aligned16(a.gamma);
+  int P = 0;
+  cudaError_t err = cudaSuccess;
+  bool done = false;
+  // Register path: narrow rows get one warp each (8 rows per CTA); wider rows
+  // keep 16 elements per thread and add warps, up to 1024 threads per row
+  // (H <= 16384); CTAs above 256 threads get a 64-register budget.
+  if (aligned && a.H % VEC == 0) {
+    const int Hv = a.H / VEC;
+    int vpt, tpr;
+    if (Hv <= 32 * VPT_MAX) {
+      tpr = 32;
+      vpt = 1;
+      while (vpt * 32 < Hv) vpt *= 2;
+    } else {
+      vpt = VPT_MAX;
+      tpr = ((Hv + vpt - 1) / vpt + 31) / 32 * 32;
+    }
+    if (tpr <= 1024) {
+      a.tpr = tpr;
+      const int rpc = tpr <= 256 ? 256 / tpr : 1;
+      const int threads = rpc * tpr;
+      P = (int)std::min<int64_t>((a.N + rpc - 1) / rpc, p_max);
+      size_t smem_f = (size_t)((rpc * 2 * (tpr / 32) * NS + 3) & ~3);
+      if (rpc > 1 && want) smem_f += 2 * (size_t)a.Hp;
+      const size_t smem = smem_f * sizeof(float);
+      if (threads <= 256) {
+        switch (vpt) {
+          case 1: err = run_reg<KIND, D, 1, 256>(a, threads, P, smem, s); break;
+          case 2: err = run_reg<KIND, D, 2, 256>(a, threads, P, smem, s); break;
+          default:
+            if constexpr (VPT_MAX >= 4) err = run_reg<KIND, D, 4, 256>(a, threads, P, smem, s);
+            break;
+        }
+      } else {
+        err = run_reg<KIND, D, VPT_MAX, 1024>(a, threads, P, smem, s);
+      }
+      done = true;
+    }
+  }
+  if (!done) {
+    P = (int)std::min<int64_t>(a.N, p_max);
+    bwd_loop_kernel<KIND, D><<<P, LOOP_THREADS, 0, s>>>(a);
+    err = cudaGetLastError();
+  }
+  if (err != cudaSuccess || !want) return err;
+  dim3 grid((a.Hp + 31) / 32, KIND == KIND_LN ? 2 : 1);
+  bwd_param_reduce_kernel<D><<<grid, 256, 0, s>>>(a.ws, P, a.Hp, a.H, dg, KIND == KIND_LN ? db : nullptr,
+                                                 a.w_f32);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_backward(int kind, Dtype dt, BwdArgs a, void* dgamma, void* dbeta,
+                            const DeviceInfo& dev, cudaStream_t s) {
+  if (dt == DT_BF16) {
+    return kind == KIND_LN ? launch_bwd_typed<KIND_LN, BF16>(a, dgamma, dbeta, dev, s)
+                           : launch_bwd_typed<KIND_RMS, BF16>(a, dgamma, nullptr, dev, s);
+  }
+  return kind == KIND_LN ? launch_bwd_typed<KIND_LN, F32>(a, dgamma, dbeta, dev, s)
+                         : launch_bwd_typed<KIND_RMS, F32>(a, dgamma, nullptr, dev, s);
+}
+
+}  // namespace normk

@@ -1,0 +1,138 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every function the
+header declares, and validates arguments on the host before any CUDA call.
+
+Pointers passed here are fake addresses; validation never dereferences them
+and every call below is rejected (or has N == 0) before reaching the GPU.
+"""
+
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+import torch
+
+from rmsnorm_ln_fwd_gb300 import _build, _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "norm.h")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE, CUDA = 0, 1, 2, 3, 4
+F32, BF16 = 0, 1
+A, B, C, D = 0x100000, 0x200000, 0x300000, 0x400000  # fake, well-separated addresses
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:norm_status|size_t|const char\*|int)\s+([a-z_0-9]+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_five_ops():
+    names = set(declared_functions())
+    for op in ["ln_forward", "rms_forward", "fused_add_rms_forward", "ln_backward", "rms_backward",
+               "norm_bwd_workspace_bytes", "norm_status_str"]:
+        assert op in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported by libnorm.so"
+        assert n in _lib.SIGNATURES, f"{n} has no binding"
+    nm = shutil.which("nm")
+    if nm:
+        out = subprocess.run([nm, "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True).stdout
+        exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+        assert set(names) <= exported
+
+
+def test_header_is_plain_c():
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    p = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-x", "c", HEADER],
+                       capture_output=True, text=True)
+    assert p.returncode == 0, p.stderr
+
+
+def test_status_strings_and_version(lib):
+    for code in range(5):
+        s = lib.norm_status_str(code).decode()
+        assert s.startswith("NORM_")
+    assert lib.norm_status_str(99).decode() == "NORM_ERR_UNKNOWN"
+    assert lib.norm_abi_version() == 10000
+
+
+def _ln(lib, **kw):
+    a = dict(x=A, ldx=64, g=None, b=None, y=B, ldy=64, mean=None, rstd=None, N=4, H=64, eps=1e-5, xd=BF16,
+             wd=BF16)
+    a.update(kw)
+    return lib.ln_forward(a["x"], a["ldx"], a["g"], a["b"], a["y"], a["ldy"], a["mean"], a["rstd"], a["N"],
+                          a["H"], a["eps"], a["xd"], a["wd"], None)
+
+
+def test_forward_validation(lib):
+    assert _ln(lib, xd=F32, wd=BF16) == UNSUPPORTED
+    assert _ln(lib, xd=7) == UNSUPPORTED
+    for eps in (0.0, -1e-5, float("nan"), float("inf")):
+        assert _ln(lib, eps=eps) == INVALID
+    assert _ln(lib, H=0) == INVALID
+    assert _ln(lib, N=-1) == INVALID
+    assert _ln(lib, H=(1 << 24) + 1, ldx=(1 << 24) + 1, ldy=(1 << 24) + 1) == INVALID
+    assert _ln(lib, ldx=63) == INVALID
+    assert _ln(lib, x=None) == INVALID
+    assert _ln(lib, y=A + 2) == INVALID            # y partially overlaps x
+    assert _ln(lib, y=A, ldy=65) == INVALID        # same start, different stride
+    assert _ln(lib, mean=C, rstd=C + 4) == INVALID  # mean/rstd overlap
+    assert _ln(lib, N=0, x=None, y=None) == OK      # nothing to do
+    assert lib.rms_forward(A, 64, None, B, 64, None, 4, 64, -1.0, BF16, BF16, None) == INVALID
+
+
+def test_fused_validation(lib):
+    def f(x=A, r=B, y=C, h=D, ld=64, N=4, H=64, ldh=64):
+        return lib.fused_add_rms_forward(x, ld, r, ld, None, y, ld, h, ldh, None, N, H, 1e-6, BF16, BF16, None)
+    assert f(h=None) == INVALID
+    assert f(r=None) == INVALID
+    assert f(y=A) == INVALID              # y may not alias an input
+    assert f(y=D) == INVALID              # nor h
+    assert f(h=A + 64) == INVALID         # h partially overlaps x
+    assert f(h=B, ldh=65) == INVALID      # h over residual with another stride
+    assert f(r=A + 8, h=A) == INVALID     # in place over x while residual overlaps x
+    assert f(N=0, x=None, r=None, y=None, h=None) == OK
+
+
+def _bwd(lib, **kw):
+    a = dict(dy=A, ldy=64, x=B, ldx=64, mean=C, rstd=C + 4096, g=None, dx=D, lddx=64, dg=None, db=None, ws=None,
+             wsb=0, N=4, H=64, xd=BF16, wd=BF16)
+    a.update(kw)
+    return lib.ln_backward(a["dy"], a["ldy"], a["x"], a["ldx"], a["mean"], a["rstd"], a["g"], a["dx"], a["lddx"],
+                           a["dg"], a["db"], a["ws"], a["wsb"], a["N"], a["H"], a["xd"], a["wd"], None)
+
+
+def test_backward_validation(lib):
+    assert _bwd(lib, xd=BF16, wd=7) == UNSUPPORTED
+    assert _bwd(lib, rstd=None) == INVALID
+    assert _bwd(lib, mean=None) == INVALID
+    assert _bwd(lib, dx=B) == INVALID            # dx may not overlap x
+    assert _bwd(lib, dx=A + 2) == INVALID        # partial overlap with dy
+    assert _bwd(lib, H=0) == INVALID
+    assert _bwd(lib, lddx=10) == INVALID
+    assert _bwd(lib, dg=0x500000, db=0x500000 + 8) == INVALID  # dgamma/dbeta overlap
+    assert lib.rms_backward(A, 64, B, 64, None, None, D, 64, None, None, 0, 4, 64, BF16, BF16, None) == INVALID
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_no_device_reports_cuda_error(lib):
+    # valid arguments, but no GPU to run on: a clean NORM_ERR_CUDA, no crash
+    assert _ln(lib) == CUDA
+    assert lib.norm_bwd_workspace_bytes(1024, 0) == 0
+    assert lib.norm_bwd_workspace_bytes(0, 0) == 0
