@@ -166,6 +166,28 @@ const char* norm_status_str(norm_status status);
 /* Version of this ABI: major*10000 + minor*100 + patch. */
 int norm_abi_version(void);
 
+/* The CUDA call and error behind the calling thread's most recent
+ * NORM_ERR_CUDA ("" if none yet).  Static per-thread storage, never NULL. */
+const char* norm_last_error(void);
+
+/*
+ * Device-side error bits raised since the last clear, for CUDA device
+ * `device`.  Kernels never trap: every wait inside them is bounded (2 s), and a
+ * wait that runs out sets NORM_DEVICE_ERR_WAIT_TIMEOUT here and abandons the
+ * call's remaining work.  The read is synchronous; call it after the streams
+ * that ran the kernels have been synchronised.  clear != 0 resets the bits.
+ */
+#define NORM_DEVICE_ERR_WAIT_TIMEOUT 1u
+norm_status norm_device_errors(int device, unsigned int* flags, int clear);
+
+/*
+ * Testing and tuning: choose the first kernel family a launch may use, for
+ * every later call in the process.  0 = all (the default: bulk-copy pipeline,
+ * then register rows, then the strided loop), 1 = register rows or loop,
+ * 2 = loop only.  Every family computes the same results within rounding.
+ */
+norm_status norm_set_kernel_path(int path);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,6 +36,9 @@ SIGNATURES = {
     "rms_backward": (_I, [_P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _P, ctypes.c_size_t, _I64, _I64, _I, _I, _P]),
     "norm_status_str": (ctypes.c_char_p, [_I]),
     "norm_abi_version": (_I, []),
+    "norm_last_error": (ctypes.c_char_p, []),
+    "norm_device_errors": (_I, [_I, ctypes.POINTER(ctypes.c_uint), _I]),
+    "norm_set_kernel_path": (_I, [_I]),
 }
 
 _lock = threading.Lock()
@@ -75,6 +78,21 @@ def status_str(status: int) -> str:
     return load().norm_status_str(int(status)).decode()
 
 
+def device_errors(device: int = 0, clear: bool = True) -> int:
+    """Error bits the kernels raised on `device` since the last clear."""
+    v = ctypes.c_uint(0)
+    check("norm_device_errors", load().norm_device_errors(int(device), ctypes.byref(v), int(clear)))
+    return int(v.value)
+
+
+def set_kernel_path(path: int) -> None:
+    """0: fastest available family (default), 1: register or loop, 2: loop."""
+    check("norm_set_kernel_path", load().norm_set_kernel_path(int(path)))
+
+
 def check(fn: str, status: int) -> None:
     if status != NORM_OK:
-        raise NormError(fn, status, status_str(status))
+        text = status_str(status)
+        if status == NORM_ERR_CUDA:
+            text += f" [{load().norm_last_error().decode()}]"
+        raise NormError(fn, status, text)

@@ -236,4 +236,110 @@ __device__ __forceinline__ Welford group_welford(Welford w, float* sh, int nw, i
   return acc;
 }
 
+
+// ---------------------------------------------------------------------------
+// Bulk-copy pipeline primitives (sm_90+ PTX, used on sm_103a): mbarriers in
+// shared memory, 1-D bulk global->shared copies that complete a transaction
+// count on an mbarrier, and programmatic dependent launch.  Every wait is
+// bounded by the global nanosecond timer; a wait that runs out records an
+// error bit for the host and returns false instead of spinning forever.
+// ---------------------------------------------------------------------------
+constexpr unsigned kErrWaitTimeout = 1u;
+constexpr unsigned kErrBadCopy = 2u;  // a bulk copy failed its bounds check and was skipped
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the phase with the given parity has completed, for at most
+// kWaitLimitNs.  On timeout, set kErrWaitTimeout in *err, raise the CTA's
+// abort flag and return false.  Once the abort flag is up (another thread's
+// wait ran out), later waits give up at once; pass abort == nullptr for a wait
+// that must run its full limit regardless (draining copies before exit).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err,
+                                          volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (abort && *abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (err) atomicOr(err, kErrWaitTimeout);
+      if (abort) *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// global to this CTA's shared memory; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Row range [lo, hi) of CTA c when N rows are split over `grid` CTAs as
+// evenly as possible (range sizes differ by at most one row).
+__device__ __forceinline__ void cta_rows(int64_t N, int c, int grid, int64_t& lo, int64_t& hi) {
+  lo = N * c / grid;
+  hi = N * (c + 1) / grid;
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue now / wait here until the previous kernel has finished and its
+// writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// 16-byte shared memory access.
+__device__ __forceinline__ uint4 lds16(const void* p) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(smem_u32(p)));
+  return r;
+}
+
 }  // namespace normk

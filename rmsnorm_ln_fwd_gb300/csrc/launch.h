@@ -11,9 +11,15 @@ namespace normk {
 enum Dtype : int { DT_F32 = 0, DT_BF16 = 1 };
 enum Kind : int { KIND_LN = 0, KIND_RMS = 1, KIND_FUSED = 2 };
 
+// Kernel families, fastest first.  A launch uses the first family whose
+// requirements the call meets, starting from DeviceInfo::path.
+enum Path : int { PATH_STAGED = 0, PATH_REGISTER = 1, PATH_LOOP = 2 };
+
 struct DeviceInfo {
   int sm_count;
   int max_smem_optin;  // bytes of shared memory one CTA may opt into
+  unsigned* err;       // this device's error-flag word (see norm_device_errors)
+  int path;            // first kernel family to try (norm_set_kernel_path)
 };
 
 // Forward: LayerNorm (KIND_LN), RMSNorm (KIND_RMS), fused add + RMSNorm (KIND_FUSED).
@@ -34,7 +40,6 @@ struct FwdArgs {
   int H;
   float eps;
   int w_f32;    // parameters are fp32 (else the row dtype)
-  int h_alias;  // fused: h_out is exactly x or residual
   int tpr;      // threads per row (filled in by the launcher)
 };
 
@@ -56,6 +61,24 @@ struct BwdArgs {
   int w_f32;
   int tpr;  // threads per row (filled in by the launcher)
 };
+
+// Shape of a staged (bulk-copy pipelined) launch, chosen on the host.  The CTA
+// has W consumer warps plus one producer warp; each stage of the shared-memory
+// ring holds G rows (one per consumer row group of W/G warps) of every staged
+// tensor, tensor-major: [tensor][row][H elements].
+struct StageCfg {
+  int G;             // rows per stage = consumer row groups
+  int S;             // stages in the ring
+  int W;             // consumer warps
+  int row_bytes;     // H * element size (a multiple of 16)
+  int red_off;       // byte offset of the cross-warp reduction scratch
+  int data_off;      // byte offset of stage 0
+  int contiguous;    // rows of every staged tensor are back to back (ld == H)
+  unsigned* err;     // device error flags (bounded waits that ran out)
+};
+
+constexpr int kStagedConsumerWarps = 16;
+constexpr int kStagedThreads = (kStagedConsumerWarps + 1) * 32;
 
 // Partial rows the backward may use on a device: a fixed multiple of the SM
 // count, independent of the number of input rows.

@@ -5,7 +5,9 @@
 // an invalid call has no effect on the GPU.  No entry point throws, aborts or
 // allocates.
 
+#include <atomic>
 #include <cmath>
+#include <cstdio>
 #include <cstdint>
 #include <mutex>
 
@@ -24,6 +26,21 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DeviceInfo g_info[kMaxDevices];
 bool g_have[kMaxDevices];
+std::atomic<int> g_path{normk::PATH_STAGED};
+
+}  // namespace
+
+// One error word per device: kernels OR error bits into it (a bounded wait
+// that ran out) instead of trapping; norm_device_errors reads it.
+__device__ unsigned g_norm_device_errors;
+
+namespace {
+
+thread_local char t_last_error[256] = "";
+
+void note_error(const char* where, cudaError_t e) {
+  snprintf(t_last_error, sizeof(t_last_error), "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
+}
 
 bool device_info(int dev, DeviceInfo* out) {
   if (dev < 0 || dev >= kMaxDevices) return false;
@@ -44,8 +61,29 @@ bool device_info(int dev, DeviceInfo* out) {
 
 bool current_device_info(DeviceInfo* out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  return device_info(dev, out);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    note_error("cudaGetDevice", e);
+    return false;
+  }
+  if (!device_info(dev, out)) {
+    snprintf(t_last_error, sizeof(t_last_error), "device %d: attribute query failed", dev);
+    return false;
+  }
+  if (out->err == nullptr) {
+    // The symbol's address on the current device (this device).
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_norm_device_errors);
+    if (e != cudaSuccess) {
+      note_error("cudaGetSymbolAddress", e);
+      return false;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_info[dev].err = static_cast<unsigned*>(p);
+    out->err = g_info[dev].err;
+  }
+  out->path = g_path.load(std::memory_order_relaxed);
+  return true;
 }
 
 size_t elem_size(norm_dtype d) { return d == NORM_BF16 ? 2 : 4; }
@@ -99,7 +137,11 @@ bool disjoint_rows(const void* p, int64_t ldp, const void* q, int64_t ldq, int64
   return !overlap(rows_span(p, N, ldp, H, es), rows_span(q, N, ldq, H, es));
 }
 
-norm_status launch_result(cudaError_t e) { return e == cudaSuccess ? NORM_OK : NORM_ERR_CUDA; }
+norm_status launch_result(const char* where, cudaError_t e) {
+  if (e == cudaSuccess) return NORM_OK;
+  note_error(where, e);
+  return NORM_ERR_CUDA;
+}
 
 normk::Dtype to_dt(norm_dtype d) { return d == NORM_BF16 ? normk::DT_BF16 : normk::DT_F32; }
 
@@ -149,8 +191,8 @@ norm_status forward_common(int kind, const void* x, int64_t ldx, const void* res
   a.H = (int)H;
   a.eps = eps;
   a.w_f32 = wd == NORM_F32;
-  a.h_alias = fused && ((h == x && ldh == ldx) || (h == res && ldh == ldr));
-  return launch_result(normk::launch_forward(kind, to_dt(xd), a, dev, reinterpret_cast<cudaStream_t>(stream)));
+  return launch_result("forward launch", normk::launch_forward(kind, to_dt(xd), a, dev,
+                                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t workspace_bytes_for(int64_t H, const DeviceInfo& dev) {
@@ -175,8 +217,8 @@ norm_status backward_common(int kind, const void* dy, int64_t lddy, const void* 
     a.N = 0;
     a.H = (int)H;
     a.w_f32 = wd == NORM_F32;
-    return launch_result(normk::launch_backward(kind, to_dt(xd), a, dgamma, dbeta, dev,
-                                                reinterpret_cast<cudaStream_t>(stream)));
+    return launch_result("backward (N = 0) launch", normk::launch_backward(kind, to_dt(xd), a, dgamma, dbeta, dev,
+                                                                     reinterpret_cast<cudaStream_t>(stream)));
   }
   if (dy == nullptr || x == nullptr || dx == nullptr || rstd == nullptr) return NORM_ERR_INVALID_VALUE;
   if (kind == normk::KIND_LN && mean == nullptr) return NORM_ERR_INVALID_VALUE;
@@ -211,8 +253,8 @@ norm_status backward_common(int kind, const void* dy, int64_t lddy, const void* 
   a.N = N;
   a.H = (int)H;
   a.w_f32 = wd == NORM_F32;
-  return launch_result(normk::launch_backward(kind, to_dt(xd), a, dgamma, dbeta, dev,
-                                              reinterpret_cast<cudaStream_t>(stream)));
+  return launch_result("backward launch", normk::launch_backward(kind, to_dt(xd), a, dgamma, dbeta, dev,
+                                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -276,5 +318,30 @@ const char* norm_status_str(norm_status status) {
 }
 
 int norm_abi_version(void) { return 10000; }
+
+const char* norm_last_error(void) { return t_last_error; }
+
+norm_status norm_set_kernel_path(int path) {
+  if (path < normk::PATH_STAGED || path > normk::PATH_LOOP) return NORM_ERR_INVALID_VALUE;
+  g_path.store(path, std::memory_order_relaxed);
+  return NORM_OK;
+}
+
+norm_status norm_device_errors(int device, unsigned int* flags, int clear) {
+  if (flags == nullptr) return NORM_ERR_INVALID_VALUE;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return NORM_ERR_CUDA;
+  if (device != cur && cudaSetDevice(device) != cudaSuccess) return NORM_ERR_CUDA;
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_norm_device_errors, sizeof(v));
+  if (e == cudaSuccess && clear) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_norm_device_errors, &zero, sizeof(zero));
+  }
+  if (device != cur) cudaSetDevice(cur);
+  if (e != cudaSuccess) return NORM_ERR_CUDA;
+  *flags = v;
+  return NORM_OK;
+}
 
 }  // extern "C"

@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "staged.cuh"
 
 namespace normk {
 
@@ -171,6 +172,180 @@ __global__ void __launch_bounds__(MAXT) bwd_reg_kernel(const BwdArgs a) {
   }
 }
 
+
+// Staged backward: the bulk-copy pipeline of staged.cuh with x and dy staged
+// per row.  Each consumer row group owns one row of every stage; each thread
+// owns VPT 16-byte column vectors (the same ones for every row), so its
+// dgamma/dbeta accumulators stay in registers for the whole row range.  The
+// saved mean/rstd of the group's next row are loaded one stage ahead.  At the
+// end the groups' accumulators are summed in shared memory (fixed order) into
+// this CTA's partial row, and the dependent reduction kernel is released.
+template <int KIND, typename D, int VPT>
+__global__ void __launch_bounds__(kStagedThreads, 1) bwd_staged_kernel(const BwdArgs a, const StageCfg c) {
+  using T = typename D::T;
+  constexpr int VEC = D::VEC;
+  constexpr bool LN = KIND == KIND_LN;
+  constexpr int NS = LN ? 3 : 1;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const StagedSmem m = staged_smem(smem, c);
+  staged_init(m, c);
+  int64_t lo, hi;
+  cta_rows(a.N, blockIdx.x, gridDim.x, lo, hi);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int H = a.H;
+  const int hv = H / VEC;
+  const int nwg = c.W / c.G;
+  const int g = warp / nwg;
+  const int wig = warp - g * nwg;
+  const int tpr = nwg * 32;
+  const int t = wig * 32 + lane;
+
+  float acc_g[VPT][VEC], acc_b[VPT][VEC];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) acc_g[v][i] = acc_b[v][i] = 0.f;
+
+  if (warp == c.W) {
+    if (lane == 0) {
+      const void* const src[2] = {a.x, a.dy};
+      const int64_t ld[2] = {a.ldx, a.lddy};
+      staged_produce<2>(m, c, src, ld, lo, hi, sizeof(T));
+    }
+    __syncwarp();  // reconverge before the CTA-wide barrier below
+  } else {
+    const float inv_h = 1.f / (float)H;
+    const bool w_f32 = a.w_f32 != 0;
+    float* sh = m.red + g * (2 * nwg * NS);
+    const int bar_id = 1 + g;
+    int parity = 0;
+    int k = 0;
+    float r_next = 0.f, mu_next = 0.f;
+    if (lo + g < hi) {
+      r_next = a.rstd[lo + g];
+      if (LN) mu_next = a.mean[lo + g];
+    }
+    for (int64_t row0 = lo; row0 < hi; row0 += c.G, ++k) {
+      const int s = k % c.S;
+      const int64_t row = row0 + g;
+      const float r = r_next, mu = mu_next;
+      if (row + c.G < hi) {  // statistics of this group's next row, one stage ahead
+        r_next = a.rstd[row + c.G];
+        if (LN) mu_next = a.mean[row + c.G];
+      }
+      const bool have = mbar_wait(&m.full[s], (k / c.S) & 1, c.err, m.abort);
+      if (row < hi) {
+        const T* xs = staged_row<T>(m, c, 2, s, 0, g);
+        const T* ds = staged_row<T>(m, c, 2, s, 1, g);
+        float S[NS];
+#pragma unroll
+        for (int q = 0; q < NS; ++q) S[q] = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int j = t + v * tpr;
+          if (j < hv) {
+            float xv[VEC], dv[VEC], gm[VEC];
+            unpack<D>(lds16(xs + j * VEC), xv);
+            unpack<D>(lds16(ds + j * VEC), dv);
+            load_param_vec<D>(a.gamma, j * VEC, w_f32, 1.f, gm);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) {
+              const float xh = LN ? (xv[i] - mu) * r : xv[i] * r;
+              const float gg = __fmul_rn(dv[i], gm[i]);
+              if (LN) {
+                S[0] += gg;
+                S[1] = fmaf(gg, xh, S[1]);
+                S[2] += xh;
+              } else {
+                S[0] = fmaf(gg, xh, S[0]);
+              }
+            }
+          }
+        }
+        group_sum<NS>(S, sh, nwg, wig, lane, bar_id, parity);
+        const float s0 = LN ? S[2] * inv_h : 0.f;  // row mean of x_hat: removes the mean's rounding shift
+        const float c1 = LN ? S[0] * inv_h : 0.f;
+        const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
+        T* dxrow = reinterpret_cast<T*>(a.dx) + row * a.lddx;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int j = t + v * tpr;
+          if (j < hv) {
+            float xv[VEC], dv[VEC], gm[VEC], out[VEC];
+            unpack<D>(lds16(xs + j * VEC), xv);
+            unpack<D>(lds16(ds + j * VEC), dv);
+            load_param_vec<D>(a.gamma, j * VEC, w_f32, 1.f, gm);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) {
+              const float xc = LN ? (xv[i] - mu) * r - s0 : xv[i] * r;
+              const float gg = __fmul_rn(dv[i], gm[i]);
+              out[i] = r * (gg - c1 - xc * c2);
+              acc_g[v][i] = fmaf(dv[i], xc, acc_g[v][i]);
+              if (LN) acc_b[v][i] += dv[i];
+            }
+            if (have) store_vec<D>(dxrow, j * VEC, out);
+          }
+        }
+      }
+      parity ^= 1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m.empty[s]);
+    }
+  }
+  pdl_launch_dependents();
+  // Every copy has landed (consumers waited on all of them; the producer
+  // drained), so the ring is free: fold the groups into one partial row.
+  __syncthreads();
+  if (a.ws == nullptr) return;
+  const int Hp = a.Hp;
+  float* pg = a.ws + (size_t)blockIdx.x * Hp;
+  float* pb = a.ws + ((size_t)gridDim.x + blockIdx.x) * Hp;
+  const bool consumer = warp < c.W;
+  if (c.G == 1) {
+    if (consumer) {
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int j = t + v * tpr;
+        if (j < hv) {
+#pragma unroll
+          for (int q = 0; q < VEC / 4; ++q) {
+            *reinterpret_cast<float4*>(pg + j * VEC + 4 * q) = make_float4(
+                acc_g[v][4 * q], acc_g[v][4 * q + 1], acc_g[v][4 * q + 2], acc_g[v][4 * q + 3]);
+            if (LN)
+              *reinterpret_cast<float4*>(pb + j * VEC + 4 * q) = make_float4(
+                  acc_b[v][4 * q], acc_b[v][4 * q + 1], acc_b[v][4 * q + 2], acc_b[v][4 * q + 3]);
+          }
+        }
+      }
+    }
+    return;
+  }
+  float* red_g = reinterpret_cast<float*>(m.data);
+  float* red_b = red_g + Hp;
+  for (int g2 = 0; g2 < c.G; ++g2) {
+    if (consumer && g == g2) {
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int j = t + v * tpr;
+        if (j < hv) {
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) {
+            const int col = j * VEC + i;
+            red_g[col] = g2 == 0 ? acc_g[v][i] : red_g[col] + acc_g[v][i];
+            if (LN) red_b[col] = g2 == 0 ? acc_b[v][i] : red_b[col] + acc_b[v][i];
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  for (int col = threadIdx.x * 4; col < H; col += blockDim.x * 4) {
+    *reinterpret_cast<float4*>(pg + col) = *reinterpret_cast<const float4*>(red_g + col);
+    if (LN) *reinterpret_cast<float4*>(pb + col) = *reinterpret_cast<const float4*>(red_b + col);
+  }
+}
+
 constexpr int LOOP_THREADS = 256;
 
 // Any H, any alignment: one row per CTA iteration, two passes over the row.
@@ -244,6 +419,7 @@ __global__ void __launch_bounds__(LOOP_THREADS) bwd_loop_kernel(const BwdArgs a)
 template <typename D>
 __global__ void __launch_bounds__(256) bwd_param_reduce_kernel(const float* ws, int P, int Hp, int H,
                                                                void* dg, void* db, int w_f32) {
+  pdl_wait_primary();  // launched as a programmatic dependent of the main kernel
   const int which = blockIdx.y;
   void* out = which ? db : dg;
   if (out == nullptr) return;
@@ -302,6 +478,17 @@ static cudaError_t run_reg(const BwdArgs& a, int threads, int P, size_t smem, cu
   return cudaGetLastError();
 }
 
+constexpr int kStagedMaxCols = 32;  // columns per consumer thread (register accumulators)
+
+template <int KIND, typename D, int VPT>
+static cudaError_t run_staged(const BwdArgs& a, const StageCfg& c, int P, size_t smem, cudaStream_t s) {
+  auto kern = bwd_staged_kernel<KIND, D, VPT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<P, kStagedThreads, smem, s>>>(a, c);
+  return cudaGetLastError();
+}
+
 template <int KIND, typename D>
 static cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& dev,
                                     cudaStream_t s) {
@@ -326,10 +513,36 @@ static cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceI
   int P = 0;
   cudaError_t err = cudaSuccess;
   bool done = false;
+  // Staged path (bulk-copy pipeline, one persistent CTA per SM).
+  if (dev.path <= PATH_STAGED && aligned && a.H % VEC == 0) {
+    StageCfg c{};
+    // 17 warps leave at most 96 registers a thread (a sub-partition holds 5
+    // warps).  LayerNorm keeps two accumulators per column, so it first tries
+    // shapes with at most 16 columns per thread.
+    const bool fits = (KIND == KIND_LN && staged_config(a.H, (int)es, 2, dev.max_smem_optin, 16, &c)) ||
+                      staged_config(a.H, (int)es, 2, dev.max_smem_optin, kStagedMaxCols, &c);
+    if (fits) {
+      c.err = dev.err;
+      c.contiguous = a.ldx == a.H && a.lddy == a.H;
+      const int tpr = 32 * (c.W / c.G);
+      const int vpt = (a.H / VEC + tpr - 1) / tpr;
+      P = (int)std::min<int64_t>((int64_t)dev.sm_count, (a.N + c.G - 1) / c.G);
+      const size_t smem = staged_smem_bytes(c, 2);
+      if (vpt <= 1) err = run_staged<KIND, D, 1>(a, c, P, smem, s);
+      else if (vpt <= 2) err = run_staged<KIND, D, 2>(a, c, P, smem, s);
+      else if (vpt <= 3) err = run_staged<KIND, D, 3>(a, c, P, smem, s);
+      else if (vpt <= 4) err = run_staged<KIND, D, 4>(a, c, P, smem, s);
+      else if constexpr (VEC == 4) {
+        if (vpt <= 6) err = run_staged<KIND, D, 6>(a, c, P, smem, s);
+        else err = run_staged<KIND, D, 8>(a, c, P, smem, s);
+      }
+      done = true;
+    }
+  }
   // Register path: narrow rows get one warp each (8 rows per CTA); wider rows
   // keep 16 elements per thread and add warps, up to 1024 threads per row
   // (H <= 16384); CTAs above 256 threads get a 64-register budget.
-  if (aligned && a.H % VEC == 0) {
+  if (!done && dev.path <= PATH_REGISTER && aligned && a.H % VEC == 0) {
     const int Hv = a.H / VEC;
     int vpt, tpr;
     if (Hv <= 32 * VPT_MAX) {
@@ -368,9 +581,22 @@ static cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceI
     err = cudaGetLastError();
   }
   if (err != cudaSuccess || !want) return err;
-  dim3 grid((a.Hp + 31) / 32, KIND == KIND_LN ? 2 : 1);
-  bwd_param_reduce_kernel<D><<<grid, 256, 0, s>>>(a.ws, P, a.Hp, a.H, dg, KIND == KIND_LN ? db : nullptr,
-                                                 a.w_f32);
+  // The column reduction is a programmatic dependent of the main kernel: it
+  // is scheduled while the main kernel drains and waits for it on the device.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.Hp + 31) / 32, KIND == KIND_LN ? 2 : 1);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float* ws = a.ws;
+  void* dbeta = KIND == KIND_LN ? db : nullptr;
+  err = cudaLaunchKernelEx(&cfg, bwd_param_reduce_kernel<D>, ws, P, a.Hp, a.H, dg, dbeta, a.w_f32);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

@@ -1,7 +1,12 @@
 // Forward kernels: LayerNorm, RMSNorm and fused residual-add + RMSNorm.
 //
-// Two kernel families:
+// Three kernel families, tried in this order:
 //
+// * fwd_staged_kernel -- persistent, one CTA per SM; a producer warp streams
+//   rows through a shared-memory ring with bulk copies (see staged.cuh) and
+//   consumer row groups compute from shared memory.  Needs 16-byte aligned
+//   rows, H a multiple of the vector width and at least three stages of rows
+//   in shared memory.
 // * fwd_reg_kernel -- the row lives in registers.  A "row group" of `tpr`
 //   threads (one warp for narrow rows, up to 1024 threads for wide rows) owns
 //   one row at a time; each thread holds VPT 16-byte vectors of it, so HBM is
@@ -11,7 +16,8 @@
 //   16-byte aligned rows and H a multiple of the vector width.
 // * fwd_loop_kernel -- any H and any alignment: one CTA per row, a strided
 //   loop over the row, a statistics pass and an output pass (the second read
-//   mostly hits L2).  Per-thread statistics use Welford's recurrence.
+//   mostly hits L2).  Per-thread statistics use Welford's recurrence.  The
+//   fused kernel stores h in the output pass, after re-forming the fp32 sum.
 //
 // Statistics ("Skill: Write CUDA LayerNorm Kernel", Required reasoning process
 // steps 2-5; "Skill: Write a Triton LayerNorm Kernel" steps 3-7):
@@ -31,6 +37,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "staged.cuh"
 
 namespace normk {
 
@@ -155,6 +162,181 @@ __global__ void __launch_bounds__(MAXT) fwd_reg_kernel(const FwdArgs a) {
   }
 }
 
+
+#ifndef NORM_STAGED_MAX_STAGES
+#define NORM_STAGED_MAX_STAGES 6
+#endif
+
+bool staged_config(int H, int es, int NT, int max_smem, int max_cols, StageCfg* c) {
+  const int row_bytes = H * es;
+  if (H <= 0 || row_bytes % 16 != 0) return false;
+  const int vec = 16 / es;
+  const int hv = H / vec;
+  c->W = kStagedConsumerWarps;
+  c->row_bytes = row_bytes;
+  c->red_off = 256;                                   // barriers + abort flag
+  c->data_off = c->red_off + 2 * c->W * 3 * 4 + 256;  // scratch, rounded up
+  c->data_off = (c->data_off + 127) & ~127;
+  for (int G = c->W; G >= 1; G /= 2) {
+    const int tpr = 32 * (c->W / G);
+    const int cols = ((hv + tpr - 1) / tpr) * vec;
+    if (max_cols > 0 && cols > max_cols) continue;
+    const size_t stage = (size_t)NT * G * row_bytes;
+    const long S = (long)(max_smem - c->data_off) / (long)stage;
+    if (S < 3) continue;
+    c->G = G;
+    c->S = (int)std::min<long>(S, NORM_STAGED_MAX_STAGES);
+    return true;
+  }
+  return false;
+}
+
+size_t staged_smem_bytes(const StageCfg& c, int NT) { return c.data_off + (size_t)c.S * NT * c.G * c.row_bytes; }
+
+template <int KIND, typename D>
+__global__ void __launch_bounds__(kStagedThreads, 1) fwd_staged_kernel(const FwdArgs a, const StageCfg c) {
+  using T = typename D::T;
+  constexpr int VEC = D::VEC;
+  constexpr int NT = KIND == KIND_FUSED ? 2 : 1;  // staged tensors: x (and residual)
+  extern __shared__ __align__(128) unsigned char smem[];
+  const StagedSmem m = staged_smem(smem, c);
+  staged_init(m, c);
+  int64_t lo, hi;
+  cta_rows(a.N, blockIdx.x, gridDim.x, lo, hi);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == c.W) {
+    if (lane == 0) {
+      if constexpr (NT == 2) {
+        const void* const src[2] = {a.x, a.res};
+        const int64_t ld[2] = {a.ldx, a.ldr};
+        staged_produce<2>(m, c, src, ld, lo, hi, sizeof(T));
+      } else {
+        const void* const src[1] = {a.x};
+        const int64_t ld[1] = {a.ldx};
+        staged_produce<1>(m, c, src, ld, lo, hi, sizeof(T));
+      }
+    }
+    return;
+  }
+
+  const int H = a.H;
+  const int hv = H / VEC;
+  const float inv_h = 1.f / (float)H;
+  const bool w_f32 = a.w_f32 != 0;
+  const int nwg = c.W / c.G;  // warps per row group
+  const int g = warp / nwg;
+  const int wig = warp - g * nwg;
+  const int tpr = nwg * 32;
+  const int t = wig * 32 + lane;
+  float* sh = m.red + g * (2 * nwg * 3);
+  const int bar_id = 1 + g;
+  int parity = 0;
+  int k = 0;
+  for (int64_t row0 = lo; row0 < hi; row0 += c.G, ++k) {
+    const int s = k % c.S;
+    const bool have = mbar_wait(&m.full[s], (k / c.S) & 1, c.err, m.abort);
+    const int64_t row = row0 + g;
+    if (row < hi) {  // uniform across the row group
+      const T* xs = staged_row<T>(m, c, NT, s, 0, g);
+      float rstd, mean_d = 0.f, pivot = 0.f;
+      if constexpr (KIND == KIND_LN) {
+        // This thread's Welford triple by two passes over its vectors, then
+        // the parallel merge across the row group.
+        pivot = load_elem<D>(xs, 0);
+        float sum = 0.f;
+        int nvec = 0;
+#pragma unroll 4
+        for (int j = t; j < hv; j += tpr) {
+          float f[VEC];
+          unpack<D>(lds16(xs + j * VEC), f);
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) sum += f[i] - pivot;
+          ++nvec;
+        }
+        const float cnt = (float)(nvec * VEC);
+        const float mloc = nvec > 0 ? sum / cnt : 0.f;
+        float m2 = 0.f;
+#pragma unroll 4
+        for (int j = t; j < hv; j += tpr) {
+          float f[VEC];
+          unpack<D>(lds16(xs + j * VEC), f);
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) {
+            const float e = (f[i] - pivot) - mloc;
+            m2 = fmaf(e, e, m2);
+          }
+        }
+        const Welford w = group_welford(Welford{cnt, mloc, m2}, sh, nwg, wig, lane, bar_id, parity);
+        mean_d = w.m;
+        rstd = rsqrtf(w.m2 * inv_h + a.eps);
+      } else {
+        float ss[1] = {0.f};
+        if constexpr (KIND == KIND_FUSED) {
+          const T* rs = staged_row<T>(m, c, NT, s, 1, g);
+          T* hrow = reinterpret_cast<T*>(a.h) + row * a.ldh;
+#pragma unroll 4
+          for (int j = t; j < hv; j += tpr) {
+            float f[VEC], r[VEC];
+            unpack<D>(lds16(xs + j * VEC), f);
+            unpack<D>(lds16(rs + j * VEC), r);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) {
+              f[i] += r[i];
+              ss[0] = fmaf(f[i], f[i], ss[0]);
+            }
+            if (have) store_vec<D>(hrow, j * VEC, f);
+          }
+        } else {
+#pragma unroll 4
+          for (int j = t; j < hv; j += tpr) {
+            float f[VEC];
+            unpack<D>(lds16(xs + j * VEC), f);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) ss[0] = fmaf(f[i], f[i], ss[0]);
+          }
+        }
+        group_sum<1>(ss, sh, nwg, wig, lane, bar_id, parity);
+        rstd = rsqrtf(ss[0] * inv_h + a.eps);
+      }
+      if (t == 0 && have) {
+        if constexpr (KIND == KIND_LN) {
+          if (a.mean) a.mean[row] = pivot + mean_d;
+        }
+        if (a.rstd) a.rstd[row] = rstd;
+      }
+      T* yrow = reinterpret_cast<T*>(a.y) + row * a.ldy;
+      const T* rs = KIND == KIND_FUSED ? staged_row<T>(m, c, NT, s, 1, g) : nullptr;
+#pragma unroll 4
+      for (int j = t; j < hv; j += tpr) {
+        float f[VEC], gm[VEC], out[VEC];
+        unpack<D>(lds16(xs + j * VEC), f);
+        load_param_vec<D>(a.gamma, j * VEC, w_f32, 1.f, gm);
+        if constexpr (KIND == KIND_LN) {
+          float b[VEC];
+          load_param_vec<D>(a.beta, j * VEC, w_f32, 0.f, b);
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) out[i] = fmaf(((f[i] - pivot) - mean_d) * rstd, gm[i], b[i]);
+        } else {
+          if constexpr (KIND == KIND_FUSED) {
+            float r[VEC];
+            unpack<D>(lds16(rs + j * VEC), r);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) f[i] += r[i];
+          }
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) out[i] = (f[i] * rstd) * gm[i];
+        }
+        if (have) store_vec<D>(yrow, j * VEC, out);
+      }
+    }
+    parity ^= 1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&m.empty[s]);
+  }
+}
+
 constexpr int LOOP_THREADS = 256;
 
 template <int KIND, typename D>
@@ -190,11 +372,11 @@ __global__ void __launch_bounds__(LOOP_THREADS) fwd_loop_kernel(const FwdArgs a)
     } else {
       float ss[1] = {0.f};
       if constexpr (KIND == KIND_FUSED) {
+        // h is only summed here; it is stored in the second pass, so that
+        // pass can still re-form the fp32 sum when h_out aliases an input.
         const T* rrow = reinterpret_cast<const T*>(a.res) + row * a.ldr;
-        T* hrow = reinterpret_cast<T*>(a.h) + row * a.ldh;
         for (int j = t; j < H; j += LOOP_THREADS) {
           const float h = load_elem<D>(xrow, j) + load_elem<D>(rrow, j);
-          store_elem<D>(hrow, j, h);
           ss[0] = fmaf(h, h, ss[0]);
         }
       } else {
@@ -221,16 +403,10 @@ __global__ void __launch_bounds__(LOOP_THREADS) fwd_loop_kernel(const FwdArgs a)
         const float b = a.beta ? load_param<D>(a.beta, j, w_f32) : 0.f;
         out = fmaf((load_elem<D>(xrow, j) - pivot - mean_d) * rstd, g, b);
       } else if constexpr (KIND == KIND_FUSED) {
-        // The row was written in the first pass by this same thread.  When
-        // h_out aliases an input, the fp32 sum can no longer be re-formed, so
-        // the stored (rounded) h is reloaded, as the fused-add page's
-        // two-pass variant does.
-        float h;
-        if (a.h_alias) {
-          h = load_elem<D>(reinterpret_cast<const T*>(a.h) + row * a.ldh, j);
-        } else {
-          h = load_elem<D>(xrow, j) + load_elem<D>(reinterpret_cast<const T*>(a.res) + row * a.ldr, j);
-        }
+        // Element j of x and residual is read, and h_out[j] written, by this
+        // thread only, so storing h here is safe when h_out aliases an input.
+        const float h = load_elem<D>(xrow, j) + load_elem<D>(reinterpret_cast<const T*>(a.res) + row * a.ldr, j);
+        store_elem<D>(reinterpret_cast<T*>(a.h) + row * a.ldh, j, h);
         out = (h * rstd) * g;
       } else {
         out = (load_elem<D>(xrow, j) * rstd) * g;
@@ -275,7 +451,22 @@ static cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream
     aligned = aligned && aligned16(a.res) && aligned16(a.h) && (a.ldr * es) % 16 == 0 &&
               (a.ldh * es) % 16 == 0;
   }
-  if (aligned && a.H % VEC == 0) {
+  if (dev.path <= PATH_STAGED && aligned && a.H % VEC == 0) {
+    StageCfg c{};
+    constexpr int NT = KIND == KIND_FUSED ? 2 : 1;
+    if (staged_config(a.H, (int)es, NT, dev.max_smem_optin, 0, &c)) {
+      c.err = dev.err;
+      c.contiguous = a.ldx == a.H && (NT == 1 || a.ldr == a.H);
+      const size_t smem = staged_smem_bytes(c, NT);
+      auto kern = fwd_staged_kernel<KIND, D>;
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      const int64_t blocks = std::min<int64_t>((int64_t)dev.sm_count, (a.N + c.G - 1) / c.G);
+      kern<<<(unsigned)blocks, kStagedThreads, smem, s>>>(a, c);
+      return cudaGetLastError();
+    }
+  }
+  if (dev.path <= PATH_REGISTER && aligned && a.H % VEC == 0) {
     const int Hv = a.H / VEC;
     int vpt, tpr;
     if (Hv <= 32 * VPT_MAX) {

@@ -5,7 +5,8 @@ Tolerances (the readings of the stated targets):
 
 * fp32 outputs and gradients: max relative error <= 1e-5, measured normwise
   per tensor, max_i |a_i - r_i| / max_i |r_i| (an elementwise ratio is
-  undefined where r_i ~ 0).  rstd, never near 0, is also checked elementwise.
+  undefined where r_i ~ 0).  rstd, never near 0, is checked elementwise; the
+  saved mean, often near 0, against the RMS of its row.
 * bf16 outputs (y, dx): |a_i - r_i| <= ulp_bf16(r_i) + 2^-20 * S_i, i.e. one
   bf16 ulp of the exact value plus the fp32 evaluation error of the expression,
   S_i being the magnitude of the terms that are summed to form element i.
@@ -90,15 +91,27 @@ def check_rstd(got, ref, what):
     assert rel <= F32_TOL, f"{what}: elementwise relative error {rel:.3e}"
 
 
+def check_mean(got, ref, x, what):
+    """The saved mean is judged against the scale of its row, RMS(x_row): a
+    mean near 0 has no relative accuracy of its own to speak of."""
+    scale = np.sqrt(np.mean(np.asarray(x, dtype=np.float64) ** 2, axis=1))
+    rel = np.max(np.abs(got - ref) / np.maximum(scale, 1e-30)) if ref.size else 0.0
+    assert rel <= F32_TOL, f"{what}: error relative to the row RMS {rel:.3e}"
+
+
 # --------------------------------------------------------------------------
 # scale terms for the bf16 slack (magnitudes of what is summed per element)
 # --------------------------------------------------------------------------
 
 def ln_y_scale(x, mean, rstd, gamma, beta):
-    xh = (x - mean[:, None]) * rstd[:, None]
+    """Magnitude of what y_i = (x_i - mean) * rstd * gamma_i + beta_i is formed
+    from.  The fp32 mean carries an absolute error of order eps_fp32 * (|mean|
+    + sigma), whatever |x_i - mean| is, so that scale enters x_hat's error."""
+    sigma = np.sqrt(np.maximum(1.0 / rstd ** 2, 0.0))
+    spread = (np.abs(x - mean[:, None]) + (np.abs(mean) + sigma)[:, None]) * rstd[:, None]
     g = np.ones(x.shape[1]) if gamma is None else gamma
     b = np.zeros(x.shape[1]) if beta is None else beta
-    return np.abs(xh * g) + np.abs(b)
+    return spread * np.abs(g) + np.abs(b)
 
 
 def rms_y_scale(x, rstd, gamma):
@@ -107,14 +120,17 @@ def rms_y_scale(x, rstd, gamma):
 
 
 def ln_dx_scale(dy, x, gamma, eps):
+    """Magnitude of the terms of dx_i = rstd * (g_i - c1 - x_hat_i * c2), with
+    x_hat's own error scale (|x_i - mean| + |mean| + sigma) * rstd."""
     H = x.shape[1]
     g = dy * (np.ones(H) if gamma is None else gamma)
     mean, var = O.two_pass_stats(x)
     r = 1.0 / np.sqrt(var + eps)
     xh = (x - mean[:, None]) * r[:, None]
+    spread = (np.abs(x - mean[:, None]) + (np.abs(mean) + np.sqrt(var))[:, None]) * r[:, None]
     c1 = g.mean(axis=1, keepdims=True)
     c2 = (g * xh).mean(axis=1, keepdims=True)
-    return r[:, None] * (np.abs(g) + np.abs(c1) + np.abs(xh * c2))
+    return r[:, None] * (np.abs(g) + np.abs(c1) + spread * np.abs(c2))
 
 
 def rms_dx_scale(dy, x, gamma, eps):

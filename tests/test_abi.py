@@ -130,6 +130,13 @@ def test_backward_validation(lib):
     assert lib.rms_backward(A, 64, B, 64, None, None, D, 64, None, None, 0, 4, 64, BF16, BF16, None) == INVALID
 
 
+def test_kernel_path_override_validation(lib):
+    assert lib.norm_set_kernel_path(3) == INVALID
+    assert lib.norm_set_kernel_path(-1) == INVALID
+    for p in (2, 1, 0):
+        assert lib.norm_set_kernel_path(p) == OK
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_no_device_reports_cuda_error(lib):
     # valid arguments, but no GPU to run on: a clean NORM_ERR_CUDA, no crash
