@@ -470,6 +470,7 @@ def run_sweep(args):
     _build.build()
     import rmsnorm_ln_fwd_gb300 as nl
     lib = nl.load_library()
+    nl._lib.set_kernel_path(args.path)
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
     peak, kind = measured_peak()
@@ -499,7 +500,8 @@ def run_sweep(args):
         us = [a.elapsed_time(b) * 1e3 for a, b in ts]
         byts = alg_bytes(op, N, H)
         med = statistics.median(us)
-        print(json.dumps({"op": op, "N": N, "H": H, "us_median": round(med, 2), "us_min": round(min(us), 2),
+        print(json.dumps({"op": op, "N": N, "H": H, "path": args.path, "us_median": round(med, 2),
+                          "us_min": round(min(us), 2),
                           "gbs": round(byts / (med * 1e-6) / 1e9, 1), "frac": round(byts / (med * 1e-6) / 1e9 / peak, 3),
                           "bytes": byts, "peak": peak, "peak_kind": kind}), flush=True)
 
@@ -512,6 +514,7 @@ def run_profile_loop(args):
     _build.build()
     import rmsnorm_ln_fwd_gb300 as nl
     lib = nl.load_library()
+    nl._lib.set_kernel_path(args.path)
     N, H = (int(v) for v in args.shape.split("x"))
     dev = torch.device("cuda", 0)
     s = Shape(N, H, dev, seed=3, lib=lib)
@@ -537,6 +540,7 @@ def main():
     p.add_argument("--ref-rows", type=int, default=64)
     p.add_argument("--sweep", action="store_true", help="per-call timings over every configured shape")
     p.add_argument("--sweep-iters", type=int, default=50)
+    p.add_argument("--path", type=int, default=0, help="kernel-family policy: 0 auto, 1 register rows, 2 loop, 3 bulk-copy pipeline")
     p.add_argument("--profile-op", choices=list(OPS), default=None)
     p.add_argument("--shape", default="8192x1024")
     p.add_argument("--iters", type=int, default=3)

@@ -181,10 +181,11 @@ const char* norm_last_error(void);
 norm_status norm_device_errors(int device, unsigned int* flags, int clear);
 
 /*
- * Testing and tuning: choose the first kernel family a launch may use, for
- * every later call in the process.  0 = all (the default: bulk-copy pipeline,
- * then register rows, then the strided loop), 1 = register rows or loop,
- * 2 = loop only.  Every family computes the same results within rounding.
+ * Testing and tuning: the kernel-family policy for every later call in the
+ * process.  0 = automatic (the default), 1 = register rows (else the strided
+ * loop), 2 = strided loop only, 3 = bulk-copy pipeline first.  A family is
+ * used only where the call meets its requirements (alignment, row width);
+ * every family computes the same results within rounding.
  */
 norm_status norm_set_kernel_path(int path);
 

@@ -86,7 +86,7 @@ def device_errors(device: int = 0, clear: bool = True) -> int:
 
 
 def set_kernel_path(path: int) -> None:
-    """0: fastest available family (default), 1: register or loop, 2: loop."""
+    """0: automatic (default), 1: register rows, 2: strided loop, 3: bulk-copy pipeline first."""
     check("norm_set_kernel_path", load().norm_set_kernel_path(int(path)))
 
 

@@ -161,6 +161,16 @@ __device__ __forceinline__ void warp_sum(float (&v)[K]) {
   }
 }
 
+// Tree sum of a short array: depth log2(n) instead of an n-long add chain.
+template <int N>
+__device__ __forceinline__ float tree_sum(const float* v) {
+  if constexpr (N == 1) {
+    return v[0];
+  } else {
+    return tree_sum<N / 2>(v) + tree_sum<N - N / 2>(v + N / 2);
+  }
+}
+
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -195,10 +205,15 @@ struct Welford {
   float n, m, m2;
 };
 
+// The weight n_b/n uses the fast reciprocal-multiply division (2 ulp): an
+// error there moves the merged mean by about |delta| * 2^-22 and perturbs
+// only the small delta^2 correction of M2, far below the fp32 sums' own error.
+// Equal counts (the common case: every thread of a full row holds the same
+// number of values) take the exact weight 1/2 with no division.
 __device__ __forceinline__ Welford welford_merge(const Welford& a, const Welford& b) {
   const float n = a.n + b.n;
   if (n == 0.f) return a;
-  const float wb = b.n / n;
+  const float wb = a.n == b.n ? 0.5f : __fdividef(b.n, n);
   const float d = b.m - a.m;
   Welford r;
   r.n = n;
@@ -220,6 +235,11 @@ __device__ __forceinline__ Welford warp_welford(Welford w, int lane) {
 }
 
 // Welford merge over the warps of a row group, same buffering as group_sum.
+// The warps' triples are combined in the closed form of the parallel merge
+// for K parts: N = sum n_k, M = sum n_k m_k / N,
+// M2 = sum M2_k + sum n_k (m_k - M)^2 -- the pairwise merge applied K-1
+// times, evaluated in about 3K operations, in warp order (every thread gets
+// the same bits).
 __device__ __forceinline__ Welford group_welford(Welford w, float* sh, int nw, int wig, int lane,
                                                  int bar_id, int parity) {
   w = warp_welford(w, lane);
@@ -231,11 +251,19 @@ __device__ __forceinline__ Welford group_welford(Welford w, float* sh, int nw, i
     buf[wig * 3 + 2] = w.m2;
   }
   named_barrier(bar_id, nw * 32);
-  Welford acc{buf[0], buf[1], buf[2]};
-  for (int k = 1; k < nw; ++k) acc = welford_merge(acc, Welford{buf[3 * k], buf[3 * k + 1], buf[3 * k + 2]});
-  return acc;
+  float n = 0.f, sm = 0.f;
+  for (int k = 0; k < nw; ++k) {
+    n += buf[3 * k];
+    sm = fmaf(buf[3 * k], buf[3 * k + 1], sm);
+  }
+  const float m = n > 0.f ? __fdividef(sm, n) : 0.f;
+  float m2 = 0.f;
+  for (int k = 0; k < nw; ++k) {
+    const float d = buf[3 * k + 1] - m;
+    m2 += fmaf(buf[3 * k] * d, d, buf[3 * k + 2]);
+  }
+  return Welford{n, m, m2};
 }
-
 
 // ---------------------------------------------------------------------------
 // Bulk-copy pipeline primitives (sm_90+ PTX, used on sm_103a): mbarriers in
@@ -340,6 +368,92 @@ __device__ __forceinline__ uint4 lds16(const void* p) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "r"(smem_u32(p)));
   return r;
+}
+
+// ---------------------------------------------------------------------------
+// Packed fp32 pairs (sm_100+ f32x2 instructions): two IEEE fp32 operations,
+// each rounded exactly as its scalar form, per instruction.  Row data are
+// handled as pairs: a 16-byte vector is VEC/2 pairs.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long f2_bits(float2 v) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+__device__ __forceinline__ float2 bits_f2(unsigned long long r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+
+// A 16-byte vector as VEC/2 fp32 pairs (pair p holds elements 2p, 2p+1).
+template <typename D>
+__device__ __forceinline__ void unpack2(const uint4& u, float2* p);
+
+template <>
+__device__ __forceinline__ void unpack2<F32>(const uint4& u, float2* p) {
+  p[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+  p[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+}
+
+template <>
+__device__ __forceinline__ void unpack2<BF16>(const uint4& u, float2* p) {
+  p[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
+  p[1] = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+  p[2] = make_float2(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u));
+  p[3] = make_float2(__uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u));
+}
+
+template <typename D>
+__device__ __forceinline__ uint4 pack2(const float2* p);
+
+template <>
+__device__ __forceinline__ uint4 pack2<F32>(const float2* p) {
+  return make_uint4(__float_as_uint(p[0].x), __float_as_uint(p[0].y), __float_as_uint(p[1].x),
+                    __float_as_uint(p[1].y));
+}
+
+template <>
+__device__ __forceinline__ uint4 pack2<BF16>(const float2* p) {
+  return make_uint4(pack_bf16x2(p[0].x, p[0].y), pack_bf16x2(p[1].x, p[1].y), pack_bf16x2(p[2].x, p[2].y),
+                    pack_bf16x2(p[3].x, p[3].y));
+}
+
+// gamma/beta for the full vector at column c as pairs (p == nullptr: fill).
+template <typename D>
+__device__ __forceinline__ void load_param_pairs(const void* p, int c, bool w_f32, float fill, float2* out) {
+  constexpr int VP = D::VEC / 2;
+  if (p == nullptr) {
+#pragma unroll
+    for (int i = 0; i < VP; ++i) out[i] = splat2(fill);
+  } else if (w_f32) {
+    const float* q = reinterpret_cast<const float*>(p) + c;
+#pragma unroll
+    for (int k = 0; k < VP / 2; ++k) unpack2<F32>(ld_cached(q + 4 * k), out + 2 * k);
+  } else {
+    unpack2<D>(ld_cached(reinterpret_cast<const typename D::T*>(p) + c), out);
+  }
 }
 
 }  // namespace normk

@@ -11,9 +11,12 @@ namespace normk {
 enum Dtype : int { DT_F32 = 0, DT_BF16 = 1 };
 enum Kind : int { KIND_LN = 0, KIND_RMS = 1, KIND_FUSED = 2 };
 
-// Kernel families, fastest first.  A launch uses the first family whose
-// requirements the call meets, starting from DeviceInfo::path.
-enum Path : int { PATH_STAGED = 0, PATH_REGISTER = 1, PATH_LOOP = 2 };
+// Kernel-family policy (norm_set_kernel_path).  AUTO: register rows when a
+// row needs at most kRowsAutoMaxThreads threads, else the bulk-copy pipeline,
+// else register rows, else the loop.  ROWS: register rows, else loop.  LOOP:
+// loop only.  STAGED: bulk-copy pipeline, else register rows, else loop.
+enum Path : int { PATH_AUTO = 0, PATH_ROWS = 1, PATH_LOOP = 2, PATH_STAGED = 3 };
+constexpr int kRowsAutoMaxThreads = 640;
 
 struct DeviceInfo {
   int sm_count;

@@ -26,7 +26,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DeviceInfo g_info[kMaxDevices];
 bool g_have[kMaxDevices];
-std::atomic<int> g_path{normk::PATH_STAGED};
+std::atomic<int> g_path{normk::PATH_AUTO};
 
 }  // namespace
 
@@ -322,7 +322,7 @@ int norm_abi_version(void) { return 10000; }
 const char* norm_last_error(void) { return t_last_error; }
 
 norm_status norm_set_kernel_path(int path) {
-  if (path < normk::PATH_STAGED || path > normk::PATH_LOOP) return NORM_ERR_INVALID_VALUE;
+  if (path < normk::PATH_AUTO || path > normk::PATH_STAGED) return NORM_ERR_INVALID_VALUE;
   g_path.store(path, std::memory_order_relaxed);
   return NORM_OK;
 }

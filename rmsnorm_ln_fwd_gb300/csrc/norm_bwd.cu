@@ -31,10 +31,18 @@ namespace normk {
 
 int bwd_max_partials(const DeviceInfo& dev) { return 2 * dev.sm_count; }
 
-template <int KIND, typename D, int VPT, int MAXT>
-__global__ void __launch_bounds__(MAXT) bwd_reg_kernel(const BwdArgs a) {
+// Register-row backward.  Persistent row groups walk rows row, row + stride,
+// ...; the next row's x, dy and saved statistics are loaded while the current
+// row computes.  Each thread owns fixed column vectors, so its dgamma/dbeta
+// accumulators stay in fp32 across all its rows: in registers (ACC_SMEM =
+// false), or, when one CTA covers a whole row (so every column has exactly one
+// owner thread), in shared memory, updated by plain read-modify-write, which
+// frees the registers for wide rows.  Elementwise math uses f32x2.
+template <int KIND, typename D, int VPT, int MAXT, int MINB, bool ACC_SMEM>
+__global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
   using T = typename D::T;
   constexpr int VEC = D::VEC;
+  constexpr int VP = VEC / 2;
   constexpr bool LN = KIND == KIND_LN;
   constexpr int NS = LN ? 3 : 1;  // values per row reduction
   extern __shared__ __align__(16) float sh_dyn[];
@@ -46,121 +54,210 @@ __global__ void __launch_bounds__(MAXT) bwd_reg_kernel(const BwdArgs a) {
   const int wig = t >> 5;
   const int lane = threadIdx.x & 31;
   const int H = a.H;
+  const int hv = H / VEC;
   const float inv_h = 1.f / (float)H;
   const bool w_f32 = a.w_f32 != 0;
   float* sh = sh_dyn + slot * (2 * nw * NS);
   const int bar_id = 1 + slot;
   const int64_t stride = (int64_t)gridDim.x * rpc;
-  int parity = 0;
+  int nvec = 0;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
 
-  float acc_g[VPT][VEC], acc_b[VPT][VEC];
+  constexpr int VA = ACC_SMEM ? 1 : VPT;  // register accumulator vectors
+  float2 acc_g[VA][VP], acc_b[VA][VP];
 #pragma unroll
-  for (int v = 0; v < VPT; ++v)
+  for (int v = 0; v < VA; ++v)
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) acc_g[v][i] = acc_b[v][i] = 0.f;
-
-  for (int64_t row = (int64_t)blockIdx.x * rpc + slot; row < a.N; row += stride) {
-    const T* xrow = reinterpret_cast<const T*>(a.x) + row * a.ldx;
-    const T* dyrow = reinterpret_cast<const T*>(a.dy) + row * a.lddy;
-    // x and dy stay packed in registers between the two passes over the row.
-    uint4 xr[VPT], dr[VPT];
-#pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      const int c = (v * tpr + t) * VEC;
-      xr[v] = load_vec_or_zero<D>(xrow, c, H);
-      dr[v] = load_vec_or_zero<D>(dyrow, c, H);
+    for (int p = 0; p < VP; ++p) acc_g[v][p] = acc_b[v][p] = splat2(0.f);
+  const int Hp = a.Hp;
+  const int red_off = ((rpc * 2 * nw * NS) + 3) & ~3;
+  float* sacc_g = sh_dyn + red_off;  // ACC_SMEM: [Hp] dgamma then [Hp] dbeta
+  float* sacc_b = sacc_g + Hp;
+  if constexpr (ACC_SMEM) {
+    for (int k = threadIdx.x * 4; k < Hp; k += blockDim.x * 4) {
+      *reinterpret_cast<float4*>(sacc_g + k) = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (LN) *reinterpret_cast<float4*>(sacc_b + k) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const float r = a.rstd[row];
-    const float mu = LN ? a.mean[row] : 0.f;
+    __syncthreads();
+  }
 
-    // Pass 1: sum(g), sum(g*x_hat) and (LayerNorm) sum(x_hat).
-    float S[NS];
-#pragma unroll
-    for (int k = 0; k < NS; ++k) S[k] = 0.f;
+  uint4 nx[VPT], nd[VPT];
+  float nrs = 0.f, nmu = 0.f;
+  auto fetch = [&](int64_t r) {
+    const T* xrow = reinterpret_cast<const T*>(a.x) + r * a.ldx;
+    const T* dyrow = reinterpret_cast<const T*>(a.dy) + r * a.lddy;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
-      const int c = (v * tpr + t) * VEC;
-      if (c >= H) continue;
-      float xv[VEC], dv[VEC], gm[VEC];
-      unpack<D>(xr[v], xv);
-      unpack<D>(dr[v], dv);
-      load_param_vec<D>(a.gamma, c, w_f32, 1.f, gm);
+      const int c = (t + v * tpr) * VEC;
+      nx[v] = load_vec_or_zero<D>(xrow, c, H);
+      nd[v] = load_vec_or_zero<D>(dyrow, c, H);
+    }
+    nrs = a.rstd[r];
+    if (LN) nmu = a.mean[r];
+  };
+
+  int parity = 0;
+  int64_t row = (int64_t)blockIdx.x * rpc + slot;
+  if (row < a.N) fetch(row);
+  for (; row < a.N; row += stride) {
+    const float r = nrs;
+    const float2 r2 = splat2(r);
+    float2 xh[VPT][VP];
+    uint4 dcur[VPT];
+    {
+      // x_hat = x*rstd - mean*rstd: the rounding of mean*rstd shifts the whole
+      // row by one constant, which the recentring below removes.
+      const float2 b2 = splat2(LN ? -nmu * r : 0.f);
 #pragma unroll
-      for (int i = 0; i < VEC; ++i) {
-        const float xh = LN ? (xv[i] - mu) * r : xv[i] * r;
-        const float g = __fmul_rn(dv[i], gm[i]);  // rounded once: both passes see the same g
-        if (LN) {
-          S[0] += g;
-          S[1] = fmaf(g, xh, S[1]);
-          S[2] += xh;
-        } else {
-          S[0] = fmaf(g, xh, S[0]);
+      for (int v = 0; v < VPT; ++v) {
+        float2 xv[VP];
+        unpack2<D>(nx[v], xv);
+#pragma unroll
+        for (int p = 0; p < VP; ++p) xh[v][p] = LN ? fma2(xv[p], r2, b2) : mul2(xv[p], r2);
+        dcur[v] = nd[v];
+      }
+    }
+    if (row + stride < a.N) fetch(row + stride);
+
+    // Pass 1: sum(g), sum(g*x_hat) and (LayerNorm) sum(x_hat), g = dy*gamma.
+    float2 sg = splat2(0.f), sgx = splat2(0.f), sx = splat2(0.f);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      if (v < nvec) {
+        float2 d[VP], gm[VP];
+        unpack2<D>(dcur[v], d);
+        load_param_pairs<D>(a.gamma, (t + v * tpr) * VEC, w_f32, 1.f, gm);
+#pragma unroll
+        for (int p = 0; p < VP; ++p) {
+          const float2 g = mul2(d[p], gm[p]);
+          sgx = fma2(g, xh[v][p], sgx);
+          if (LN) {
+            sg = add2(sg, g);
+            sx = add2(sx, xh[v][p]);
+          }
         }
       }
     }
+    float S[NS];
+    if (LN) {
+      S[0] = sg.x + sg.y;
+      S[1] = sgx.x + sgx.y;
+      S[NS - 1] = sx.x + sx.y;
+    } else {
+      S[0] = sgx.x + sgx.y;
+    }
     group_sum<NS>(S, sh, nw, wig, lane, bar_id, parity);
-
-    // Pass 2: dx and the parameter-gradient accumulators.
-    T* dxrow = reinterpret_cast<T*>(a.dx) + row * a.lddx;
-    const float s0 = LN ? S[2] * inv_h : 0.f;  // row mean of x_hat: removes the mean's rounding shift
+    // LayerNorm: mean(x_hat) is 0 exactly; its computed value s0 is the shift
+    // left by the saved mean's rounding, removed from x_hat here.
+    const float s0 = LN ? S[NS - 1] * inv_h : 0.f;
     const float c1 = LN ? S[0] * inv_h : 0.f;
     const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
+    const float2 s02 = splat2(s0), c12 = splat2(c1), nc22 = splat2(-c2);
+
+    // Pass 2: dx = rstd * (g - c1 - x_hat * c2) and the accumulators.
+    T* dxrow = reinterpret_cast<T*>(a.dx) + row * a.lddx;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
-      const int c = (v * tpr + t) * VEC;
-      if (c >= H) continue;
-      float xv[VEC], dv[VEC], gm[VEC], out[VEC];
-      unpack<D>(xr[v], xv);
-      unpack<D>(dr[v], dv);
-      load_param_vec<D>(a.gamma, c, w_f32, 1.f, gm);
+      if (v < nvec) {
+        const int col = (t + v * tpr) * VEC;
+        float2 d[VP], gm[VP], out[VP];
+        unpack2<D>(dcur[v], d);
+        load_param_pairs<D>(a.gamma, col, w_f32, 1.f, gm);
+        float2 ag[VP], ab[VP];
+        if constexpr (ACC_SMEM) {
 #pragma unroll
-      for (int i = 0; i < VEC; ++i) {
-        const float xc = LN ? (xv[i] - mu) * r - s0 : xv[i] * r;
-        const float g = __fmul_rn(dv[i], gm[i]);  // rounded once: both passes see the same g
-        out[i] = r * (g - c1 - xc * c2);
-        acc_g[v][i] = fmaf(dv[i], xc, acc_g[v][i]);
-        if (LN) acc_b[v][i] += dv[i];
+          for (int q = 0; q < VP / 2; ++q) {
+            const float4 u = *reinterpret_cast<const float4*>(sacc_g + col + 4 * q);
+            ag[2 * q] = make_float2(u.x, u.y);
+            ag[2 * q + 1] = make_float2(u.z, u.w);
+            if (LN) {
+              const float4 w = *reinterpret_cast<const float4*>(sacc_b + col + 4 * q);
+              ab[2 * q] = make_float2(w.x, w.y);
+              ab[2 * q + 1] = make_float2(w.z, w.w);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int p = 0; p < VP; ++p) {
+            ag[p] = acc_g[ACC_SMEM ? 0 : v][p];
+            ab[p] = acc_b[ACC_SMEM ? 0 : v][p];
+          }
+        }
+#pragma unroll
+        for (int p = 0; p < VP; ++p) {
+          const float2 xc = LN ? sub2(xh[v][p], s02) : xh[v][p];
+          const float2 g = mul2(d[p], gm[p]);
+          out[p] = mul2(fma2(xc, nc22, LN ? sub2(g, c12) : g), r2);
+          ag[p] = fma2(d[p], xc, ag[p]);
+          if (LN) ab[p] = add2(ab[p], d[p]);
+        }
+        if constexpr (ACC_SMEM) {
+#pragma unroll
+          for (int q = 0; q < VP / 2; ++q) {
+            *reinterpret_cast<float4*>(sacc_g + col + 4 * q) =
+                make_float4(ag[2 * q].x, ag[2 * q].y, ag[2 * q + 1].x, ag[2 * q + 1].y);
+            if (LN)
+              *reinterpret_cast<float4*>(sacc_b + col + 4 * q) =
+                  make_float4(ab[2 * q].x, ab[2 * q].y, ab[2 * q + 1].x, ab[2 * q + 1].y);
+          }
+        } else {
+#pragma unroll
+          for (int p = 0; p < VP; ++p) {
+            acc_g[ACC_SMEM ? 0 : v][p] = ag[p];
+            acc_b[ACC_SMEM ? 0 : v][p] = ab[p];
+          }
+        }
+        st_vec(dxrow + col, pack2<D>(out));
       }
-      store_vec<D>(dxrow, c, out);
     }
     parity ^= 1;
   }
 
   if (a.ws == nullptr) return;
-  // Fold the CTA's row groups into partial row blockIdx.x.  Columns a thread
-  // never visited hold zeros.
-  const int Hp = a.Hp;
+  // Fold the CTA's row groups into partial row blockIdx.x.
   float* pg = a.ws + (size_t)blockIdx.x * Hp;
   float* pb = a.ws + ((size_t)gridDim.x + blockIdx.x) * Hp;
+  if constexpr (ACC_SMEM) {
+    __syncthreads();
+    for (int k = threadIdx.x * 4; k < H; k += blockDim.x * 4) {
+      *reinterpret_cast<float4*>(pg + k) = *reinterpret_cast<const float4*>(sacc_g + k);
+      if (LN) *reinterpret_cast<float4*>(pb + k) = *reinterpret_cast<const float4*>(sacc_b + k);
+    }
+    return;
+  }
   if (rpc == 1) {
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      const int c = (v * tpr + t) * VEC;
-      if (c >= H) continue;
+    for (int v = 0; v < VA; ++v) {
+      if (v < nvec) {
+        const int col = (t + v * tpr) * VEC;
 #pragma unroll
-      for (int k = 0; k < VEC / 4; ++k) {
-        *reinterpret_cast<float4*>(pg + c + 4 * k) =
-            make_float4(acc_g[v][4 * k], acc_g[v][4 * k + 1], acc_g[v][4 * k + 2], acc_g[v][4 * k + 3]);
-        if (LN)
-          *reinterpret_cast<float4*>(pb + c + 4 * k) =
-              make_float4(acc_b[v][4 * k], acc_b[v][4 * k + 1], acc_b[v][4 * k + 2], acc_b[v][4 * k + 3]);
+        for (int q = 0; q < VP / 2; ++q) {
+          *reinterpret_cast<float4*>(pg + col + 4 * q) =
+              make_float4(acc_g[v][2 * q].x, acc_g[v][2 * q].y, acc_g[v][2 * q + 1].x, acc_g[v][2 * q + 1].y);
+          if (LN)
+            *reinterpret_cast<float4*>(pb + col + 4 * q) =
+                make_float4(acc_b[v][2 * q].x, acc_b[v][2 * q].y, acc_b[v][2 * q + 1].x, acc_b[v][2 * q + 1].y);
+        }
       }
     }
     return;
   }
-  const int red_off = ((rpc * 2 * nw * NS) + 3) & ~3;
-  float* red_g = sh_dyn + red_off;
-  float* red_b = red_g + Hp;
+  float* red_g = sacc_g;
+  float* red_b = sacc_b;
   for (int s2 = 0; s2 < rpc; ++s2) {
     if (slot == s2) {
 #pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        const int c = (v * tpr + t) * VEC;
-        if (c >= H) continue;
+      for (int v = 0; v < VA; ++v) {
+        if (v < nvec) {
+          const int col = (t + v * tpr) * VEC;
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) {
-          red_g[c + i] = s2 == 0 ? acc_g[v][i] : red_g[c + i] + acc_g[v][i];
-          if (LN) red_b[c + i] = s2 == 0 ? acc_b[v][i] : red_b[c + i] + acc_b[v][i];
+          for (int p = 0; p < VP; ++p) {
+            float2* dg2 = reinterpret_cast<float2*>(red_g + col) + p;
+            float2* db2 = reinterpret_cast<float2*>(red_b + col) + p;
+            *dg2 = s2 == 0 ? acc_g[v][p] : add2(*dg2, acc_g[v][p]);
+            if (LN) *db2 = s2 == 0 ? acc_b[v][p] : add2(*db2, acc_b[v][p]);
+          }
         }
       }
     }
@@ -171,7 +268,6 @@ __global__ void __launch_bounds__(MAXT) bwd_reg_kernel(const BwdArgs a) {
     if (LN) *reinterpret_cast<float4*>(pb + k) = *reinterpret_cast<const float4*>(red_b + k);
   }
 }
-
 
 // Staged backward: the bulk-copy pipeline of staged.cuh with x and dy staged
 // per row.  Each consumer row group owns one row of every stage; each thread
@@ -249,17 +345,21 @@ __global__ void __launch_bounds__(kStagedThreads, 1) bwd_staged_kernel(const Bwd
             unpack<D>(lds16(xs + j * VEC), xv);
             unpack<D>(lds16(ds + j * VEC), dv);
             load_param_vec<D>(a.gamma, j * VEC, w_f32, 1.f, gm);
+            // per-vector tree sums: short dependency chains
 #pragma unroll
             for (int i = 0; i < VEC; ++i) {
               const float xh = LN ? (xv[i] - mu) * r : xv[i] * r;
               const float gg = __fmul_rn(dv[i], gm[i]);
-              if (LN) {
-                S[0] += gg;
-                S[1] = fmaf(gg, xh, S[1]);
-                S[2] += xh;
-              } else {
-                S[0] = fmaf(gg, xh, S[0]);
-              }
+              gm[i] = gg * xh;
+              dv[i] = gg;
+              xv[i] = xh;
+            }
+            if (LN) {
+              S[0] += tree_sum<VEC>(dv);
+              S[1] += tree_sum<VEC>(gm);
+              S[2] += tree_sum<VEC>(xv);
+            } else {
+              S[0] += tree_sum<VEC>(gm);
             }
           }
         }
@@ -467,14 +567,19 @@ __global__ void __launch_bounds__(256) bwd_param_reduce_kernel(const float* ws, 
 
 static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <int KIND, typename D, int VPT, int MAXT>
-static cudaError_t run_reg(const BwdArgs& a, int threads, int P, size_t smem, cudaStream_t s) {
-  auto kern = bwd_reg_kernel<KIND, D, VPT, MAXT>;
+template <int KIND, typename D, int VPT, int MAXT, int MINB, bool ACC_SMEM = false>
+static cudaError_t run_rows(const BwdArgs& a, int threads, int* P, int p_cap, size_t smem, const DeviceInfo& dev,
+                            cudaStream_t s) {
+  auto kern = bwd_rows_kernel<KIND, D, VPT, MAXT, MINB, ACC_SMEM>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  kern<<<P, threads, smem, s>>>(a);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  *P = std::max(1, std::min(p_cap, per_sm * dev.sm_count));
+  kern<<<*P, threads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -513,67 +618,81 @@ static cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceI
   int P = 0;
   cudaError_t err = cudaSuccess;
   bool done = false;
-  // Staged path (bulk-copy pipeline, one persistent CTA per SM).
-  if (dev.path <= PATH_STAGED && aligned && a.H % VEC == 0) {
-    StageCfg c{};
-    // 17 warps leave at most 96 registers a thread (a sub-partition holds 5
-    // warps).  LayerNorm keeps two accumulators per column, so it first tries
-    // shapes with at most 16 columns per thread.
-    const bool fits = (KIND == KIND_LN && staged_config(a.H, (int)es, 2, dev.max_smem_optin, 16, &c)) ||
-                      staged_config(a.H, (int)es, 2, dev.max_smem_optin, kStagedMaxCols, &c);
-    if (fits) {
-      c.err = dev.err;
-      c.contiguous = a.ldx == a.H && a.lddy == a.H;
-      const int tpr = 32 * (c.W / c.G);
-      const int vpt = (a.H / VEC + tpr - 1) / tpr;
-      P = (int)std::min<int64_t>((int64_t)dev.sm_count, (a.N + c.G - 1) / c.G);
-      const size_t smem = staged_smem_bytes(c, 2);
-      if (vpt <= 1) err = run_staged<KIND, D, 1>(a, c, P, smem, s);
-      else if (vpt <= 2) err = run_staged<KIND, D, 2>(a, c, P, smem, s);
-      else if (vpt <= 3) err = run_staged<KIND, D, 3>(a, c, P, smem, s);
-      else if (vpt <= 4) err = run_staged<KIND, D, 4>(a, c, P, smem, s);
-      else if constexpr (VEC == 4) {
-        if (vpt <= 6) err = run_staged<KIND, D, 6>(a, c, P, smem, s);
-        else err = run_staged<KIND, D, 8>(a, c, P, smem, s);
-      }
-      done = true;
-    }
+  // Register-row shape: narrow rows one warp each, wider rows 16 elements a
+  // thread with more warps (H <= 16384).
+  const bool vec_ok = aligned && a.H % VEC == 0;
+  const int Hv = a.H / VEC;
+  int vpt = VPT_MAX, tpr = 0;
+  if (Hv <= 32 * VPT_MAX) {
+    tpr = 32;
+    vpt = 1;
+    while (vpt * 32 < Hv) vpt *= 2;
+  } else {
+    tpr = ((Hv + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32;
   }
-  // Register path: narrow rows get one warp each (8 rows per CTA); wider rows
-  // keep 16 elements per thread and add warps, up to 1024 threads per row
-  // (H <= 16384); CTAs above 256 threads get a 64-register budget.
-  if (!done && dev.path <= PATH_REGISTER && aligned && a.H % VEC == 0) {
-    const int Hv = a.H / VEC;
-    int vpt, tpr;
-    if (Hv <= 32 * VPT_MAX) {
-      tpr = 32;
-      vpt = 1;
-      while (vpt * 32 < Hv) vpt *= 2;
-    } else {
-      vpt = VPT_MAX;
-      tpr = ((Hv + vpt - 1) / vpt + 31) / 32 * 32;
+  const bool rows_ok = vec_ok && tpr <= 1024;
+  // Staged shape.  17 warps leave at most 96 registers a thread (a
+  // sub-partition holds 5 warps).  LayerNorm keeps two accumulators per
+  // column, so it first tries shapes with at most 24 columns per thread.
+  StageCfg c{};
+  const bool staged_ok =
+      vec_ok && ((KIND == KIND_LN && staged_config(a.H, (int)es, 2, dev.max_smem_optin, 24, &c)) ||
+                 staged_config(a.H, (int)es, 2, dev.max_smem_optin, kStagedMaxCols, &c));
+  bool use_rows = false, use_staged = false;
+  switch (dev.path) {
+    case PATH_AUTO:
+      use_rows = rows_ok && tpr <= kRowsAutoMaxThreads;
+      use_staged = !use_rows && staged_ok;
+      use_rows = use_rows || (!use_staged && rows_ok);
+      break;
+    case PATH_ROWS: use_rows = rows_ok; break;
+    case PATH_STAGED:
+      use_staged = staged_ok;
+      use_rows = !use_staged && rows_ok;
+      break;
+    default: break;
+  }
+  if (use_staged) {
+    c.err = dev.err;
+    c.contiguous = a.ldx == a.H && a.lddy == a.H;
+    const int stpr = 32 * (c.W / c.G);
+    const int svpt = (Hv + stpr - 1) / stpr;
+    P = (int)std::min<int64_t>((int64_t)dev.sm_count, (a.N + c.G - 1) / c.G);
+    const size_t smem = staged_smem_bytes(c, 2);
+    if (svpt <= 1) err = run_staged<KIND, D, 1>(a, c, P, smem, s);
+    else if (svpt <= 2) err = run_staged<KIND, D, 2>(a, c, P, smem, s);
+    else if (svpt <= 3) err = run_staged<KIND, D, 3>(a, c, P, smem, s);
+    else if (svpt <= 4) err = run_staged<KIND, D, 4>(a, c, P, smem, s);
+    else if constexpr (VEC == 4) {
+      if (svpt <= 6) err = run_staged<KIND, D, 6>(a, c, P, smem, s);
+      else err = run_staged<KIND, D, 8>(a, c, P, smem, s);
     }
-    if (tpr <= 1024) {
-      a.tpr = tpr;
-      const int rpc = tpr <= 256 ? 256 / tpr : 1;
-      const int threads = rpc * tpr;
-      P = (int)std::min<int64_t>((a.N + rpc - 1) / rpc, p_max);
-      size_t smem_f = (size_t)((rpc * 2 * (tpr / 32) * NS + 3) & ~3);
-      if (rpc > 1 && want) smem_f += 2 * (size_t)a.Hp;
-      const size_t smem = smem_f * sizeof(float);
-      if (threads <= 256) {
-        switch (vpt) {
-          case 1: err = run_reg<KIND, D, 1, 256>(a, threads, P, smem, s); break;
-          case 2: err = run_reg<KIND, D, 2, 256>(a, threads, P, smem, s); break;
-          default:
-            if constexpr (VPT_MAX >= 4) err = run_reg<KIND, D, 4, 256>(a, threads, P, smem, s);
-            break;
-        }
-      } else {
-        err = run_reg<KIND, D, VPT_MAX, 1024>(a, threads, P, smem, s);
+    done = true;
+  }
+  // Register rows; the grid is persistent: as many CTAs as fit, at most
+  // 2 x SM count (the partial rows the workspace holds).
+  if (!done && use_rows) {
+    a.tpr = tpr;
+    const int rpc = tpr <= 256 ? 256 / tpr : 1;
+    const int threads = rpc * tpr;
+    const int p_cap = (int)std::min<int64_t>((a.N + rpc - 1) / rpc, p_max);
+    size_t smem_f = (size_t)((rpc * 2 * (tpr / 32) * NS + 3) & ~3);
+    if (want || rpc == 1) smem_f += 2 * (size_t)a.Hp;  // fold buffer / shared accumulators
+    const size_t smem = smem_f * sizeof(float);
+    if (threads <= 256) {
+      switch (vpt) {
+        case 1: err = run_rows<KIND, D, 1, 256, 2>(a, threads, &P, p_cap, smem, dev, s); break;
+        case 2: err = run_rows<KIND, D, 2, 256, 2>(a, threads, &P, p_cap, smem, dev, s); break;
+        default:
+          if constexpr (VPT_MAX >= 4) err = run_rows<KIND, D, 4, 256, 2>(a, threads, &P, p_cap, smem, dev, s);
+          break;
       }
-      done = true;
+    } else if (threads <= 640) {
+      err = run_rows<KIND, D, VPT_MAX, 640, 1, true>(a, threads, &P, p_cap, smem, dev, s);
+    } else {
+      err = run_rows<KIND, D, VPT_MAX, 1024, 1, true>(a, threads, &P, p_cap, smem, dev, s);
     }
+    done = true;
   }
   if (!done) {
     P = (int)std::min<int64_t>(a.N, p_max);

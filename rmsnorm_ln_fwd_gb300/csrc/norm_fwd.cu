@@ -7,10 +7,10 @@
 //   consumer row groups compute from shared memory.  Needs 16-byte aligned
 //   rows, H a multiple of the vector width and at least three stages of rows
 //   in shared memory.
-// * fwd_reg_kernel -- the row lives in registers.  A "row group" of `tpr`
+// * fwd_rows_kernel -- the row lives in registers.  A "row group" of `tpr`
 //   threads (one warp for narrow rows, up to 1024 threads for wide rows) owns
-//   one row at a time; each thread holds VPT 16-byte vectors of it, so HBM is
-//   read exactly once and written exactly once.  Vector v of thread t covers
+//   one row at a time and prefetches its next; each thread holds VPT 16-byte
+//   vectors of it, so HBM is read exactly once and written exactly once.  Vector v of thread t covers
 //   columns [(v*tpr + t)*VEC, +VEC): consecutive threads touch consecutive
 //   16-byte chunks, so every warp-wide access is fully coalesced.  Needs
 //   16-byte aligned rows and H a multiple of the vector width.
@@ -41,10 +41,16 @@
 
 namespace normk {
 
-template <int KIND, typename D, int VPT, int MAXT>
-__global__ void __launch_bounds__(MAXT) fwd_reg_kernel(const FwdArgs a) {
+// Register-row kernel.  Persistent row groups of `tpr` threads walk rows
+// row, row + stride, ...; while a group computes one row, the 16-byte loads
+// of its next row are already in flight (software pipelining), so each warp
+// keeps two rows' worth of HBM reads outstanding.  Each row is unpacked once
+// into fp32 pairs and every elementwise step uses packed f32x2 instructions.
+template <int KIND, typename D, int VPT, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
   using T = typename D::T;
   constexpr int VEC = D::VEC;
+  constexpr int VP = VEC / 2;
   extern __shared__ float sh_dyn[];
   const int tpr = a.tpr;
   const int rpc = blockDim.x / tpr;
@@ -54,85 +60,105 @@ __global__ void __launch_bounds__(MAXT) fwd_reg_kernel(const FwdArgs a) {
   const int wig = t >> 5;
   const int lane = threadIdx.x & 31;
   const int H = a.H;
+  const int hv = H / VEC;
   const float inv_h = 1.f / (float)H;
   const bool w_f32 = a.w_f32 != 0;
   float* sh = sh_dyn + slot * (2 * nw * 3);
   const int bar_id = 1 + slot;
   const int64_t stride = (int64_t)gridDim.x * rpc;
-  int parity = 0;
+  int nvec = 0;  // vectors of each row this thread owns
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
 
-  for (int64_t row = (int64_t)blockIdx.x * rpc + slot; row < a.N; row += stride) {
-    const T* xrow = reinterpret_cast<const T*>(a.x) + row * a.ldx;
-    // Issue every 16-byte load of the row before the first use.
-    uint4 raw[VPT];
+  uint4 nx[VPT], nr[VPT];
+  float npivot = 0.f;
+  auto fetch = [&](int64_t r) {
+    const T* xrow = reinterpret_cast<const T*>(a.x) + r * a.ldx;
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) raw[v] = load_vec_or_zero<D>(xrow, (v * tpr + t) * VEC, H);
-    float f[VPT][VEC];
+    for (int v = 0; v < VPT; ++v) nx[v] = load_vec_or_zero<D>(xrow, (t + v * tpr) * VEC, H);
     if constexpr (KIND == KIND_FUSED) {
-      const T* rrow = reinterpret_cast<const T*>(a.res) + row * a.ldr;
-      uint4 rraw[VPT];
+      const T* rrow = reinterpret_cast<const T*>(a.res) + r * a.ldr;
 #pragma unroll
-      for (int v = 0; v < VPT; ++v) rraw[v] = load_vec_or_zero<D>(rrow, (v * tpr + t) * VEC, H);
+      for (int v = 0; v < VPT; ++v) nr[v] = load_vec_or_zero<D>(rrow, (t + v * tpr) * VEC, H);
+    }
+    if constexpr (KIND == KIND_LN) npivot = load_elem<D>(xrow, 0);
+  };
+
+  int parity = 0;
+  int64_t row = (int64_t)blockIdx.x * rpc + slot;
+  if (row < a.N) fetch(row);
+  for (; row < a.N; row += stride) {
+    // Unpack the current row (it arrived while the previous row computed).
+    float2 f[VPT][VP];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) unpack2<D>(nx[v], f[v]);
+    const float pivot = npivot;
+    if constexpr (KIND == KIND_FUSED) {
       T* hrow = reinterpret_cast<T*>(a.h) + row * a.ldh;
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
-        const int c = (v * tpr + t) * VEC;
-        float r[VEC];
-        unpack<D>(raw[v], f[v]);
-        unpack<D>(rraw[v], r);
+        float2 r[VP];
+        unpack2<D>(nr[v], r);
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) f[v][i] += r[i];
-        if (c < H) store_vec<D>(hrow, c, f[v]);
+        for (int p = 0; p < VP; ++p) f[v][p] = add2(f[v][p], r[p]);
+        if (v < nvec) st_vec(reinterpret_cast<T*>(hrow) + (t + v * tpr) * VEC, pack2<D>(f[v]));
       }
-    } else {
-#pragma unroll
-      for (int v = 0; v < VPT; ++v) unpack<D>(raw[v], f[v]);
     }
+    // Issue the next row's loads before computing this one.
+    if (row + stride < a.N) fetch(row + stride);
 
-    float rstd, mean_d = 0.f, pivot = 0.f;
+    float rstd, mean_d = 0.f;
     if constexpr (KIND == KIND_LN) {
-      pivot = load_elem<D>(xrow, 0);
-      // This thread's Welford triple by two passes over its own values, then
-      // the parallel merge across the row group.
-      int nvec = 0;
-      float s = 0.f;
+      // This thread's Welford triple (count, mean, M2) by two passes over its
+      // own values, then the parallel merge across the row group.
+      const float2 pv = splat2(pivot);
+      float2 s2 = splat2(0.f);
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
-        if ((v * tpr + t) * VEC < H) {
-          ++nvec;
+        if (v < nvec) {
 #pragma unroll
-          for (int i = 0; i < VEC; ++i) {
-            f[v][i] -= pivot;
-            s += f[v][i];
-          }
+          for (int p = 0; p < VP; ++p) f[v][p] = sub2(f[v][p], pv);
+          float2 vs = f[v][0];
+#pragma unroll
+          for (int p = 1; p < VP; ++p) vs = add2(vs, f[v][p]);
+          s2 = add2(s2, vs);
         }
       }
       const float cnt = (float)(nvec * VEC);
-      const float m = nvec > 0 ? s / cnt : 0.f;
-      float m2 = 0.f;
+      const float mloc = nvec > 0 ? __fdividef(s2.x + s2.y, cnt) : 0.f;
+      const float2 ml = splat2(mloc);
+      float2 q2 = splat2(0.f);
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
-        if ((v * tpr + t) * VEC < H) {
+        if (v < nvec) {
+          float2 e = sub2(f[v][0], ml);
+          float2 vq = mul2(e, e);
 #pragma unroll
-          for (int i = 0; i < VEC; ++i) {
-            const float e = f[v][i] - m;
-            m2 = fmaf(e, e, m2);
+          for (int p = 1; p < VP; ++p) {
+            e = sub2(f[v][p], ml);
+            vq = fma2(e, e, vq);
           }
+          q2 = add2(q2, vq);
         }
       }
-      const Welford w = group_welford(Welford{cnt, m, m2}, sh, nw, wig, lane, bar_id, parity);
+      const Welford w = group_welford(Welford{cnt, mloc, q2.x + q2.y}, sh, nw, wig, lane, bar_id, parity);
       mean_d = w.m;
       rstd = rsqrtf(w.m2 * inv_h + a.eps);
     } else {
-      float ss[1] = {0.f};
+      float2 s2 = splat2(0.f);
 #pragma unroll
-      for (int v = 0; v < VPT; ++v)
+      for (int v = 0; v < VPT; ++v) {
+        if (v < nvec) {
+          float2 vq = mul2(f[v][0], f[v][0]);
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) ss[0] = fmaf(f[v][i], f[v][i], ss[0]);
+          for (int p = 1; p < VP; ++p) vq = fma2(f[v][p], f[v][p], vq);
+          s2 = add2(s2, vq);
+        }
+      }
+      float ss[1] = {s2.x + s2.y};
       group_sum<1>(ss, sh, nw, wig, lane, bar_id, parity);
       rstd = rsqrtf(ss[0] * inv_h + a.eps);
     }
-
     if (t == 0) {
       if constexpr (KIND == KIND_LN) {
         if (a.mean) a.mean[row] = pivot + mean_d;
@@ -141,27 +167,29 @@ __global__ void __launch_bounds__(MAXT) fwd_reg_kernel(const FwdArgs a) {
     }
 
     T* yrow = reinterpret_cast<T*>(a.y) + row * a.ldy;
+    const float2 r2 = splat2(rstd);
+    const float2 b2 = splat2(-mean_d * rstd);
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
-      const int c = (v * tpr + t) * VEC;
-      if (c >= H) continue;
-      float g[VEC], out[VEC];
-      load_param_vec<D>(a.gamma, c, w_f32, 1.f, g);
-      if constexpr (KIND == KIND_LN) {
-        float b[VEC];
-        load_param_vec<D>(a.beta, c, w_f32, 0.f, b);
+      if (v < nvec) {
+        const int col = (t + v * tpr) * VEC;
+        float2 gm[VP], out[VP];
+        load_param_pairs<D>(a.gamma, col, w_f32, 1.f, gm);
+        if constexpr (KIND == KIND_LN) {
+          float2 be[VP];
+          load_param_pairs<D>(a.beta, col, w_f32, 0.f, be);
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) out[i] = fmaf((f[v][i] - mean_d) * rstd, g[i], b[i]);
-      } else {
+          for (int p = 0; p < VP; ++p) out[p] = fma2(fma2(f[v][p], r2, b2), gm[p], be[p]);
+        } else {
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) out[i] = (f[v][i] * rstd) * g[i];
+          for (int p = 0; p < VP; ++p) out[p] = mul2(mul2(f[v][p], r2), gm[p]);
+        }
+        st_vec(yrow + col, pack2<D>(out));
       }
-      store_vec<D>(yrow, c, out);
     }
     parity ^= 1;
   }
 }
-
 
 #ifndef NORM_STAGED_MAX_STAGES
 #define NORM_STAGED_MAX_STAGES 6
@@ -193,7 +221,11 @@ bool staged_config(int H, int es, int NT, int max_smem, int max_cols, StageCfg* 
 
 size_t staged_smem_bytes(const StageCfg& c, int NT) { return c.data_off + (size_t)c.S * NT * c.G * c.row_bytes; }
 
-template <int KIND, typename D>
+// Consumers copy their VPT vectors of the row from shared memory into packed
+// registers, release the stage at once (the producer can refill it while they
+// compute), and run every pass from registers.  Per-thread sums are formed per
+// 16-byte vector as a short tree, so no pass is one long dependent add chain.
+template <int KIND, typename D, int VPT>
 __global__ void __launch_bounds__(kStagedThreads, 1) fwd_staged_kernel(const FwdArgs a, const StageCfg c) {
   using T = typename D::T;
   constexpr int VEC = D::VEC;
@@ -232,108 +264,129 @@ __global__ void __launch_bounds__(kStagedThreads, 1) fwd_staged_kernel(const Fwd
   const int t = wig * 32 + lane;
   float* sh = m.red + g * (2 * nwg * 3);
   const int bar_id = 1 + g;
+  int nvec = 0;  // vectors of each row this thread owns
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
   int parity = 0;
   int k = 0;
   for (int64_t row0 = lo; row0 < hi; row0 += c.G, ++k) {
     const int s = k % c.S;
     const bool have = mbar_wait(&m.full[s], (k / c.S) & 1, c.err, m.abort);
     const int64_t row = row0 + g;
-    if (row < hi) {  // uniform across the row group
+    const bool mine = row < hi;  // uniform across the row group
+    uint4 xr[VPT], rr[VPT];
+    float pivot = 0.f;
+    if (mine) {
       const T* xs = staged_row<T>(m, c, NT, s, 0, g);
-      float rstd, mean_d = 0.f, pivot = 0.f;
-      if constexpr (KIND == KIND_LN) {
-        // This thread's Welford triple by two passes over its vectors, then
-        // the parallel merge across the row group.
-        pivot = load_elem<D>(xs, 0);
-        float sum = 0.f;
-        int nvec = 0;
-#pragma unroll 4
-        for (int j = t; j < hv; j += tpr) {
-          float f[VEC];
-          unpack<D>(lds16(xs + j * VEC), f);
 #pragma unroll
-          for (int i = 0; i < VEC; ++i) sum += f[i] - pivot;
-          ++nvec;
+      for (int v = 0; v < VPT; ++v) {
+        const int j = t + v * tpr;
+        xr[v] = j < hv ? lds16(xs + j * VEC) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      if constexpr (NT == 2) {
+        const T* rs = staged_row<T>(m, c, NT, s, 1, g);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int j = t + v * tpr;
+          rr[v] = j < hv ? lds16(rs + j * VEC) : make_uint4(0u, 0u, 0u, 0u);
         }
-        const float cnt = (float)(nvec * VEC);
-        const float mloc = nvec > 0 ? sum / cnt : 0.f;
-        float m2 = 0.f;
-#pragma unroll 4
-        for (int j = t; j < hv; j += tpr) {
+      }
+      if constexpr (KIND == KIND_LN) pivot = load_elem<D>(xs, 0);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&m.empty[s]);  // the row is in registers: the stage may be refilled
+    parity ^= 1;
+    if (!mine) continue;
+
+    float rstd, mean_d = 0.f;
+    if constexpr (KIND == KIND_LN) {
+      // This thread's Welford triple by two passes over its own values, then
+      // the parallel merge across the row group.
+      float sum = 0.f;
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        if (v < nvec) {
           float f[VEC];
-          unpack<D>(lds16(xs + j * VEC), f);
+          unpack<D>(xr[v], f);
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) f[i] -= pivot;
+          sum += tree_sum<VEC>(f);
+        }
+      }
+      const float cnt = (float)(nvec * VEC);
+      const float mloc = nvec > 0 ? sum / cnt : 0.f;
+      float m2 = 0.f;
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        if (v < nvec) {
+          float f[VEC];
+          unpack<D>(xr[v], f);
 #pragma unroll
           for (int i = 0; i < VEC; ++i) {
             const float e = (f[i] - pivot) - mloc;
-            m2 = fmaf(e, e, m2);
+            f[i] = e * e;
           }
+          m2 += tree_sum<VEC>(f);
         }
-        const Welford w = group_welford(Welford{cnt, mloc, m2}, sh, nwg, wig, lane, bar_id, parity);
-        mean_d = w.m;
-        rstd = rsqrtf(w.m2 * inv_h + a.eps);
-      } else {
-        float ss[1] = {0.f};
-        if constexpr (KIND == KIND_FUSED) {
-          const T* rs = staged_row<T>(m, c, NT, s, 1, g);
-          T* hrow = reinterpret_cast<T*>(a.h) + row * a.ldh;
-#pragma unroll 4
-          for (int j = t; j < hv; j += tpr) {
-            float f[VEC], r[VEC];
-            unpack<D>(lds16(xs + j * VEC), f);
-            unpack<D>(lds16(rs + j * VEC), r);
-#pragma unroll
-            for (int i = 0; i < VEC; ++i) {
-              f[i] += r[i];
-              ss[0] = fmaf(f[i], f[i], ss[0]);
-            }
-            if (have) store_vec<D>(hrow, j * VEC, f);
-          }
-        } else {
-#pragma unroll 4
-          for (int j = t; j < hv; j += tpr) {
-            float f[VEC];
-            unpack<D>(lds16(xs + j * VEC), f);
-#pragma unroll
-            for (int i = 0; i < VEC; ++i) ss[0] = fmaf(f[i], f[i], ss[0]);
-          }
-        }
-        group_sum<1>(ss, sh, nwg, wig, lane, bar_id, parity);
-        rstd = rsqrtf(ss[0] * inv_h + a.eps);
       }
-      if (t == 0 && have) {
-        if constexpr (KIND == KIND_LN) {
-          if (a.mean) a.mean[row] = pivot + mean_d;
+      const Welford w = group_welford(Welford{cnt, mloc, m2}, sh, nwg, wig, lane, bar_id, parity ^ 1);
+      mean_d = w.m;
+      rstd = rsqrtf(w.m2 * inv_h + a.eps);
+    } else {
+      float ss[1] = {0.f};
+      T* hrow = reinterpret_cast<T*>(a.h) + row * a.ldh;
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        if (v < nvec) {
+          float f[VEC];
+          unpack<D>(xr[v], f);
+          if constexpr (KIND == KIND_FUSED) {
+            float r[VEC];
+            unpack<D>(rr[v], r);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) f[i] += r[i];
+            if (have) store_vec<D>(hrow, (t + v * tpr) * VEC, f);
+          }
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) f[i] *= f[i];
+          ss[0] += tree_sum<VEC>(f);
         }
-        if (a.rstd) a.rstd[row] = rstd;
       }
-      T* yrow = reinterpret_cast<T*>(a.y) + row * a.ldy;
-      const T* rs = KIND == KIND_FUSED ? staged_row<T>(m, c, NT, s, 1, g) : nullptr;
-#pragma unroll 4
-      for (int j = t; j < hv; j += tpr) {
+      group_sum<1>(ss, sh, nwg, wig, lane, bar_id, parity ^ 1);
+      rstd = rsqrtf(ss[0] * inv_h + a.eps);
+    }
+    if (t == 0 && have) {
+      if constexpr (KIND == KIND_LN) {
+        if (a.mean) a.mean[row] = pivot + mean_d;
+      }
+      if (a.rstd) a.rstd[row] = rstd;
+    }
+    T* yrow = reinterpret_cast<T*>(a.y) + row * a.ldy;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      if (v < nvec) {
+        const int col = (t + v * tpr) * VEC;
         float f[VEC], gm[VEC], out[VEC];
-        unpack<D>(lds16(xs + j * VEC), f);
-        load_param_vec<D>(a.gamma, j * VEC, w_f32, 1.f, gm);
+        unpack<D>(xr[v], f);
+        load_param_vec<D>(a.gamma, col, w_f32, 1.f, gm);
         if constexpr (KIND == KIND_LN) {
           float b[VEC];
-          load_param_vec<D>(a.beta, j * VEC, w_f32, 0.f, b);
+          load_param_vec<D>(a.beta, col, w_f32, 0.f, b);
 #pragma unroll
           for (int i = 0; i < VEC; ++i) out[i] = fmaf(((f[i] - pivot) - mean_d) * rstd, gm[i], b[i]);
         } else {
           if constexpr (KIND == KIND_FUSED) {
             float r[VEC];
-            unpack<D>(lds16(rs + j * VEC), r);
+            unpack<D>(rr[v], r);
 #pragma unroll
             for (int i = 0; i < VEC; ++i) f[i] += r[i];
           }
 #pragma unroll
           for (int i = 0; i < VEC; ++i) out[i] = (f[i] * rstd) * gm[i];
         }
-        if (have) store_vec<D>(yrow, j * VEC, out);
+        if (have) store_vec<D>(yrow, col, out);
       }
     }
-    parity ^= 1;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&m.empty[s]);
   }
 }
 
@@ -423,26 +476,50 @@ __global__ void __launch_bounds__(LOOP_THREADS) fwd_loop_kernel(const FwdArgs a)
 
 static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Persistent grid for the row kernels: as many CTAs as fit on the GPU at
+// once (queried per kernel), or fewer when there are fewer row groups.
+template <typename K>
+static int64_t persistent_blocks(K kern, int threads, size_t smem, const DeviceInfo& dev, int64_t want) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  return std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)per_sm * dev.sm_count));
+}
+
 template <int KIND, typename D, int VPT>
-static cudaError_t run_reg(const FwdArgs& a, int threads, int64_t blocks, size_t smem, cudaStream_t s) {
+static cudaError_t run_rows(const FwdArgs& a, int threads, int rpc, size_t smem, const DeviceInfo& dev,
+                            cudaStream_t s) {
+  const int64_t groups = (a.N + rpc - 1) / rpc;
   if (threads <= 256) {
-    fwd_reg_kernel<KIND, D, VPT, 256><<<(unsigned)blocks, threads, smem, s>>>(a);
+    auto kern = fwd_rows_kernel<KIND, D, VPT, 256, (VPT * D::VEC > 16 ? 2 : 3)>;
+    kern<<<(unsigned)persistent_blocks(kern, threads, smem, dev, groups), threads, smem, s>>>(a);
+  } else if (threads <= 640) {
+    auto kern = fwd_rows_kernel<KIND, D, VPT, 640, 1>;
+    kern<<<(unsigned)persistent_blocks(kern, threads, smem, dev, groups), threads, smem, s>>>(a);
   } else {
-    fwd_reg_kernel<KIND, D, VPT, 1024><<<(unsigned)blocks, threads, smem, s>>>(a);
+    auto kern = fwd_rows_kernel<KIND, D, VPT, 1024, 1>;
+    kern<<<(unsigned)persistent_blocks(kern, threads, smem, dev, groups), threads, smem, s>>>(a);
   }
   return cudaGetLastError();
 }
 
-// Register path: rows 16-byte aligned and H a multiple of the vector width.
-// Narrow rows get one warp each (VPT = smallest power of two covering H, up to
-// 32 elements per thread, 8 rows per 256-thread CTA); wider rows keep 32
-// elements per thread and add warps: tpr = ceil(H / 32) rounded up to a warp,
-// up to 1024 threads (H <= 32768).  Everything else takes the loop path.
+template <int KIND, typename D, int VPT>
+static cudaError_t run_staged(const FwdArgs& a, const StageCfg& c, int64_t blocks, size_t smem, cudaStream_t s) {
+  auto kern = fwd_staged_kernel<KIND, D, VPT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)blocks, kStagedThreads, smem, s>>>(a, c);
+  return cudaGetLastError();
+}
+
 template <int KIND, typename D>
 static cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream_t s) {
   using T = typename D::T;
   constexpr int VEC = D::VEC;
-  constexpr int VPT_MAX = 32 / VEC;
+  // Elements a thread: 32 for bf16 LayerNorm/RMSNorm (halves the per-row
+  // reduction overhead per element), else 16 (fused keeps two rows' inputs in
+  // flight; fp32 takes twice the registers per element).
+  constexpr int VPT_MAX = (KIND != KIND_FUSED && VEC == 8) ? 4 : 16 / VEC;
   const size_t es = sizeof(T);
   bool aligned = aligned16(a.x) && aligned16(a.y) && (a.ldx * es) % 16 == 0 && (a.ldy * es) % 16 == 0;
   if (a.gamma) aligned = aligned && aligned16(a.gamma);
@@ -451,46 +528,65 @@ static cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream
     aligned = aligned && aligned16(a.res) && aligned16(a.h) && (a.ldr * es) % 16 == 0 &&
               (a.ldh * es) % 16 == 0;
   }
-  if (dev.path <= PATH_STAGED && aligned && a.H % VEC == 0) {
-    StageCfg c{};
-    constexpr int NT = KIND == KIND_FUSED ? 2 : 1;
-    if (staged_config(a.H, (int)es, NT, dev.max_smem_optin, 0, &c)) {
-      c.err = dev.err;
-      c.contiguous = a.ldx == a.H && (NT == 1 || a.ldr == a.H);
-      const size_t smem = staged_smem_bytes(c, NT);
-      auto kern = fwd_staged_kernel<KIND, D>;
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      const int64_t blocks = std::min<int64_t>((int64_t)dev.sm_count, (a.N + c.G - 1) / c.G);
-      kern<<<(unsigned)blocks, kStagedThreads, smem, s>>>(a, c);
-      return cudaGetLastError();
+  // Register-row shape: narrow rows one warp each (VPT = smallest power of
+  // two covering H), wider rows 16 elements a thread with more warps.
+  const bool vec_ok = aligned && a.H % VEC == 0;
+  const int Hv = a.H / VEC;
+  int vpt = VPT_MAX, tpr = 0;
+  if (Hv <= 32 * VPT_MAX) {
+    tpr = 32;
+    vpt = 1;
+    while (vpt * 32 < Hv) vpt *= 2;
+  } else {
+    tpr = ((Hv + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32;
+  }
+  const bool rows_ok = vec_ok && tpr <= 1024;
+  StageCfg c{};
+  constexpr int NT = KIND == KIND_FUSED ? 2 : 1;
+  // Staged consumers keep at most 8 packed vectors of each tensor.
+  const bool staged_ok = vec_ok && staged_config(a.H, (int)es, NT, dev.max_smem_optin, (8 / NT) * VEC, &c);
+  bool use_rows = false, use_staged = false;
+  switch (dev.path) {
+    case PATH_AUTO:
+      use_rows = rows_ok && tpr <= kRowsAutoMaxThreads;
+      use_staged = !use_rows && staged_ok;
+      use_rows = use_rows || (!use_staged && rows_ok);
+      break;
+    case PATH_ROWS: use_rows = rows_ok; break;
+    case PATH_STAGED:
+      use_staged = staged_ok;
+      use_rows = !use_staged && rows_ok;
+      break;
+    default: break;
+  }
+  if (use_staged) {
+    c.err = dev.err;
+    c.contiguous = a.ldx == a.H && (NT == 1 || a.ldr == a.H);
+    const int stpr = 32 * (c.W / c.G);
+    const int svpt = (Hv + stpr - 1) / stpr;
+    const size_t smem = staged_smem_bytes(c, NT);
+    const int64_t blocks = std::min<int64_t>((int64_t)dev.sm_count, (a.N + c.G - 1) / c.G);
+    if (svpt <= 1) return run_staged<KIND, D, 1>(a, c, blocks, smem, s);
+    if (svpt <= 2) return run_staged<KIND, D, 2>(a, c, blocks, smem, s);
+    if (svpt <= 3) return run_staged<KIND, D, 3>(a, c, blocks, smem, s);
+    if (svpt <= 4) return run_staged<KIND, D, 4>(a, c, blocks, smem, s);
+    if constexpr (NT == 1) {
+      if (svpt <= 5) return run_staged<KIND, D, 5>(a, c, blocks, smem, s);
+      if (svpt <= 6) return run_staged<KIND, D, 6>(a, c, blocks, smem, s);
+      return run_staged<KIND, D, 8>(a, c, blocks, smem, s);
     }
   }
-  if (dev.path <= PATH_REGISTER && aligned && a.H % VEC == 0) {
-    const int Hv = a.H / VEC;
-    int vpt, tpr;
-    if (Hv <= 32 * VPT_MAX) {
-      tpr = 32;
-      vpt = 1;
-      while (vpt * 32 < Hv) vpt *= 2;
-    } else {
-      vpt = VPT_MAX;
-      tpr = ((Hv + vpt - 1) / vpt + 31) / 32 * 32;
-    }
-    if (tpr <= 1024) {
-      a.tpr = tpr;
-      const int rpc = tpr <= 256 ? 256 / tpr : 1;
-      const int threads = rpc * tpr;
-      const int64_t blocks = std::min<int64_t>((a.N + rpc - 1) / rpc, 0x7fffffff);
-      const size_t smem = (size_t)rpc * 2 * (tpr / 32) * 3 * sizeof(float);
-      switch (vpt) {
-        case 1: return run_reg<KIND, D, 1>(a, threads, blocks, smem, s);
-        case 2: return run_reg<KIND, D, 2>(a, threads, blocks, smem, s);
-        case 4: return run_reg<KIND, D, 4>(a, threads, blocks, smem, s);
-        default:
-          if constexpr (VPT_MAX >= 8) return run_reg<KIND, D, 8>(a, threads, blocks, smem, s);
-          break;
-      }
+  if (use_rows) {
+    a.tpr = tpr;
+    const int rpc = tpr <= 256 ? 256 / tpr : 1;
+    const int threads = rpc * tpr;
+    const size_t smem = (size_t)rpc * 2 * (tpr / 32) * 3 * sizeof(float);
+    switch (vpt) {
+      case 1: return run_rows<KIND, D, 1>(a, threads, rpc, smem, dev, s);
+      case 2: return run_rows<KIND, D, 2>(a, threads, rpc, smem, dev, s);
+      default:
+        if constexpr (VPT_MAX >= 4) return run_rows<KIND, D, 4>(a, threads, rpc, smem, dev, s);
+        break;
     }
   }
   const int64_t blocks = std::min<int64_t>(a.N, (int64_t)dev.sm_count * 8);

@@ -120,26 +120,29 @@ def rms_y_scale(x, rstd, gamma):
 
 
 def ln_dx_scale(dy, x, gamma, eps):
-    """Magnitude of the terms of dx_i = rstd * (g_i - c1 - x_hat_i * c2), with
-    x_hat's own error scale (|x_i - mean| + |mean| + sigma) * rstd."""
+    """Magnitude of what dx_i = rstd * (g_i - c1 - x_hat_i * c2) is formed
+    from: x_hat's error scale (|x_i - mean| + |mean| + sigma) * rstd, and the
+    row sums c1 = mean(g), c2 = mean(g * x_hat), whose fp32 error scales with
+    mean|g| and mean|g * x_hat| rather than with their (cancelling) values."""
     H = x.shape[1]
     g = dy * (np.ones(H) if gamma is None else gamma)
     mean, var = O.two_pass_stats(x)
     r = 1.0 / np.sqrt(var + eps)
     xh = (x - mean[:, None]) * r[:, None]
     spread = (np.abs(x - mean[:, None]) + (np.abs(mean) + np.sqrt(var))[:, None]) * r[:, None]
-    c1 = g.mean(axis=1, keepdims=True)
-    c2 = (g * xh).mean(axis=1, keepdims=True)
-    return r[:, None] * (np.abs(g) + np.abs(c1) + spread * np.abs(c2))
+    c1 = np.abs(g).mean(axis=1, keepdims=True)
+    c2 = np.abs(g * xh).mean(axis=1, keepdims=True)
+    return r[:, None] * (np.abs(g) + c1 + spread * c2)
 
 
 def rms_dx_scale(dy, x, gamma, eps):
+    """As ln_dx_scale, for dx_i = rstd * (g_i - x_hat_i * c2)."""
     H = x.shape[1]
     g = dy * (np.ones(H) if gamma is None else gamma)
     r = 1.0 / np.sqrt((x * x).mean(axis=1) + eps)
     xh = x * r[:, None]
-    c2 = (g * xh).mean(axis=1, keepdims=True)
-    return r[:, None] * (np.abs(g) + np.abs(xh * c2))
+    c2 = np.abs(g * xh).mean(axis=1, keepdims=True)
+    return r[:, None] * (np.abs(g) + np.abs(xh) * c2)
 
 
 # --------------------------------------------------------------------------

@@ -131,9 +131,9 @@ def test_backward_validation(lib):
 
 
 def test_kernel_path_override_validation(lib):
-    assert lib.norm_set_kernel_path(3) == INVALID
+    assert lib.norm_set_kernel_path(4) == INVALID
     assert lib.norm_set_kernel_path(-1) == INVALID
-    for p in (2, 1, 0):
+    for p in (3, 2, 1, 0):
         assert lib.norm_set_kernel_path(p) == OK
 
 

@@ -369,11 +369,12 @@ def test_device_side_errors():
 
 
 # ---------------------------------------------------------------------------
-# every kernel family on the same shapes: 0 = bulk-copy pipeline (default),
-# 1 = register rows, 2 = strided loop
+# every kernel family on the same shapes (the default policy is covered by
+# every test above): 1 = register rows, 2 = strided loop, 3 = bulk-copy
+# pipeline
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("path", [1, 2], ids=["register", "loop"])
+@pytest.mark.parametrize("path", [1, 2, 3], ids=["rows", "loop", "staged"])
 @pytest.mark.parametrize("H,dt", [(1024, BF), (5120, BF), (16384, BF), (2048, F32), (256, F32), (96, BF)])
 def test_forced_kernel_paths(path, H, dt):
     nl._lib.set_kernel_path(path)
