@@ -456,4 +456,49 @@ __device__ __forceinline__ void load_param_pairs(const void* p, int c, bool w_f3
   }
 }
 
+// ---------------------------------------------------------------------------
+// Per-CTA fp32 copies of gamma/beta for persistent row kernels.  A thread's
+// columns never change, so the parameters are converted once and laid out
+// thread-interleaved: float4 slot (v * VEC/4 + q) of thread t sits at
+// [slot * tpr + t] and holds columns (t + v*tpr)*VEC + 4q .. +3.  Each thread
+// reads only its own slots, with conflict-free 16-byte shared loads.
+// ---------------------------------------------------------------------------
+template <typename D, int VPT>
+__device__ __forceinline__ void stage_params(float4* dst, const void* p, bool w_f32, float fill, int t, int tpr,
+                                             int hv) {
+  constexpr int VEC = D::VEC;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int j = t + v * tpr;
+    float2 pr[VEC / 2];
+    if (j < hv) {
+      load_param_pairs<D>(p, j * VEC, w_f32, fill, pr);
+    } else {
+#pragma unroll
+      for (int i = 0; i < VEC / 2; ++i) pr[i] = splat2(0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < VEC / 4; ++q)
+      dst[(v * (VEC / 4) + q) * tpr + t] = make_float4(pr[2 * q].x, pr[2 * q].y, pr[2 * q + 1].x, pr[2 * q + 1].y);
+  }
+}
+
+// The VEC/2 pairs of vector v of this thread from a thread-interleaved array.
+template <int VEC>
+__device__ __forceinline__ void read_pairs(const float4* src, int v, int t, int tpr, float2* out) {
+#pragma unroll
+  for (int q = 0; q < VEC / 4; ++q) {
+    const float4 u = src[(v * (VEC / 4) + q) * tpr + t];
+    out[2 * q] = make_float2(u.x, u.y);
+    out[2 * q + 1] = make_float2(u.z, u.w);
+  }
+}
+
+template <int VEC>
+__device__ __forceinline__ void write_pairs(float4* dst, int v, int t, int tpr, const float2* in) {
+#pragma unroll
+  for (int q = 0; q < VEC / 4; ++q)
+    dst[(v * (VEC / 4) + q) * tpr + t] = make_float4(in[2 * q].x, in[2 * q].y, in[2 * q + 1].x, in[2 * q + 1].y);
+}
+
 }  // namespace normk

@@ -71,16 +71,27 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
 #pragma unroll
     for (int p = 0; p < VP; ++p) acc_g[v][p] = acc_b[v][p] = splat2(0.f);
   const int Hp = a.Hp;
-  const int red_off = ((rpc * 2 * nw * NS) + 3) & ~3;
-  float* sacc_g = sh_dyn + red_off;  // ACC_SMEM: [Hp] dgamma then [Hp] dbeta
-  float* sacc_b = sacc_g + Hp;
+  // Shared memory: group scratch | fp32 gamma (thread-interleaved, shared by
+  // the row slots) | accumulators (ACC_SMEM, thread-interleaved: dgamma then
+  // dbeta) or the fold buffer of the row slots.
+  const int off_g = ((rpc * 2 * nw * NS) + 3) & ~3;
+  const int slots = VPT * VEC * tpr;  // floats of one thread-interleaved array
+  float4* gs = reinterpret_cast<float4*>(sh_dyn + off_g);
+  float* sh_acc = sh_dyn + off_g + slots;
+  float4* sacc_g = reinterpret_cast<float4*>(sh_acc);
+  float4* sacc_b = sacc_g + slots / 4;
+  if (slot == 0) stage_params<D, VPT>(gs, a.gamma, w_f32, 1.f, t, tpr, hv);
   if constexpr (ACC_SMEM) {
-    for (int k = threadIdx.x * 4; k < Hp; k += blockDim.x * 4) {
-      *reinterpret_cast<float4*>(sacc_g + k) = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (LN) *reinterpret_cast<float4*>(sacc_b + k) = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      float2 z[VP];
+#pragma unroll
+      for (int p = 0; p < VP; ++p) z[p] = splat2(0.f);
+      write_pairs<VEC>(sacc_g, v, t, tpr, z);
+      if (LN) write_pairs<VEC>(sacc_b, v, t, tpr, z);
     }
-    __syncthreads();
   }
+  __syncthreads();
 
   uint4 nx[VPT], nd[VPT];
   float nrs = 0.f, nmu = 0.f;
@@ -127,7 +138,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
       if (v < nvec) {
         float2 d[VP], gm[VP];
         unpack2<D>(dcur[v], d);
-        load_param_pairs<D>(a.gamma, (t + v * tpr) * VEC, w_f32, 1.f, gm);
+        read_pairs<VEC>(gs, v, t, tpr, gm);
 #pragma unroll
         for (int p = 0; p < VP; ++p) {
           const float2 g = mul2(d[p], gm[p]);
@@ -163,20 +174,11 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
         const int col = (t + v * tpr) * VEC;
         float2 d[VP], gm[VP], out[VP];
         unpack2<D>(dcur[v], d);
-        load_param_pairs<D>(a.gamma, col, w_f32, 1.f, gm);
+        read_pairs<VEC>(gs, v, t, tpr, gm);
         float2 ag[VP], ab[VP];
         if constexpr (ACC_SMEM) {
-#pragma unroll
-          for (int q = 0; q < VP / 2; ++q) {
-            const float4 u = *reinterpret_cast<const float4*>(sacc_g + col + 4 * q);
-            ag[2 * q] = make_float2(u.x, u.y);
-            ag[2 * q + 1] = make_float2(u.z, u.w);
-            if (LN) {
-              const float4 w = *reinterpret_cast<const float4*>(sacc_b + col + 4 * q);
-              ab[2 * q] = make_float2(w.x, w.y);
-              ab[2 * q + 1] = make_float2(w.z, w.w);
-            }
-          }
+          read_pairs<VEC>(sacc_g, v, t, tpr, ag);
+          if (LN) read_pairs<VEC>(sacc_b, v, t, tpr, ab);
         } else {
 #pragma unroll
           for (int p = 0; p < VP; ++p) {
@@ -193,14 +195,8 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
           if (LN) ab[p] = add2(ab[p], d[p]);
         }
         if constexpr (ACC_SMEM) {
-#pragma unroll
-          for (int q = 0; q < VP / 2; ++q) {
-            *reinterpret_cast<float4*>(sacc_g + col + 4 * q) =
-                make_float4(ag[2 * q].x, ag[2 * q].y, ag[2 * q + 1].x, ag[2 * q + 1].y);
-            if (LN)
-              *reinterpret_cast<float4*>(sacc_b + col + 4 * q) =
-                  make_float4(ab[2 * q].x, ab[2 * q].y, ab[2 * q + 1].x, ab[2 * q + 1].y);
-          }
+          write_pairs<VEC>(sacc_g, v, t, tpr, ag);
+          if (LN) write_pairs<VEC>(sacc_b, v, t, tpr, ab);
         } else {
 #pragma unroll
           for (int p = 0; p < VP; ++p) {
@@ -219,10 +215,17 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
   float* pg = a.ws + (size_t)blockIdx.x * Hp;
   float* pb = a.ws + ((size_t)gridDim.x + blockIdx.x) * Hp;
   if constexpr (ACC_SMEM) {
-    __syncthreads();
-    for (int k = threadIdx.x * 4; k < H; k += blockDim.x * 4) {
-      *reinterpret_cast<float4*>(pg + k) = *reinterpret_cast<const float4*>(sacc_g + k);
-      if (LN) *reinterpret_cast<float4*>(pb + k) = *reinterpret_cast<const float4*>(sacc_b + k);
+    // Each thread owns its accumulator slots: copy them straight out.
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      if (v < nvec) {
+        const int col = (t + v * tpr) * VEC;
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+          *reinterpret_cast<float4*>(pg + col + 4 * q) = sacc_g[(v * (VEC / 4) + q) * tpr + t];
+          if (LN) *reinterpret_cast<float4*>(pb + col + 4 * q) = sacc_b[(v * (VEC / 4) + q) * tpr + t];
+        }
+      }
     }
     return;
   }
@@ -243,8 +246,8 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
     }
     return;
   }
-  float* red_g = sacc_g;
-  float* red_b = sacc_b;
+  float* red_g = sh_acc;  // fold buffer: [Hp] dgamma then [Hp] dbeta
+  float* red_b = red_g + Hp;
   for (int s2 = 0; s2 < rpc; ++s2) {
     if (slot == s2) {
 #pragma unroll
@@ -676,8 +679,12 @@ static cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceI
     const int rpc = tpr <= 256 ? 256 / tpr : 1;
     const int threads = rpc * tpr;
     const int p_cap = (int)std::min<int64_t>((a.N + rpc - 1) / rpc, p_max);
-    size_t smem_f = (size_t)((rpc * 2 * (tpr / 32) * NS + 3) & ~3);
-    if (want || rpc == 1) smem_f += 2 * (size_t)a.Hp;  // fold buffer / shared accumulators
+    // group scratch | fp32 gamma | shared accumulators (one row slot) or the
+    // fold buffer of several row slots
+    const size_t slots = (size_t)vpt * VEC * tpr;
+    size_t smem_f = (size_t)((rpc * 2 * (tpr / 32) * NS + 3) & ~3) + slots;
+    if (rpc == 1) smem_f += (KIND == KIND_LN ? 2 : 1) * slots;
+    else if (want) smem_f += 2 * (size_t)a.Hp;
     const size_t smem = smem_f * sizeof(float);
     if (threads <= 256) {
       switch (vpt) {

@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
   using T = typename D::T;
   constexpr int VEC = D::VEC;
   constexpr int VP = VEC / 2;
-  extern __shared__ float sh_dyn[];
+  extern __shared__ __align__(16) float sh_dyn[];
   const int tpr = a.tpr;
   const int rpc = blockDim.x / tpr;
   const int slot = threadIdx.x / tpr;
@@ -69,6 +69,14 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
   int nvec = 0;  // vectors of each row this thread owns
 #pragma unroll
   for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
+  // gamma (and beta) as fp32, thread-interleaved, shared by the row slots.
+  float4* gs = reinterpret_cast<float4*>(sh_dyn + ((rpc * 2 * nw * 3 + 3) & ~3));
+  float4* bs = gs + VPT * (VEC / 4) * tpr;
+  if (slot == 0) {
+    stage_params<D, VPT>(gs, a.gamma, w_f32, 1.f, t, tpr, hv);
+    if constexpr (KIND == KIND_LN) stage_params<D, VPT>(bs, a.beta, w_f32, 0.f, t, tpr, hv);
+  }
+  __syncthreads();
 
   uint4 nx[VPT], nr[VPT];
   float npivot = 0.f;
@@ -174,10 +182,10 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
       if (v < nvec) {
         const int col = (t + v * tpr) * VEC;
         float2 gm[VP], out[VP];
-        load_param_pairs<D>(a.gamma, col, w_f32, 1.f, gm);
+        read_pairs<VEC>(gs, v, t, tpr, gm);
         if constexpr (KIND == KIND_LN) {
           float2 be[VP];
-          load_param_pairs<D>(a.beta, col, w_f32, 0.f, be);
+          read_pairs<VEC>(bs, v, t, tpr, be);
 #pragma unroll
           for (int p = 0; p < VP; ++p) out[p] = fma2(fma2(f[v][p], r2, b2), gm[p], be[p]);
         } else {
@@ -486,21 +494,26 @@ static int64_t persistent_blocks(K kern, int threads, size_t smem, const DeviceI
   return std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)per_sm * dev.sm_count));
 }
 
+template <typename K>
+static cudaError_t launch_rows(K kern, const FwdArgs& a, int threads, size_t smem, const DeviceInfo& dev,
+                               int64_t groups, cudaStream_t s) {
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<(unsigned)persistent_blocks(kern, threads, smem, dev, groups), threads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int KIND, typename D, int VPT>
 static cudaError_t run_rows(const FwdArgs& a, int threads, int rpc, size_t smem, const DeviceInfo& dev,
                             cudaStream_t s) {
   const int64_t groups = (a.N + rpc - 1) / rpc;
-  if (threads <= 256) {
-    auto kern = fwd_rows_kernel<KIND, D, VPT, 256, (VPT * D::VEC > 16 ? 2 : 3)>;
-    kern<<<(unsigned)persistent_blocks(kern, threads, smem, dev, groups), threads, smem, s>>>(a);
-  } else if (threads <= 640) {
-    auto kern = fwd_rows_kernel<KIND, D, VPT, 640, 1>;
-    kern<<<(unsigned)persistent_blocks(kern, threads, smem, dev, groups), threads, smem, s>>>(a);
-  } else {
-    auto kern = fwd_rows_kernel<KIND, D, VPT, 1024, 1>;
-    kern<<<(unsigned)persistent_blocks(kern, threads, smem, dev, groups), threads, smem, s>>>(a);
-  }
-  return cudaGetLastError();
+  if (threads <= 256)
+    return launch_rows(fwd_rows_kernel<KIND, D, VPT, 256, (VPT * D::VEC > 16 ? 2 : 3)>, a, threads, smem, dev,
+                       groups, s);
+  if (threads <= 640) return launch_rows(fwd_rows_kernel<KIND, D, VPT, 640, 1>, a, threads, smem, dev, groups, s);
+  return launch_rows(fwd_rows_kernel<KIND, D, VPT, 1024, 1>, a, threads, smem, dev, groups, s);
 }
 
 template <int KIND, typename D, int VPT>
@@ -580,7 +593,9 @@ static cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream
     a.tpr = tpr;
     const int rpc = tpr <= 256 ? 256 / tpr : 1;
     const int threads = rpc * tpr;
-    const size_t smem = (size_t)rpc * 2 * (tpr / 32) * 3 * sizeof(float);
+    // group scratch, then fp32 gamma (and beta) for vpt vectors of tpr threads
+    const size_t smem = (((size_t)rpc * 2 * (tpr / 32) * 3 + 3) & ~(size_t)3) * sizeof(float) +
+                        (KIND == KIND_LN ? 2 : 1) * (size_t)vpt * VEC * tpr * sizeof(float);
     switch (vpt) {
       case 1: return run_rows<KIND, D, 1>(a, threads, rpc, smem, dev, s);
       case 2: return run_rows<KIND, D, 2>(a, threads, rpc, smem, dev, s);
