@@ -70,6 +70,25 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
   for (int v = 0; v < VA; ++v)
 #pragma unroll
     for (int p = 0; p < VP; ++p) acc_g[v][p] = acc_b[v][p] = splat2(0.f);
+  uint4 nx[VPT], nd[VPT];
+  float nrs = 0.f, nmu = 0.f;
+  auto fetch = [&](int64_t r) {
+    const T* xrow = reinterpret_cast<const T*>(a.x) + r * a.ldx;
+    const T* dyrow = reinterpret_cast<const T*>(a.dy) + r * a.lddy;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = (t + v * tpr) * VEC;
+      nx[v] = load_vec_or_zero<D>(xrow, c, H);
+      nd[v] = load_vec_or_zero<D>(dyrow, c, H);
+    }
+    nrs = a.rstd[r];
+    if (LN) nmu = a.mean[r];
+  };
+
+  int parity = 0;
+  int64_t row = (int64_t)blockIdx.x * rpc + slot;
+  if (row < a.N) fetch(row);  // first row in flight while gamma is staged
+
   const int Hp = a.Hp;
   // Shared memory: group scratch | fp32 gamma (thread-interleaved, shared by
   // the row slots) | accumulators (ACC_SMEM, thread-interleaved: dgamma then
@@ -93,24 +112,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
   }
   __syncthreads();
 
-  uint4 nx[VPT], nd[VPT];
-  float nrs = 0.f, nmu = 0.f;
-  auto fetch = [&](int64_t r) {
-    const T* xrow = reinterpret_cast<const T*>(a.x) + r * a.ldx;
-    const T* dyrow = reinterpret_cast<const T*>(a.dy) + r * a.lddy;
-#pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      const int c = (t + v * tpr) * VEC;
-      nx[v] = load_vec_or_zero<D>(xrow, c, H);
-      nd[v] = load_vec_or_zero<D>(dyrow, c, H);
-    }
-    nrs = a.rstd[r];
-    if (LN) nmu = a.mean[r];
-  };
 
-  int parity = 0;
-  int64_t row = (int64_t)blockIdx.x * rpc + slot;
-  if (row < a.N) fetch(row);
   for (; row < a.N; row += stride) {
     const float r = nrs;
     const float2 r2 = splat2(r);
@@ -518,7 +520,11 @@ __global__ void __launch_bounds__(LOOP_THREADS) bwd_loop_kernel(const BwdArgs a)
 
 // dgamma[j] = sum_p partial[0][p][j], dbeta[j] = sum_p partial[1][p][j]: 8
 // column vectors (32 columns) x 32 row groups per CTA, blockIdx.y picks the
-// parameter.  Fixed summation order, one rounding to the output dtype.
+// parameter.  Each thread issues the loads of all its (up to kReduceRows)
+// partial rows before adding, so the kernel costs about one L2 round trip.
+// Fixed summation order, one rounding to the output dtype.
+constexpr int kReduceRows = 16;
+
 template <typename D>
 __global__ void __launch_bounds__(256) bwd_param_reduce_kernel(const float* ws, int P, int Hp, int H,
                                                                void* dg, void* db, int w_f32) {
@@ -532,13 +538,20 @@ __global__ void __launch_bounds__(256) bwd_param_reduce_kernel(const float* ws, 
   const int col = (blockIdx.x * 8 + cl) * 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (col < Hp) {
-#pragma unroll 4
-    for (int p = rg; p < P; p += 32) {
-      const float4 v = *reinterpret_cast<const float4*>(src + (size_t)p * Hp + col);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+    for (int p0 = rg; p0 < P; p0 += 32 * kReduceRows) {
+      float4 v[kReduceRows];
+#pragma unroll
+      for (int k = 0; k < kReduceRows; ++k) {
+        const int p = p0 + 32 * k;
+        v[k] = p < P ? *reinterpret_cast<const float4*>(src + (size_t)p * Hp + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < kReduceRows; ++k) {
+        acc.x += v[k].x;
+        acc.y += v[k].y;
+        acc.z += v[k].z;
+        acc.w += v[k].w;
+      }
     }
   }
   __shared__ float4 sm[32][8];

@@ -69,15 +69,6 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
   int nvec = 0;  // vectors of each row this thread owns
 #pragma unroll
   for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
-  // gamma (and beta) as fp32, thread-interleaved, shared by the row slots.
-  float4* gs = reinterpret_cast<float4*>(sh_dyn + ((rpc * 2 * nw * 3 + 3) & ~3));
-  float4* bs = gs + VPT * (VEC / 4) * tpr;
-  if (slot == 0) {
-    stage_params<D, VPT>(gs, a.gamma, w_f32, 1.f, t, tpr, hv);
-    if constexpr (KIND == KIND_LN) stage_params<D, VPT>(bs, a.beta, w_f32, 0.f, t, tpr, hv);
-  }
-  __syncthreads();
-
   uint4 nx[VPT], nr[VPT];
   float npivot = 0.f;
   auto fetch = [&](int64_t r) {
@@ -94,7 +85,17 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
 
   int parity = 0;
   int64_t row = (int64_t)blockIdx.x * rpc + slot;
-  if (row < a.N) fetch(row);
+  if (row < a.N) fetch(row);  // first row in flight while the parameters are staged
+
+  // gamma (and beta) as fp32, thread-interleaved, shared by the row slots.
+  float4* gs = reinterpret_cast<float4*>(sh_dyn + ((rpc * 2 * nw * 3 + 3) & ~3));
+  float4* bs = gs + VPT * (VEC / 4) * tpr;
+  if (slot == 0) {
+    stage_params<D, VPT>(gs, a.gamma, w_f32, 1.f, t, tpr, hv);
+    if constexpr (KIND == KIND_LN) stage_params<D, VPT>(bs, a.beta, w_f32, 0.f, t, tpr, hv);
+  }
+  __syncthreads();
+
   for (; row < a.N; row += stride) {
     // Unpack the current row (it arrived while the previous row computed).
     float2 f[VPT][VP];
