@@ -160,6 +160,36 @@ norm_status rms_backward(const void* dy, int64_t lddy, const void* x, int64_t ld
                          int64_t N, int64_t H,
                          norm_dtype x_dtype, norm_dtype w_dtype, norm_stream_t stream);
 
+/*
+ * ln_backward for callers that cannot allocate device memory when they call
+ * it -- for example a plugin inside a framework that owns all device memory
+ * and gives plugins no allocator, or latency-critical code that must not pay
+ * for cudaMalloc mid-step.  (The pages have no counterpart: this is an
+ * interface convenience, not part of the method.)
+ *
+ * Same arguments and results as ln_backward, without the workspace: the
+ * dgamma/dbeta partial rows go to a scratch array of
+ * NORM_STATIC_WORKSPACE_BYTES (64 MiB) compiled into the library, one copy per
+ * GPU that loads it, held until the process exits.  Nothing is allocated.
+ * - Widths whose partial rows need more than that (when dgamma or dbeta is
+ *   requested: norm_bwd_workspace_bytes(H, device) > the limit; H up to about
+ *   27000 on a 152-SM GPU) are refused with NORM_ERR_WORKSPACE.
+ * - The first call on each device looks up that device's copy of the array
+ *   (cudaGetSymbolAddress, with the device current); make that first call
+ *   before any stream capture.
+ * - Every call on a device shares the one array, which keeps the last call's
+ *   contents; no part of it needs clearing, as each call writes every partial
+ *   value before reading it.  Calls whose GPU work overlaps (other streams,
+ *   other host threads) race on the array and must be ordered, e.g. on one
+ *   stream.
+ */
+#define NORM_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
+norm_status ln_backward_static_workspace(const void* dy, int64_t lddy, const void* x, int64_t ldx,
+                                         const float* mean, const float* rstd, const void* gamma,
+                                         void* dx, int64_t lddx, void* dgamma, void* dbeta,
+                                         int64_t N, int64_t H,
+                                         norm_dtype x_dtype, norm_dtype w_dtype, norm_stream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char* norm_status_str(norm_status status);
 
