@@ -175,9 +175,12 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Sum K values over the `nw` warps of one row group.  `sh` holds 2*nw*K floats
-// private to the group; `parity` alternates per row so one barrier per row is
-// enough (a buffer is rewritten only after the next row's barrier).
+// Sum K values over the `nw` (<= 32) warps of one row group.  `sh` holds
+// 2*nw*K floats private to the group; `parity` alternates per row so one
+// barrier per row is enough (a buffer is rewritten only after the next row's
+// barrier).  After the barrier, lane k picks up warp k's partial and a second
+// butterfly finishes the sum: 5 shuffle steps whatever nw is, in a fixed
+// order, identical in every thread.
 template <int K>
 __device__ __forceinline__ void group_sum(float (&v)[K], float* sh, int nw, int wig, int lane,
                                           int bar_id, int parity) {
@@ -190,56 +193,35 @@ __device__ __forceinline__ void group_sum(float (&v)[K], float* sh, int nw, int 
   }
   named_barrier(bar_id, nw * 32);
 #pragma unroll
-  for (int k = 0; k < K; ++k) {
-    float s = buf[k];
-    for (int w = 1; w < nw; ++w) s += buf[w * K + k];
-    v[k] = s;
-  }
+  for (int k = 0; k < K; ++k) v[k] = lane < nw ? buf[lane * K + k] : 0.f;
+  warp_sum<K>(v);
 }
 
 // Welford accumulator (count, mean, M2) and the parallel merge of
-// "Skill: Write CUDA LayerNorm Kernel", Required reasoning process step 3:
-// n = na + nb, delta = mb - ma, mean = ma + delta*nb/n,
-// M2 = M2a + M2b + delta^2*na*nb/n; count 0 is the identity.
+// "Skill: Write CUDA LayerNorm Kernel", Required reasoning process step 3
+// (n = na + nb, delta = mb - ma, mean = ma + delta*nb/n,
+// M2 = M2a + M2b + delta^2*na*nb/n; count 0 is the identity), used below in
+// its closed form for K parts.
 struct Welford {
   float n, m, m2;
 };
 
-// The weight n_b/n uses the fast reciprocal-multiply division (2 ulp): an
-// error there moves the merged mean by about |delta| * 2^-22 and perturbs
-// only the small delta^2 correction of M2, far below the fp32 sums' own error.
-// Equal counts (the common case: every thread of a full row holds the same
-// number of values) take the exact weight 1/2 with no division.
-__device__ __forceinline__ Welford welford_merge(const Welford& a, const Welford& b) {
-  const float n = a.n + b.n;
-  if (n == 0.f) return a;
-  const float wb = a.n == b.n ? 0.5f : __fdividef(b.n, n);
-  const float d = b.m - a.m;
-  Welford r;
-  r.n = n;
-  r.m = fmaf(d, wb, a.m);
-  r.m2 = a.m2 + b.m2 + d * d * a.n * wb;
-  return r;
-}
-
+// Parallel merge of the 32 lanes' triples in the closed form for K parts:
+// N = sum n_k, M = sum n_k m_k / N, M2 = sum (M2_k + n_k (m_k - M)^2) -- the
+// pairwise merge applied across all parts at once.  Three shuffle
+// all-reductions, no branches; every lane gets the same bits.
 __device__ __forceinline__ Welford warp_welford(Welford w, int lane) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    Welford o;
-    o.n = __shfl_xor_sync(0xffffffffu, w.n, off);
-    o.m = __shfl_xor_sync(0xffffffffu, w.m, off);
-    o.m2 = __shfl_xor_sync(0xffffffffu, w.m2, off);
-    w = (lane & off) ? welford_merge(o, w) : welford_merge(w, o);
-  }
-  return w;
+  float v[2] = {w.n, w.n * w.m};
+  warp_sum<2>(v);
+  const float m = v[0] > 0.f ? __fdividef(v[1], v[0]) : 0.f;
+  const float d = w.m - m;
+  float q[1] = {fmaf(w.n * d, d, w.m2)};
+  warp_sum<1>(q);
+  return Welford{v[0], m, q[0]};
 }
 
-// Welford merge over the warps of a row group, same buffering as group_sum.
-// The warps' triples are combined in the closed form of the parallel merge
-// for K parts: N = sum n_k, M = sum n_k m_k / N,
-// M2 = sum M2_k + sum n_k (m_k - M)^2 -- the pairwise merge applied K-1
-// times, evaluated in about 3K operations, in warp order (every thread gets
-// the same bits).
+// The same over the `nw` warps of a row group (buffering as group_sum): lane
+// k picks up warp k's triple (lanes >= nw hold the identity, count 0).
 __device__ __forceinline__ Welford group_welford(Welford w, float* sh, int nw, int wig, int lane,
                                                  int bar_id, int parity) {
   w = warp_welford(w, lane);
@@ -251,18 +233,9 @@ __device__ __forceinline__ Welford group_welford(Welford w, float* sh, int nw, i
     buf[wig * 3 + 2] = w.m2;
   }
   named_barrier(bar_id, nw * 32);
-  float n = 0.f, sm = 0.f;
-  for (int k = 0; k < nw; ++k) {
-    n += buf[3 * k];
-    sm = fmaf(buf[3 * k], buf[3 * k + 1], sm);
-  }
-  const float m = n > 0.f ? __fdividef(sm, n) : 0.f;
-  float m2 = 0.f;
-  for (int k = 0; k < nw; ++k) {
-    const float d = buf[3 * k + 1] - m;
-    m2 += fmaf(buf[3 * k] * d, d, buf[3 * k + 2]);
-  }
-  return Welford{n, m, m2};
+  Welford x{0.f, 0.f, 0.f};
+  if (lane < nw) x = Welford{buf[3 * lane], buf[3 * lane + 1], buf[3 * lane + 2]};
+  return warp_welford(x, lane);
 }
 
 // ---------------------------------------------------------------------------
