@@ -75,6 +75,7 @@ struct StageCfg {
   int W;             // consumer warps
   int row_bytes;     // H * element size (a multiple of 16)
   int red_off;       // byte offset of the cross-warp reduction scratch
+  int par_off;       // byte offset of the fp32 parameter copies (thread-interleaved)
   int data_off;      // byte offset of stage 0
   int contiguous;    // rows of every staged tensor are back to back (ld == H)
   unsigned* err;     // device error flags (bounded waits that ran out)

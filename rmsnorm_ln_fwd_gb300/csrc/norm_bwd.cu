@@ -646,7 +646,15 @@ static cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceI
   } else {
     tpr = ((Hv + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32;
   }
-  const bool rows_ok = vec_ok && tpr <= 1024;
+  const int rpc_rows = tpr <= 256 ? 256 / tpr : 1;
+  // group scratch | fp32 gamma | shared accumulators (one row slot) or the
+  // fold buffer of several row slots
+  const size_t rows_slots = (size_t)vpt * VEC * tpr;
+  size_t rows_smem_f = (size_t)((rpc_rows * 2 * (tpr / 32) * NS + 3) & ~3) + rows_slots;
+  if (rpc_rows == 1) rows_smem_f += (KIND == KIND_LN ? 2 : 1) * rows_slots;
+  else if (want) rows_smem_f += 2 * (size_t)a.Hp;
+  const size_t rows_smem = rows_smem_f * sizeof(float);
+  const bool rows_ok = vec_ok && tpr <= 1024 && rows_smem <= (size_t)dev.max_smem_optin;
   // Staged shape.  17 warps leave at most 96 registers a thread (a
   // sub-partition holds 5 warps).  LayerNorm keeps two accumulators per
   // column, so it first tries shapes with at most 24 columns per thread.
@@ -689,16 +697,10 @@ static cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceI
   // 2 x SM count (the partial rows the workspace holds).
   if (!done && use_rows) {
     a.tpr = tpr;
-    const int rpc = tpr <= 256 ? 256 / tpr : 1;
+    const int rpc = rpc_rows;
     const int threads = rpc * tpr;
     const int p_cap = (int)std::min<int64_t>((a.N + rpc - 1) / rpc, p_max);
-    // group scratch | fp32 gamma | shared accumulators (one row slot) or the
-    // fold buffer of several row slots
-    const size_t slots = (size_t)vpt * VEC * tpr;
-    size_t smem_f = (size_t)((rpc * 2 * (tpr / 32) * NS + 3) & ~3) + slots;
-    if (rpc == 1) smem_f += (KIND == KIND_LN ? 2 : 1) * slots;
-    else if (want) smem_f += 2 * (size_t)a.Hp;
-    const size_t smem = smem_f * sizeof(float);
+    const size_t smem = rows_smem;
     if (threads <= 256) {
       switch (vpt) {
         case 1: err = run_rows<KIND, D, 1, 256, 2>(a, threads, &P, p_cap, smem, dev, s); break;
@@ -741,6 +743,7 @@ static cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceI
 
 cudaError_t launch_backward(int kind, Dtype dt, BwdArgs a, void* dgamma, void* dbeta,
                             const DeviceInfo& dev, cudaStream_t s) {
+  (void)cudaGetLastError();  // drop a stale, non-sticky error left by an earlier call
   if (dt == DT_BF16) {
     return kind == KIND_LN ? launch_bwd_typed<KIND_LN, BF16>(a, dgamma, dbeta, dev, s)
                            : launch_bwd_typed<KIND_RMS, BF16>(a, dgamma, nullptr, dev, s);

@@ -204,25 +204,28 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
 #define NORM_STAGED_MAX_STAGES 6
 #endif
 
-bool staged_config(int H, int es, int NT, int max_smem, int max_cols, StageCfg* c) {
+bool staged_config(int H, int es, int NT, int max_smem, int max_cols, StageCfg* c, int n_par) {
   const int row_bytes = H * es;
   if (H <= 0 || row_bytes % 16 != 0) return false;
   const int vec = 16 / es;
   const int hv = H / vec;
   c->W = kStagedConsumerWarps;
   c->row_bytes = row_bytes;
-  c->red_off = 256;                                   // barriers + abort flag
-  c->data_off = c->red_off + 2 * c->W * 3 * 4 + 256;  // scratch, rounded up
-  c->data_off = (c->data_off + 127) & ~127;
+  c->red_off = 256;                           // barriers + abort flag
+  c->par_off = c->red_off + 2 * c->W * 3 * 4;  // after the reduction scratch
+  c->par_off = (c->par_off + 127) & ~127;
   for (int G = c->W; G >= 1; G /= 2) {
     const int tpr = 32 * (c->W / G);
-    const int cols = ((hv + tpr - 1) / tpr) * vec;
+    const int vpt = (hv + tpr - 1) / tpr;
+    const int cols = vpt * vec;
     if (max_cols > 0 && cols > max_cols) continue;
+    const int data_off = (c->par_off + n_par * vpt * vec * tpr * 4 + 127) & ~127;
     const size_t stage = (size_t)NT * G * row_bytes;
-    const long S = (long)(max_smem - c->data_off) / (long)stage;
+    const long S = (long)(max_smem - data_off) / (long)stage;
     if (S < 3) continue;
     c->G = G;
     c->S = (int)std::min<long>(S, NORM_STAGED_MAX_STAGES);
+    c->data_off = data_off;
     return true;
   }
   return false;
@@ -232,12 +235,14 @@ size_t staged_smem_bytes(const StageCfg& c, int NT) { return c.data_off + (size_
 
 // Consumers copy their VPT vectors of the row from shared memory into packed
 // registers, release the stage at once (the producer can refill it while they
-// compute), and run every pass from registers.  Per-thread sums are formed per
-// 16-byte vector as a short tree, so no pass is one long dependent add chain.
+// compute), unpack it once into fp32 pairs and run every pass from registers
+// with f32x2 math; gamma/beta are read from fp32 copies staged once per CTA in
+// shared memory (thread-interleaved, conflict-free).
 template <int KIND, typename D, int VPT>
 __global__ void __launch_bounds__(kStagedThreads, 1) fwd_staged_kernel(const FwdArgs a, const StageCfg c) {
   using T = typename D::T;
   constexpr int VEC = D::VEC;
+  constexpr int VP = VEC / 2;
   constexpr int NT = KIND == KIND_FUSED ? 2 : 1;  // staged tensors: x (and residual)
   extern __shared__ __align__(128) unsigned char smem[];
   const StagedSmem m = staged_smem(smem, c);
@@ -276,6 +281,15 @@ __global__ void __launch_bounds__(kStagedThreads, 1) fwd_staged_kernel(const Fwd
   int nvec = 0;  // vectors of each row this thread owns
 #pragma unroll
   for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
+  // fp32 gamma (and beta), staged by row group 0 while the first copies fly.
+  float4* gs = m.par;
+  float4* bs = gs + VPT * (VEC / 4) * tpr;
+  if (g == 0) {
+    stage_params<D, VPT>(gs, a.gamma, w_f32, 1.f, t, tpr, hv);
+    if constexpr (KIND == KIND_LN) stage_params<D, VPT>(bs, a.beta, w_f32, 0.f, t, tpr, hv);
+  }
+  named_barrier(15, c.W * 32);  // consumers only (group barriers use ids 1..G, G <= 8 when used)
+
   int parity = 0;
   int k = 0;
   for (int64_t row0 = lo; row0 < hi; row0 += c.G, ++k) {
@@ -304,64 +318,72 @@ __global__ void __launch_bounds__(kStagedThreads, 1) fwd_staged_kernel(const Fwd
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&m.empty[s]);  // the row is in registers: the stage may be refilled
+    const int par = parity;
     parity ^= 1;
     if (!mine) continue;
 
-    float rstd, mean_d = 0.f;
-    if constexpr (KIND == KIND_LN) {
-      // This thread's Welford triple by two passes over its own values, then
-      // the parallel merge across the row group.
-      float sum = 0.f;
+    float2 f[VPT][VP];
 #pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        if (v < nvec) {
-          float f[VEC];
-          unpack<D>(xr[v], f);
-#pragma unroll
-          for (int i = 0; i < VEC; ++i) f[i] -= pivot;
-          sum += tree_sum<VEC>(f);
-        }
-      }
-      const float cnt = (float)(nvec * VEC);
-      const float mloc = nvec > 0 ? sum / cnt : 0.f;
-      float m2 = 0.f;
-#pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        if (v < nvec) {
-          float f[VEC];
-          unpack<D>(xr[v], f);
-#pragma unroll
-          for (int i = 0; i < VEC; ++i) {
-            const float e = (f[i] - pivot) - mloc;
-            f[i] = e * e;
-          }
-          m2 += tree_sum<VEC>(f);
-        }
-      }
-      const Welford w = group_welford(Welford{cnt, mloc, m2}, sh, nwg, wig, lane, bar_id, parity ^ 1);
-      mean_d = w.m;
-      rstd = rsqrtf(w.m2 * inv_h + a.eps);
-    } else {
-      float ss[1] = {0.f};
+    for (int v = 0; v < VPT; ++v) unpack2<D>(xr[v], f[v]);
+    if constexpr (KIND == KIND_FUSED) {
       T* hrow = reinterpret_cast<T*>(a.h) + row * a.ldh;
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
+        float2 r[VP];
+        unpack2<D>(rr[v], r);
+#pragma unroll
+        for (int p = 0; p < VP; ++p) f[v][p] = add2(f[v][p], r[p]);
+        if (v < nvec && have) st_vec(hrow + (t + v * tpr) * VEC, pack2<D>(f[v]));
+      }
+    }
+    float rstd, mean_d = 0.f;
+    if constexpr (KIND == KIND_LN) {
+      const float2 pv = splat2(pivot);
+      float2 s2 = splat2(0.f);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
         if (v < nvec) {
-          float f[VEC];
-          unpack<D>(xr[v], f);
-          if constexpr (KIND == KIND_FUSED) {
-            float r[VEC];
-            unpack<D>(rr[v], r);
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) f[i] += r[i];
-            if (have) store_vec<D>(hrow, (t + v * tpr) * VEC, f);
-          }
+          for (int p = 0; p < VP; ++p) f[v][p] = sub2(f[v][p], pv);
+          float2 vs = f[v][0];
 #pragma unroll
-          for (int i = 0; i < VEC; ++i) f[i] *= f[i];
-          ss[0] += tree_sum<VEC>(f);
+          for (int p = 1; p < VP; ++p) vs = add2(vs, f[v][p]);
+          s2 = add2(s2, vs);
         }
       }
-      group_sum<1>(ss, sh, nwg, wig, lane, bar_id, parity ^ 1);
+      const float cnt = (float)(nvec * VEC);
+      const float mloc = nvec > 0 ? __fdividef(s2.x + s2.y, cnt) : 0.f;
+      const float2 ml = splat2(mloc);
+      float2 q2 = splat2(0.f);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        if (v < nvec) {
+          float2 e = sub2(f[v][0], ml);
+          float2 vq = mul2(e, e);
+#pragma unroll
+          for (int p = 1; p < VP; ++p) {
+            e = sub2(f[v][p], ml);
+            vq = fma2(e, e, vq);
+          }
+          q2 = add2(q2, vq);
+        }
+      }
+      const Welford w = group_welford(Welford{cnt, mloc, q2.x + q2.y}, sh, nwg, wig, lane, bar_id, par);
+      mean_d = w.m;
+      rstd = rsqrtf(w.m2 * inv_h + a.eps);
+    } else {
+      float2 s2 = splat2(0.f);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        if (v < nvec) {
+          float2 vq = mul2(f[v][0], f[v][0]);
+#pragma unroll
+          for (int p = 1; p < VP; ++p) vq = fma2(f[v][p], f[v][p], vq);
+          s2 = add2(s2, vq);
+        }
+      }
+      float ss[1] = {s2.x + s2.y};
+      group_sum<1>(ss, sh, nwg, wig, lane, bar_id, par);
       rstd = rsqrtf(ss[0] * inv_h + a.eps);
     }
     if (t == 0 && have) {
@@ -371,29 +393,24 @@ __global__ void __launch_bounds__(kStagedThreads, 1) fwd_staged_kernel(const Fwd
       if (a.rstd) a.rstd[row] = rstd;
     }
     T* yrow = reinterpret_cast<T*>(a.y) + row * a.ldy;
+    const float2 r2 = splat2(rstd);
+    const float2 b2 = splat2(-mean_d * rstd);
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       if (v < nvec) {
         const int col = (t + v * tpr) * VEC;
-        float f[VEC], gm[VEC], out[VEC];
-        unpack<D>(xr[v], f);
-        load_param_vec<D>(a.gamma, col, w_f32, 1.f, gm);
+        float2 gm[VP], out[VP];
+        read_pairs<VEC>(gs, v, t, tpr, gm);
         if constexpr (KIND == KIND_LN) {
-          float b[VEC];
-          load_param_vec<D>(a.beta, col, w_f32, 0.f, b);
+          float2 be[VP];
+          read_pairs<VEC>(bs, v, t, tpr, be);
 #pragma unroll
-          for (int i = 0; i < VEC; ++i) out[i] = fmaf(((f[i] - pivot) - mean_d) * rstd, gm[i], b[i]);
+          for (int p = 0; p < VP; ++p) out[p] = fma2(fma2(f[v][p], r2, b2), gm[p], be[p]);
         } else {
-          if constexpr (KIND == KIND_FUSED) {
-            float r[VEC];
-            unpack<D>(rr[v], r);
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) f[i] += r[i];
-          }
-#pragma unroll
-          for (int i = 0; i < VEC; ++i) out[i] = (f[i] * rstd) * gm[i];
+          for (int p = 0; p < VP; ++p) out[p] = mul2(mul2(f[v][p], r2), gm[p]);
         }
-        if (have) store_vec<D>(yrow, col, out);
+        if (have) st_vec(yrow + col, pack2<D>(out));
       }
     }
   }
@@ -554,11 +571,17 @@ static cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream
   } else {
     tpr = ((Hv + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32;
   }
-  const bool rows_ok = vec_ok && tpr <= 1024;
+  const int rpc_rows = tpr <= 256 ? 256 / tpr : 1;
+  // group scratch, then fp32 gamma (and beta) for vpt vectors of tpr threads
+  const size_t rows_smem = (((size_t)rpc_rows * 2 * (tpr / 32) * 3 + 3) & ~(size_t)3) * sizeof(float) +
+                           (KIND == KIND_LN ? 2 : 1) * (size_t)vpt * VEC * tpr * sizeof(float);
+  const bool rows_ok = vec_ok && tpr <= 1024 && rows_smem <= (size_t)dev.max_smem_optin;
   StageCfg c{};
   constexpr int NT = KIND == KIND_FUSED ? 2 : 1;
-  // Staged consumers keep at most 8 packed vectors of each tensor.
-  const bool staged_ok = vec_ok && staged_config(a.H, (int)es, NT, dev.max_smem_optin, (8 / NT) * VEC, &c);
+  // Staged consumers keep at most 8 packed vectors of each tensor, and fp32
+  // copies of gamma (and beta) in shared memory.
+  const bool staged_ok = vec_ok && staged_config(a.H, (int)es, NT, dev.max_smem_optin, (8 / NT) * VEC, &c,
+                                                 KIND == KIND_LN ? 2 : 1);
   bool use_rows = false, use_staged = false;
   switch (dev.path) {
     case PATH_AUTO:
@@ -592,11 +615,9 @@ static cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream
   }
   if (use_rows) {
     a.tpr = tpr;
-    const int rpc = tpr <= 256 ? 256 / tpr : 1;
+    const int rpc = rpc_rows;
     const int threads = rpc * tpr;
-    // group scratch, then fp32 gamma (and beta) for vpt vectors of tpr threads
-    const size_t smem = (((size_t)rpc * 2 * (tpr / 32) * 3 + 3) & ~(size_t)3) * sizeof(float) +
-                        (KIND == KIND_LN ? 2 : 1) * (size_t)vpt * VEC * tpr * sizeof(float);
+    const size_t smem = rows_smem;
     switch (vpt) {
       case 1: return run_rows<KIND, D, 1>(a, threads, rpc, smem, dev, s);
       case 2: return run_rows<KIND, D, 2>(a, threads, rpc, smem, dev, s);
@@ -612,6 +633,7 @@ static cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream
 
 cudaError_t launch_forward(int kind, Dtype dt, FwdArgs a, const DeviceInfo& dev, cudaStream_t s) {
   if (a.N == 0) return cudaSuccess;
+  (void)cudaGetLastError();  // drop a stale, non-sticky error left by an earlier call
   if (dt == DT_BF16) {
     switch (kind) {
       case KIND_LN: return launch_fwd_typed<KIND_LN, BF16>(a, dev, s);

@@ -24,6 +24,7 @@ struct StagedSmem {
   uint64_t* full;
   uint64_t* empty;
   float* red;
+  float4* par;
   unsigned char* data;
   volatile int* abort;
 };
@@ -34,6 +35,7 @@ __device__ __forceinline__ StagedSmem staged_smem(unsigned char* smem, const Sta
   m.empty = m.full + c.S;
   m.abort = reinterpret_cast<volatile int*>(m.empty + c.S);
   m.red = reinterpret_cast<float*>(smem + c.red_off);
+  m.par = reinterpret_cast<float4*>(smem + c.par_off);
   m.data = smem + c.data_off;
   return m;
 }
@@ -112,10 +114,11 @@ __device__ __forceinline__ const T* staged_row(const StagedSmem& m, const StageC
 }
 
 // Host side: pick G (rows per stage) and S (stages) for NT staged tensors of
-// row_bytes each, within `budget` bytes of shared memory, with at least three
-// stages and at most `max_cols` columns per consumer thread (0 = no limit).
-// Returns false when no shape fits.
-bool staged_config(int H, int es, int NT, int max_smem, int max_cols, StageCfg* c);
+// row_bytes each, within `max_smem` bytes of shared memory, with at least
+// three stages, at most `max_cols` columns per consumer thread (0 = no limit)
+// and room for `n_par` fp32 parameter arrays (one value per column a consumer
+// thread owns, thread-interleaved).  Returns false when no shape fits.
+bool staged_config(int H, int es, int NT, int max_smem, int max_cols, StageCfg* c, int n_par = 0);
 size_t staged_smem_bytes(const StageCfg& c, int NT);
 
 }  // namespace normk
