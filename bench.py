@@ -219,6 +219,18 @@ def step_calls(shapes):
     return [(s, op) for s in shapes for op in OPS]
 
 
+def aggregate(step_ms, step_bytes, world, dist=None, device=None):
+    """(max step time over ranks, whole-job GB/s).  Every rank runs an
+    independent replica of the same step (rows are independent; nothing is
+    exchanged), so the job moves world * step_bytes in the slowest rank's time."""
+    import torch
+    t = torch.tensor([float(step_ms)], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    return ms, world * step_bytes / (ms * 1e-3) / 1e9
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -269,11 +281,7 @@ def run_ours(args):
     per_call = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)] for i in range(n)]
     step_ms = sum(sum(c) for c in per_call) / args.steps
     step_bytes = sum(s.bytes[op] for s, op in calls)
-    ms_t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    step_ms_max = float(ms_t.item())
-    value = world * step_bytes / (step_ms_max * 1e-3) / 1e9
+    step_ms_max, value = aggregate(step_ms, step_bytes, world, dist, dev)
 
     peak, peak_kind = measured_peak()
     breakdown = {}
@@ -369,14 +377,10 @@ def run_e2e(args, shapes, stream, dev, world, dist):
         results = one_step()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / e2e_steps
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms = float(ms_t.item())
     d2h = sum(o.numel() * o.element_size() for o in results)
     step_bytes = sum(s.bytes[op] for s in shapes for op in OPS)
-    return {"value": round(world * step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+    ms, gbs = aggregate(a.elapsed_time(b) / e2e_steps, step_bytes, world, dist, dev)
+    return {"value": round(gbs, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
             "steps": e2e_steps}
 
