@@ -208,7 +208,17 @@ const char* norm_last_error(void);
  * that ran the kernels have been synchronised.  clear != 0 resets the bits.
  */
 #define NORM_DEVICE_ERR_WAIT_TIMEOUT 1u
+#define NORM_DEVICE_ERR_BAD_COPY 2u /* a bulk copy failed its bounds check and was skipped */
 norm_status norm_device_errors(int device, unsigned int* flags, int clear);
+
+/*
+ * Self-test of the failure path above: enqueue one small kernel that waits,
+ * with the given limit, on a barrier nothing ever signals.  The wait gives up
+ * after limit_ns (1 ms .. 2 s, else NORM_ERR_INVALID_VALUE), sets
+ * NORM_DEVICE_ERR_WAIT_TIMEOUT on the current device and returns; the CUDA
+ * context stays usable.  No data is touched.
+ */
+norm_status norm_selftest_bounded_wait(unsigned long long limit_ns, norm_stream_t stream);
 
 /*
  * Testing and tuning: the kernel-family policy for every later call in the

@@ -40,6 +40,7 @@ SIGNATURES = {
     "norm_abi_version": (_I, []),
     "norm_last_error": (ctypes.c_char_p, []),
     "norm_device_errors": (_I, [_I, ctypes.POINTER(ctypes.c_uint), _I]),
+    "norm_selftest_bounded_wait": (_I, [ctypes.c_ulonglong, _P]),
     "norm_set_kernel_path": (_I, [_I]),
 }
 

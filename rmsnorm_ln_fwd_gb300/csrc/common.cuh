@@ -297,12 +297,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // wait ran out), later waits give up at once; pass abort == nullptr for a wait
 // that must run its full limit regardless (draining copies before exit).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err,
-                                          volatile int* abort) {
+                                          volatile int* abort,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (abort && *abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       if (err) atomicOr(err, kErrWaitTimeout);
       if (abort) *abort = 1;
       return false;

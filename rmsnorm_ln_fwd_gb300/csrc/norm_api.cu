@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "common.cuh"
 #include "launch.h"
 #include "norm.h"
 
@@ -33,6 +34,21 @@ std::atomic<int> g_path{normk::PATH_AUTO};
 // One error word per device: kernels OR error bits into it (a bounded wait
 // that ran out) instead of trapping; norm_device_errors reads it.
 __device__ unsigned g_norm_device_errors;
+
+// Self-test of the bounded wait: an mbarrier nothing ever arrives on, waited
+// on by one warp with a short limit.  The wait must give up, record
+// kErrWaitTimeout and let the kernel return; no copy is in flight.
+__global__ void selftest_wait_kernel(unsigned* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    normk::mbar_init(&bar, 1);
+    abort_flag = 0;
+    normk::fence_barrier_init();
+  }
+  __syncwarp();
+  normk::mbar_wait(&bar, 0, err, &abort_flag, limit_ns);
+}
 
 namespace {
 
@@ -325,6 +341,15 @@ norm_status norm_set_kernel_path(int path) {
   if (path < normk::PATH_AUTO || path > normk::PATH_STAGED) return NORM_ERR_INVALID_VALUE;
   g_path.store(path, std::memory_order_relaxed);
   return NORM_OK;
+}
+
+norm_status norm_selftest_bounded_wait(unsigned long long limit_ns, norm_stream_t stream) {
+  if (limit_ns < 1000000ull || limit_ns > normk::kWaitLimitNs) return NORM_ERR_INVALID_VALUE;
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return NORM_ERR_CUDA;
+  (void)cudaGetLastError();
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(dev.err, limit_ns);
+  return launch_result("self-test launch", cudaGetLastError());
 }
 
 norm_status norm_device_errors(int device, unsigned int* flags, int clear) {

@@ -130,6 +130,11 @@ def test_backward_validation(lib):
     assert lib.rms_backward(A, 64, B, 64, None, None, D, 64, None, None, 0, 4, 64, BF16, BF16, None) == INVALID
 
 
+def test_selftest_limit_validation(lib):
+    assert lib.norm_selftest_bounded_wait(10, None) == INVALID          # below 1 ms
+    assert lib.norm_selftest_bounded_wait(3_000_000_000, None) == INVALID  # above 2 s
+
+
 def test_kernel_path_override_validation(lib):
     assert lib.norm_set_kernel_path(4) == INVALID
     assert lib.norm_set_kernel_path(-1) == INVALID
