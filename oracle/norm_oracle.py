@@ -39,6 +39,7 @@ __all__ = [
     "layer_norm_backward",
     "rms_norm_backward",
     "fused_add_rms_norm_backward",
+    "fused_add_rms_norm_backward_from_h",
     "welford_sequential",
     "welford_merge",
     "welford_tree",
@@ -276,6 +277,23 @@ def fused_add_rms_norm_backward(dy, x, residual, gamma=None, eps=1e-6):
     h = _f64_2d(x) + _f64_2d(residual)
     dh, dgamma = rms_norm_backward(dy, h, gamma, eps)
     return dh, dh.copy(), dgamma
+
+
+def fused_add_rms_norm_backward_from_h(dy, h, gamma=None, eps=1e-6, dh_stream=None):
+    """Backward of the fused add from the stored h -> (dh, dgamma).
+
+    "Skill: Write a Triton Fused Add+RMSNorm Kernel", Required reasoning
+    process steps 9-10: training keeps rstd and the summed activation h (the
+    stored copy is what the backward can read); the RMSNorm gradient with
+    respect to h is formed once and is the gradient of both x and residual
+    (dh/dx = dh/dres = 1).  ``dh_stream`` is the gradient arriving through
+    the stored h itself (the residual stream's consumers), added to that same
+    total: dL/dh = rmsnorm_backward(dy, h) + dh_stream.
+    """
+    dh, dgamma = rms_norm_backward(dy, h, gamma, eps)
+    if dh_stream is not None:
+        dh = dh + _f64_2d(dh_stream)
+    return dh, dgamma
 
 
 # ---------------------------------------------------------------------------

@@ -329,6 +329,31 @@ def pin_fused(O):
         _close(rstd, 1.0 / np.sqrt((exact.numpy() ** 2).mean(axis=1) + eps), 1e-12, 0, "fused rstd")
 
 
+def pin_fused_backward_from_h(O):
+    """The stored-h form of the fused backward.
+
+    * With h = x + res exactly, it equals the (x, res) form (which finite
+      differences pin) for both inputs' gradient and dgamma.
+    * The residual-stream gradient enters linearly: the result minus
+      dh_stream is independent of dh_stream, and equals torch autograd of
+      rms_norm(h) plus dh_stream.
+    """
+    for i, (N, H) in enumerate(SHAPES):
+        eps = 1e-6
+        x, gamma, _, dy, res = _case(110 + i, N, H)
+        h = x + res
+        dx, dres, dg = O.fused_add_rms_norm_backward(dy, x, res, gamma, eps)
+        dh, dg2 = O.fused_add_rms_norm_backward_from_h(dy, h, gamma, eps)
+        _close(dh, dx, 1e-13, 1e-13, "from-h dh vs dx")
+        _close(dh, dres, 1e-13, 1e-13, "from-h dh vs dres")
+        _close(dg2, dg, 1e-13, 1e-13, "from-h dgamma")
+        stream = _rng(120 + i).standard_normal((N, H))
+        dh_s, dg_s = O.fused_add_rms_norm_backward_from_h(dy, h, gamma, eps, stream)
+        tdx, tdg, _ = _autograd(lambda a, g, b: F.rms_norm(a, (H,), g, eps), h, gamma, None, dy)
+        _close(dh_s, tdx + stream, 1e-9, 1e-11, "from-h with stream vs autograd")
+        _close(dg_s, tdg, 1e-9, 1e-11, "from-h dgamma vs autograd")
+
+
 # --------------------------------------------------------------------------
 # storage rounding
 # --------------------------------------------------------------------------
@@ -363,5 +388,6 @@ ALL_PINS = [
     pin_closed_forms,
     pin_welford,
     pin_fused,
+    pin_fused_backward_from_h,
     pin_bf16_rounding,
 ]

@@ -100,6 +100,12 @@ def _fused_bwd_half():
     return f
 
 
+def _fused_from_h_forgets_stream():
+    def f(dy, h, gamma=None, eps=1e-6, dh_stream=None):
+        return R.rms_norm_backward(dy, h, gamma, eps)
+    return f
+
+
 def _merge_wrong(a, b):
     na, ma, m2a = a
     nb, mb, m2b = b
@@ -143,6 +149,7 @@ MUTANTS = {
     "rms_bwd_dgamma_of_x": dict(rms_norm_backward=_rms_bwd(dgamma_of_x=True)),
     "fused_normalises_x_not_h": dict(fused_add_rms_norm_forward=_fused_from_x()),
     "fused_bwd_halves_dres": dict(fused_add_rms_norm_backward=_fused_bwd_half()),
+    "fused_bwd_from_h_forgets_stream": dict(fused_add_rms_norm_backward_from_h=_fused_from_h_forgets_stream()),
     "welford_merge_wrong_weight": dict(welford_merge=_merge_wrong),
     "welford_recurrence_old_mean_twice": dict(welford_sequential=_welford_seq_wrong),
     "bf16_truncates": dict(round_to_bfloat16=_bf16_truncate),
