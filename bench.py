@@ -46,7 +46,10 @@ EPS, EPS_FUSED = 1e-5, 1e-6
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "LN/RMSNorm fwd+bwd achieved HBM GB/s and % of GB300 peak; bwd µs per shape (bf16)"
 OPS = ("ln_fwd", "ln_bwd", "rms_fwd", "rms_bwd", "fused_fwd")
-LAUNCHES = {"ln_fwd": 1, "rms_fwd": 1, "fused_fwd": 1, "ln_bwd": 2, "rms_bwd": 2}
+# Measured by --sweep / --profile-op, not part of the step: the fused-add
+# backward (dx and dres from the stored h, plus the residual-stream gradient).
+EXTRA_OPS = ("fused_bwd",)
+LAUNCHES = {"ln_fwd": 1, "rms_fwd": 1, "fused_fwd": 1, "ln_bwd": 2, "rms_bwd": 2, "fused_bwd": 2}
 
 
 def alg_bytes(op: str, N: int, H: int, e: int = 2, ew: int = 2) -> int:
@@ -58,6 +61,8 @@ def alg_bytes(op: str, N: int, H: int, e: int = 2, ew: int = 2) -> int:
         "fused_fwd": 4 * nh + H * ew + 4 * N,
         "ln_bwd": 3 * nh + 8 * N + H * ew + 2 * H * ew,
         "rms_bwd": 3 * nh + 4 * N + H * ew + H * ew,
+        # reads dy, h, the stream gradient; writes dx and dres
+        "fused_bwd": 5 * nh + 4 * N + H * ew + H * ew,
     }[op]
 
 
@@ -162,11 +167,11 @@ class ClockSampler:
 class Shape:
     """Device tensors of one (N, H) shape and argument tuples for the C ABI."""
 
-    def __init__(self, N, H, dev, seed, lib):
+    def __init__(self, N, H, dev, seed, lib, extra=False):
         import torch
         from rmsnorm_ln_fwd_gb300 import synth, ops
         self.N, self.H, self.lib, self.dev = N, H, lib, dev
-        host = synth.norm_inputs(N, H, "bf16", seed=seed, with_residual=True)
+        host = synth.norm_inputs(N, H, "bf16", seed=seed, with_residual=True, with_dh_stream=extra)
         self.host = host
         t = {k: v.to(dev) for k, v in host.items()}
         self.t = t
@@ -188,6 +193,10 @@ class Shape:
         self.wsb = ops.bwd_workspace_bytes(H, dev)
         self.ws = e((self.wsb + 3) // 4, dtype=torch.float32, device=dev)
         self.bytes = {op: alg_bytes(op, N, H) for op in OPS}
+        if extra:
+            self.dxf = e(N, H, dtype=bf, device=dev)
+            self.dresf = e(N, H, dtype=bf, device=dev)
+            self.dgf = e(H, dtype=bf, device=dev)
 
     def call(self, op, stream):
         L, t, N, H = self.lib, self.t, self.N, self.H
@@ -207,6 +216,11 @@ class Shape:
             st = L.rms_backward(t["dy"].data_ptr(), H, t["x"].data_ptr(), H, self.rstd_r.data_ptr(),
                                 t["gamma"].data_ptr(), self.dxr.data_ptr(), H, self.dgr.data_ptr(),
                                 self.ws.data_ptr(), self.wsb, N, H, BF, BF, stream)
+        elif op == "fused_bwd":
+            st = L.fused_add_rms_backward(t["dy"].data_ptr(), H, self.h.data_ptr(), H, self.rstd_f.data_ptr(),
+                                          t["gamma"].data_ptr(), t["dh_stream"].data_ptr(), H, self.dxf.data_ptr(),
+                                          H, self.dresf.data_ptr(), H, self.dgf.data_ptr(), self.ws.data_ptr(),
+                                          self.wsb, N, H, BF, BF, stream)
         else:
             st = L.fused_add_rms_forward(t["x"].data_ptr(), H, t["residual"].data_ptr(), H, t["gamma"].data_ptr(),
                                          self.yf.data_ptr(), H, self.h.data_ptr(), H, self.rstd_f.data_ptr(), N, H,
@@ -465,7 +479,9 @@ SWEEP = [("ln_fwd", 8192, 1024), ("rms_fwd", 8192, 1024), ("ln_bwd", 8192, 1024)
          ("fused_fwd", 16384, 4096), ("ln_bwd", 32768, 1024), ("rms_bwd", 32768, 1024), ("ln_bwd", 16384, 2048),
          ("rms_bwd", 16384, 2048), ("ln_fwd", 2048, 16384), ("rms_fwd", 2048, 16384), ("ln_bwd", 2048, 16384),
          ("rms_bwd", 2048, 16384), ("ln_fwd", 512, 16384), ("rms_fwd", 512, 16384), ("ln_bwd", 512, 16384),
-         ("rms_bwd", 512, 16384)]
+         ("rms_bwd", 512, 16384), ("fused_bwd", 8192, 1024), ("fused_bwd", 8192, 5120), ("fused_bwd", 16384, 4096)]
+
+FORWARD_OF = {"ln_bwd": "ln_fwd", "rms_bwd": "rms_fwd", "fused_bwd": "fused_fwd"}
 
 
 def run_sweep(args):
@@ -485,10 +501,10 @@ def run_sweep(args):
         if (N, H) not in cache:
             cache.clear()
             torch.cuda.empty_cache()
-            cache[(N, H)] = Shape(N, H, dev, seed=7, lib=lib)
+            cache[(N, H)] = Shape(N, H, dev, seed=7, lib=lib, extra=True)
         s = cache[(N, H)]
-        if op.endswith("bwd"):
-            s.call("ln_fwd" if op == "ln_bwd" else "rms_fwd", stream.cuda_stream)
+        if op in FORWARD_OF:
+            s.call(FORWARD_OF[op], stream.cuda_stream)
         for _ in range(5):
             flush.zero_()
             s.call(op, stream.cuda_stream)
@@ -521,11 +537,11 @@ def run_profile_loop(args):
     nl._lib.set_kernel_path(args.path)
     N, H = (int(v) for v in args.shape.split("x"))
     dev = torch.device("cuda", 0)
-    s = Shape(N, H, dev, seed=3, lib=lib)
+    s = Shape(N, H, dev, seed=3, lib=lib, extra=True)
     sh = torch.cuda.current_stream(dev).cuda_stream
     op = args.profile_op
-    if op.endswith("bwd"):
-        s.call("ln_fwd" if op == "ln_bwd" else "rms_fwd", sh)
+    if op in FORWARD_OF:
+        s.call(FORWARD_OF[op], sh)
     for _ in range(args.iters):
         s.call(op, sh)
     torch.cuda.synchronize()
@@ -545,7 +561,7 @@ def main():
     p.add_argument("--sweep", action="store_true", help="per-call timings over every configured shape")
     p.add_argument("--sweep-iters", type=int, default=50)
     p.add_argument("--path", type=int, default=0, help="kernel-family policy: 0 auto, 1 register rows, 2 loop, 3 bulk-copy pipeline")
-    p.add_argument("--profile-op", choices=list(OPS), default=None)
+    p.add_argument("--profile-op", choices=list(OPS + EXTRA_OPS), default=None)
     p.add_argument("--shape", default="8192x1024")
     p.add_argument("--iters", type=int, default=3)
     args = p.parse_args()

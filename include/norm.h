@@ -190,6 +190,32 @@ norm_status ln_backward_static_workspace(const void* dy, int64_t lddy, const voi
                                          int64_t N, int64_t H,
                                          norm_dtype x_dtype, norm_dtype w_dtype, norm_stream_t stream);
 
+/*
+ * Fused residual add + RMSNorm backward.  "Skill: Write a Triton Fused
+ * Add+RMSNorm Kernel", Required reasoning process steps 9-10: the backward
+ * reads the stored sum h and rstd; the RMSNorm gradient with respect to h,
+ *   dL/dh_j = rstd * (g_j - h_hat_j * sum(g * h_hat) / H) + dh_in_j,
+ *   with g = dy * gamma and h_hat = h * rstd,
+ * is the gradient of both inputs (dh/dx = dh/dresidual = 1).  dh_in is the
+ * gradient arriving through the stored h itself (the residual stream's later
+ * consumers), added in the same pass, or NULL.  dgamma_j = sum over rows of
+ * dy_j * h_hat_j.
+ * dy [N x lddy], h [N x ldh] (the forward's h_out), rstd [N] fp32, gamma [H]
+ *   or NULL.
+ * dx [N x lddx]: dL/dh for x.  May be exactly dy or dh_in (in place); must
+ *   not overlap h.
+ * dres [N x lddres]: dL/dh again, for the residual input; NULL to write dx
+ *   only; exactly dx when x and residual were one tensor, which then
+ *   receives the sum 2 * dL/dh.
+ * dgamma [H] or NULL; workspace as in rms_backward.
+ */
+norm_status fused_add_rms_backward(const void* dy, int64_t lddy, const void* h, int64_t ldh,
+                                   const float* rstd, const void* gamma,
+                                   const void* dh_in, int64_t lddh_in,
+                                   void* dx, int64_t lddx, void* dres, int64_t lddres, void* dgamma,
+                                   void* workspace, size_t workspace_bytes, int64_t N, int64_t H,
+                                   norm_dtype x_dtype, norm_dtype w_dtype, norm_stream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char* norm_status_str(norm_status status);
 

@@ -9,6 +9,7 @@ there is no CPU or PyTorch fallback.
 from ._lib import NormError, load as load_library, LIB_PATH  # noqa: F401
 from .ops import (  # noqa: F401
     bwd_workspace_bytes,
+    fused_add_rms_backward,
     fused_add_rms_forward,
     ln_backward,
     ln_forward,
@@ -20,6 +21,7 @@ __all__ = [
     "ln_forward",
     "rms_forward",
     "fused_add_rms_forward",
+    "fused_add_rms_backward",
     "ln_backward",
     "rms_backward",
     "bwd_workspace_bytes",

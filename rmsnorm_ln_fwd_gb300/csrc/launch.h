@@ -59,6 +59,12 @@ struct BwdArgs {
   int64_t lddx;
   float* ws;  // [2][P][Hp] fp32 partial rows (dgamma, dbeta), or null
   int Hp;     // partial row stride in floats (H rounded up to 4)
+  // Fused add + RMSNorm backward only (KIND_FUSED; x is the stored h):
+  const void* dh_in;  // gradient arriving through h (the residual stream), or null
+  int64_t lddh;
+  void* dres;  // second copy of dL/dh for the residual input, or null
+  int64_t lddres;
+  int dx_twice;  // dres is dx itself (x and residual were one tensor): dx = 2 dL/dh
   int64_t N;
   int H;
   int w_f32;

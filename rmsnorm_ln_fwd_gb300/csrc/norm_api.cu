@@ -218,7 +218,9 @@ size_t workspace_bytes_for(int64_t H, const DeviceInfo& dev) {
 norm_status backward_common(int kind, const void* dy, int64_t lddy, const void* x, int64_t ldx,
                             const float* mean, const float* rstd, const void* gamma, void* dx,
                             int64_t lddx, void* dgamma, void* dbeta, void* ws, size_t ws_bytes,
-                            int64_t N, int64_t H, norm_dtype xd, norm_dtype wd, norm_stream_t stream) {
+                            int64_t N, int64_t H, norm_dtype xd, norm_dtype wd, norm_stream_t stream,
+                            const void* dh_in = nullptr, int64_t lddh = 0, void* dres = nullptr,
+                            int64_t lddres = 0) {
   norm_status st = check_dtypes(xd, wd);
   if (st != NORM_OK) return st;
   if (!shape_ok(N, H)) return NORM_ERR_INVALID_VALUE;
@@ -241,6 +243,19 @@ norm_status backward_common(int kind, const void* dy, int64_t lddy, const void* 
   if (!ld_ok(lddy, N, H, es) || !ld_ok(ldx, N, H, es) || !ld_ok(lddx, N, H, es)) return NORM_ERR_INVALID_VALUE;
   if (!disjoint_rows(dx, lddx, x, ldx, N, H, es) || !same_or_disjoint(dx, lddx, dy, lddy, N, H, es))
     return NORM_ERR_INVALID_VALUE;
+  // Fused-add extras: the stream gradient may be dx itself (accumulate in
+  // place); a second output is dx itself (one tensor fed both inputs) or a
+  // separate buffer clear of everything but the inputs it may replace.
+  const bool dx_twice = dres != nullptr && dres == dx && lddres == lddx;
+  if (dh_in) {
+    if (!ld_ok(lddh, N, H, es) || !same_or_disjoint(dx, lddx, dh_in, lddh, N, H, es)) return NORM_ERR_INVALID_VALUE;
+  }
+  if (dres && !dx_twice) {
+    if (!ld_ok(lddres, N, H, es) || !disjoint_rows(dres, lddres, x, ldx, N, H, es) ||
+        !disjoint_rows(dres, lddres, dx, lddx, N, H, es) || !same_or_disjoint(dres, lddres, dy, lddy, N, H, es))
+      return NORM_ERR_INVALID_VALUE;
+    if (dh_in && !same_or_disjoint(dres, lddres, dh_in, lddh, N, H, es)) return NORM_ERR_INVALID_VALUE;
+  }
   const Span sdx = rows_span(dx, N, lddx, H, es);
   if (dgamma && overlap(vec_span(dgamma, H, wes), sdx)) return NORM_ERR_INVALID_VALUE;
   if (dbeta && overlap(vec_span(dbeta, H, wes), sdx)) return NORM_ERR_INVALID_VALUE;
@@ -269,6 +284,11 @@ norm_status backward_common(int kind, const void* dy, int64_t lddy, const void* 
   a.N = N;
   a.H = (int)H;
   a.w_f32 = wd == NORM_F32;
+  a.dh_in = dh_in;
+  a.lddh = lddh;
+  a.dres = dx_twice ? nullptr : dres;
+  a.lddres = lddres;
+  a.dx_twice = dx_twice;
   return launch_result("backward launch", normk::launch_backward(kind, to_dt(xd), a, dgamma, dbeta, dev,
                                                                  reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -320,6 +340,15 @@ norm_status rms_backward(const void* dy, int64_t lddy, const void* x, int64_t ld
                          norm_stream_t stream) {
   return backward_common(normk::KIND_RMS, dy, lddy, x, ldx, nullptr, rstd, gamma, dx, lddx, dgamma, nullptr,
                          workspace, workspace_bytes, N, H, x_dtype, w_dtype, stream);
+}
+
+norm_status fused_add_rms_backward(const void* dy, int64_t lddy, const void* h, int64_t ldh, const float* rstd,
+                                   const void* gamma, const void* dh_in, int64_t lddh_in, void* dx, int64_t lddx,
+                                   void* dres, int64_t lddres, void* dgamma, void* workspace,
+                                   size_t workspace_bytes, int64_t N, int64_t H, norm_dtype x_dtype,
+                                   norm_dtype w_dtype, norm_stream_t stream) {
+  return backward_common(normk::KIND_FUSED, dy, lddy, h, ldh, nullptr, rstd, gamma, dx, lddx, dgamma, nullptr,
+                         workspace, workspace_bytes, N, H, x_dtype, w_dtype, stream, dh_in, lddh_in, dres, lddres);
 }
 
 const char* norm_status_str(norm_status status) {

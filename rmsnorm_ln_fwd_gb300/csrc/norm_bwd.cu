@@ -70,6 +70,8 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
   for (int v = 0; v < VA; ++v)
 #pragma unroll
     for (int p = 0; p < VP; ++p) acc_g[v][p] = acc_b[v][p] = splat2(0.f);
+  constexpr bool FUSED = KIND == KIND_FUSED;
+  constexpr int VH = FUSED ? VPT : 1;  // stream-gradient vectors (fused only)
   uint4 nx[VPT], nd[VPT];
   float nrs = 0.f, nmu = 0.f;
   auto fetch = [&](int64_t r) {
@@ -117,7 +119,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
     const float r = nrs;
     const float2 r2 = splat2(r);
     float2 xh[VPT][VP];
-    uint4 dcur[VPT];
+    uint4 dcur[VPT], hcur[VH];
     {
       // x_hat = x*rstd - mean*rstd: the rounding of mean*rstd shifts the whole
       // row by one constant, which the recentring below removes.
@@ -132,6 +134,15 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
       }
     }
     if (row + stride < a.N) fetch(row + stride);
+    if constexpr (FUSED) {
+      // The gradient through h is only added in pass 2: load it for this row
+      // now, in flight over the row reduction, rather than a row ahead.
+      if (a.dh_in) {
+        const T* hrow = reinterpret_cast<const T*>(a.dh_in) + row * a.lddh;
+#pragma unroll
+        for (int v = 0; v < VH; ++v) hcur[v] = load_vec_or_zero<D>(hrow, (t + v * tpr) * VEC, H);
+      }
+    }
 
     // Pass 1: sum(g), sum(g*x_hat) and (LayerNorm) sum(x_hat), g = dy*gamma.
     float2 sg = splat2(0.f), sgx = splat2(0.f), sx = splat2(0.f);
@@ -206,7 +217,24 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
             acc_b[ACC_SMEM ? 0 : v][p] = ab[p];
           }
         }
-        st_vec(dxrow + col, pack2<D>(out));
+        if constexpr (FUSED) {
+          // dL/dh = RMSNorm gradient + the gradient through h, for x and residual
+          if (a.dh_in) {
+            float2 e[VP];
+            unpack2<D>(hcur[v], e);
+#pragma unroll
+            for (int p = 0; p < VP; ++p) out[p] = add2(out[p], e[p]);
+          }
+          if (a.dx_twice) {
+#pragma unroll
+            for (int p = 0; p < VP; ++p) out[p] = add2(out[p], out[p]);
+          }
+        }
+        const uint4 packed = pack2<D>(out);
+        st_vec(dxrow + col, packed);
+        if constexpr (FUSED) {
+          if (a.dres) st_vec(reinterpret_cast<T*>(a.dres) + row * a.lddres + col, packed);
+        }
       }
     }
     parity ^= 1;
@@ -508,7 +536,13 @@ __global__ void __launch_bounds__(LOOP_THREADS) bwd_loop_kernel(const BwdArgs a)
       const float dyv = load_elem<D>(dyrow, j);
       const float xc = LN ? (xv - mu) * r - s0 : xv * r;
       const float g = __fmul_rn(dyv, a.gamma ? load_param<D>(a.gamma, j, w_f32) : 1.f);
-      store_elem<D>(dxrow, j, r * (g - c1 - xc * c2));
+      float dxv = r * (g - c1 - xc * c2);
+      if constexpr (KIND == KIND_FUSED) {
+        if (a.dh_in) dxv += load_elem<D>(reinterpret_cast<const T*>(a.dh_in) + row * a.lddh, j);
+        if (a.dx_twice) dxv += dxv;
+        if (a.dres) store_elem<D>(reinterpret_cast<T*>(a.dres) + row * a.lddres, j, dxv);
+      }
+      store_elem<D>(dxrow, j, dxv);
       if (pg) {
         pg[j] = fmaf(dyv, xc, pg[j]);
         if (LN) pb[j] += dyv;
@@ -630,6 +664,8 @@ static cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceI
   const int p_max = bwd_max_partials(dev);
   bool aligned = aligned16(a.x) && aligned16(a.dy) && aligned16(a.dx) && (a.ldx * es) % 16 == 0 &&
                  (a.lddy * es) % 16 == 0 && (a.lddx * es) % 16 == 0;
+  if (a.dh_in) aligned = aligned && aligned16(a.dh_in) && (a.lddh * es) % 16 == 0;
+  if (a.dres) aligned = aligned && aligned16(a.dres) && (a.lddres * es) % 16 == 0;
   if (a.gamma) aligned = aligned && aligned16(a.gamma);
   int P = 0;
   cudaError_t err = cudaSuccess;
@@ -660,8 +696,9 @@ static cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceI
   // column, so it first tries shapes with at most 24 columns per thread.
   StageCfg c{};
   const bool staged_ok =
-      vec_ok && ((KIND == KIND_LN && staged_config(a.H, (int)es, 2, dev.max_smem_optin, 24, &c)) ||
-                 staged_config(a.H, (int)es, 2, dev.max_smem_optin, kStagedMaxCols, &c));
+      KIND != KIND_FUSED && vec_ok &&
+      ((KIND == KIND_LN && staged_config(a.H, (int)es, 2, dev.max_smem_optin, 24, &c)) ||
+       staged_config(a.H, (int)es, 2, dev.max_smem_optin, kStagedMaxCols, &c));
   bool use_rows = false, use_staged = false;
   switch (dev.path) {
     case PATH_AUTO:
@@ -676,7 +713,8 @@ static cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceI
       break;
     default: break;
   }
-  if (use_staged) {
+  if constexpr (KIND != KIND_FUSED) {
+   if (use_staged) {
     c.err = dev.err;
     c.contiguous = a.ldx == a.H && a.lddy == a.H;
     const int stpr = 32 * (c.W / c.G);
@@ -692,6 +730,7 @@ static cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceI
       else err = run_staged<KIND, D, 8>(a, c, P, smem, s);
     }
     done = true;
+   }
   }
   // Register rows; the grid is persistent: as many CTAs as fit, at most
   // 2 x SM count (the partial rows the workspace holds).
@@ -745,11 +784,17 @@ cudaError_t launch_backward(int kind, Dtype dt, BwdArgs a, void* dgamma, void* d
                             const DeviceInfo& dev, cudaStream_t s) {
   (void)cudaGetLastError();  // drop a stale, non-sticky error left by an earlier call
   if (dt == DT_BF16) {
-    return kind == KIND_LN ? launch_bwd_typed<KIND_LN, BF16>(a, dgamma, dbeta, dev, s)
-                           : launch_bwd_typed<KIND_RMS, BF16>(a, dgamma, nullptr, dev, s);
+    switch (kind) {
+      case KIND_LN: return launch_bwd_typed<KIND_LN, BF16>(a, dgamma, dbeta, dev, s);
+      case KIND_RMS: return launch_bwd_typed<KIND_RMS, BF16>(a, dgamma, nullptr, dev, s);
+      default: return launch_bwd_typed<KIND_FUSED, BF16>(a, dgamma, nullptr, dev, s);
+    }
   }
-  return kind == KIND_LN ? launch_bwd_typed<KIND_LN, F32>(a, dgamma, dbeta, dev, s)
-                         : launch_bwd_typed<KIND_RMS, F32>(a, dgamma, nullptr, dev, s);
+  switch (kind) {
+    case KIND_LN: return launch_bwd_typed<KIND_LN, F32>(a, dgamma, dbeta, dev, s);
+    case KIND_RMS: return launch_bwd_typed<KIND_RMS, F32>(a, dgamma, nullptr, dev, s);
+    default: return launch_bwd_typed<KIND_FUSED, F32>(a, dgamma, nullptr, dev, s);
+  }
 }
 
 }  // namespace normk

@@ -204,3 +204,51 @@ def rms_backward(dy, x, rstd, gamma=None, *, need_param_grads: bool = True, work
                               ov.data_ptr(), lddx, _ptr(dgamma), _ptr(ws), wsb, N, H, xc, wc, _stream(x.device))
     _lib.check("rms_backward", st)
     return out, dgamma
+
+
+def fused_add_rms_backward(dy, h, rstd, gamma=None, dh_in=None, *, need_param_grads: bool = True,
+                           residual_grad: str = "separate", workspace=None, dx=None, param_dtype=None):
+    """Backward of fused_add_rms_forward from its stored h and rstd.
+
+    Returns (dx, dres, dgamma): dL/dh for x and for the residual, where
+    dL/dh = RMSNorm gradient + dh_in (the gradient arriving through h, or
+    None).  ``residual_grad``: "separate" writes a second buffer, "none"
+    returns dres = None (the caller reuses dx), "same" treats x and residual
+    as one tensor and returns 2 * dL/dh in dx (dres is dx)."""
+    dyv, N, H, lddy = _rows(dy, "dy")
+    hv, Nh, Hh, ldh = _rows(h, "h")
+    if (Nh, Hh) != (N, H) or dy.dtype != h.dtype:
+        raise ValueError("dy must match h")
+    xc = _dtype_code(h, "h")
+    gamma = _vec(gamma, H, "gamma")
+    wdt = gamma.dtype if gamma is not None else (param_dtype or h.dtype)
+    wc = _DT[wdt]
+    if dh_in is not None:
+        dv, Nd, Hd, lddh = _rows(dh_in, "dh_in")
+        if (Nd, Hd) != (N, H) or dh_in.dtype != h.dtype:
+            raise ValueError("dh_in must match h")
+    else:
+        dv, lddh = None, 0
+    out = torch.empty_like(h, memory_format=torch.contiguous_format) if dx is None else dx
+    ov, No, Ho, lddx = _rows(out, "dx")
+    if residual_grad == "separate":
+        dres = torch.empty_like(h, memory_format=torch.contiguous_format)
+        rv, _, _, lddres = _rows(dres, "dres")
+    elif residual_grad == "same":
+        dres, rv, lddres = out, ov, lddx
+    elif residual_grad == "none":
+        dres, rv, lddres = None, None, 0
+    else:
+        raise ValueError("residual_grad must be 'separate', 'same' or 'none'")
+    dgamma = torch.empty(H, device=h.device, dtype=wdt) if need_param_grads else None
+    ws, wsb = (None, 0)
+    if need_param_grads:
+        ws, wsb = _workspace(workspace, H, h.device)
+    lib = _lib.load()
+    with torch.cuda.device(h.device):
+        st = lib.fused_add_rms_backward(dyv.data_ptr(), lddy, hv.data_ptr(), ldh, rstd.data_ptr(), _ptr(gamma),
+                                        None if dv is None else dv.data_ptr(), lddh, ov.data_ptr(), lddx,
+                                        None if rv is None else rv.data_ptr(), lddres, _ptr(dgamma), _ptr(ws),
+                                        wsb, N, H, xc, wc, _stream(h.device))
+    _lib.check("fused_add_rms_backward", st)
+    return out, (dres if residual_grad == "separate" else (out if residual_grad == "same" else None)), dgamma

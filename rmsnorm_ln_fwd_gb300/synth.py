@@ -7,7 +7,7 @@ to the CUDA library and to the CPU oracle.
 Recipe (every tensor drawn in fp32 on the CPU from its own seeded
 ``torch.Generator``, then cast once to its storage dtype):
 
-* x, residual, dy ~ N(0, 1)  (x = offset + scale * N(0, 1) for the
+* x, residual, dy, dh_stream ~ N(0, 1)  (x = offset + scale * N(0, 1) for the
   large-offset stability workload, e.g. offset 1000, scale 1e-2);
 * gamma = 1 + 0.1 * N(0, 1);  beta = 0.1 * N(0, 1).
 """
@@ -18,7 +18,7 @@ import torch
 
 # One independent generator stream per tensor role, so a tensor's values do
 # not depend on which other tensors are drawn or on their shapes.
-_STREAM = {"x": 1, "gamma": 2, "beta": 3, "dy": 4, "residual": 5}
+_STREAM = {"x": 1, "gamma": 2, "beta": 3, "dy": 4, "residual": 5, "dh_stream": 6}
 
 DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 
@@ -43,8 +43,9 @@ def normal(shape, seed: int, role: str, *, mean: float = 0.0, std: float = 1.0,
 def norm_inputs(N: int, H: int, dtype="bf16", w_dtype=None, seed: int = 0, *,
                 x_offset: float = 0.0, x_scale: float = 1.0,
                 with_beta: bool = True, with_dy: bool = True,
-                with_residual: bool = False) -> dict:
-    """CPU tensors for one (N, H) workload: x, gamma, beta, dy, residual."""
+                with_residual: bool = False, with_dh_stream: bool = False) -> dict:
+    """CPU tensors for one (N, H) workload: x, gamma, beta, dy, residual and
+    dh_stream (a gradient arriving through the stored residual sum)."""
     dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
     wdt = dt if w_dtype is None else (DTYPES[w_dtype] if isinstance(w_dtype, str) else w_dtype)
     out = {
@@ -57,4 +58,6 @@ def norm_inputs(N: int, H: int, dtype="bf16", w_dtype=None, seed: int = 0, *,
         out["dy"] = normal((N, H), seed, "dy", dtype=dt)
     if with_residual:
         out["residual"] = normal((N, H), seed, "residual", dtype=dt)
+    if with_dh_stream:
+        out["dh_stream"] = normal((N, H), seed, "dh_stream", dtype=dt)
     return out

@@ -38,7 +38,7 @@ def declared_functions():
 def test_header_declares_the_five_ops():
     names = set(declared_functions())
     for op in ["ln_forward", "rms_forward", "fused_add_rms_forward", "ln_backward", "rms_backward",
-               "norm_bwd_workspace_bytes", "norm_status_str"]:
+               "fused_add_rms_backward", "norm_bwd_workspace_bytes", "norm_status_str"]:
         assert op in names
 
 
@@ -128,6 +128,31 @@ def test_backward_validation(lib):
     assert _bwd(lib, lddx=10) == INVALID
     assert _bwd(lib, dg=0x500000, db=0x500000 + 8) == INVALID  # dgamma/dbeta overlap
     assert lib.rms_backward(A, 64, B, 64, None, None, D, 64, None, None, 0, 4, 64, BF16, BF16, None) == INVALID
+
+
+def _fbwd(lib, **kw):
+    a = dict(dy=A, lddy=64, h=B, ldh=64, rstd=C, g=None, dh=None, lddh=0, dx=D, lddx=64, dres=None, lddres=0,
+             dg=None, ws=None, wsb=0, N=4, H=64, xd=BF16, wd=BF16)
+    a.update(kw)
+    return lib.fused_add_rms_backward(a["dy"], a["lddy"], a["h"], a["ldh"], a["rstd"], a["g"], a["dh"], a["lddh"],
+                                      a["dx"], a["lddx"], a["dres"], a["lddres"], a["dg"], a["ws"], a["wsb"], a["N"],
+                                      a["H"], a["xd"], a["wd"], None)
+
+
+def test_fused_backward_validation(lib):
+    assert _fbwd(lib, wd=7) == UNSUPPORTED
+    assert _fbwd(lib, rstd=None) == INVALID
+    assert _fbwd(lib, h=None) == INVALID
+    assert _fbwd(lib, dx=B) == INVALID                      # dx over h
+    assert _fbwd(lib, dx=A + 2) == INVALID                  # dx partly over dy
+    assert _fbwd(lib, dh=0x500000, lddh=10) == INVALID      # short stream-gradient stride
+    assert _fbwd(lib, dh=D + 2, lddh=64) == INVALID         # stream gradient partly under dx
+    assert _fbwd(lib, dres=B, lddres=64) == INVALID         # dres over h
+    assert _fbwd(lib, dres=D + 2, lddres=64) == INVALID     # dres partly over dx
+    assert _fbwd(lib, dres=D, lddres=72) == INVALID         # dres at dx with another stride
+    assert _fbwd(lib, dres=A + 2, lddres=64) == INVALID     # dres partly over dy
+    assert _fbwd(lib, dres=0x500000, lddres=10) == INVALID  # short dres stride
+    assert _fbwd(lib, dh=0x500000, lddh=64, dres=0x500000 + 2, lddres=64) == INVALID  # dres partly over dh
 
 
 def test_selftest_limit_validation(lib):
