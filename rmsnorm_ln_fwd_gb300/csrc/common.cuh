@@ -161,6 +161,23 @@ __device__ __forceinline__ void warp_sum(float (&v)[K]) {
   }
 }
 
+// Butterfly over groups of `p` lanes (p a power of two, 2 <= p <= 32): every
+// lane ends with the sum over its group, and lanes holding the same values in
+// the same group positions end with identical bits.
+template <int K>
+__device__ __forceinline__ void warp_sum_pow2(float (&v)[K], int p) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    if (off < p) {
+#pragma unroll
+      for (int k = 0; k < K; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], off);
+    }
+  }
+}
+
+// Smallest power of two >= n, for 2 <= n <= 32.
+__device__ __forceinline__ int pow2_ceil(int n) { return 1 << (32 - __clz(n - 1)); }
+
 // Tree sum of a short array: depth log2(n) instead of an n-long add chain.
 template <int N>
 __device__ __forceinline__ float tree_sum(const float* v) {
@@ -178,9 +195,10 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
 // Sum K values over the `nw` (<= 32) warps of one row group.  `sh` holds
 // 2*nw*K floats private to the group; `parity` alternates per row so one
 // barrier per row is enough (a buffer is rewritten only after the next row's
-// barrier).  After the barrier, lane k picks up warp k's partial and a second
-// butterfly finishes the sum: 5 shuffle steps whatever nw is, in a fixed
-// order, identical in every thread.
+// barrier).  After the barrier, lane k picks up warp (k mod P)'s partial, P
+// the power of two >= nw (0 past nw), and a butterfly over groups of P lanes
+// finishes the sum in log2(P) steps, in a fixed order, identical in every
+// thread (each group of P lanes holds the same values).
 template <int K>
 __device__ __forceinline__ void group_sum(float (&v)[K], float* sh, int nw, int wig, int lane,
                                           int bar_id, int parity) {
@@ -192,9 +210,11 @@ __device__ __forceinline__ void group_sum(float (&v)[K], float* sh, int nw, int 
     for (int k = 0; k < K; ++k) buf[wig * K + k] = v[k];
   }
   named_barrier(bar_id, nw * 32);
+  const int P = pow2_ceil(nw);
+  const int src = lane & (P - 1);
 #pragma unroll
-  for (int k = 0; k < K; ++k) v[k] = lane < nw ? buf[lane * K + k] : 0.f;
-  warp_sum<K>(v);
+  for (int k = 0; k < K; ++k) v[k] = src < nw ? buf[src * K + k] : 0.f;
+  warp_sum_pow2<K>(v, P);
 }
 
 // Welford accumulator (count, mean, M2) and the parallel merge of
@@ -210,21 +230,23 @@ struct Welford {
 // N = sum n_k, M = sum n_k m_k / N, M2 = sum (M2_k + n_k (m_k - M)^2) -- the
 // pairwise merge applied across all parts at once.  Three shuffle
 // all-reductions, no branches; every lane gets the same bits.
-__device__ __forceinline__ Welford warp_welford(Welford w, int lane) {
+// Over groups of `p` lanes (p = 32: the whole warp).
+__device__ __forceinline__ Welford warp_welford(Welford w, int p = 32) {
   float v[2] = {w.n, w.n * w.m};
-  warp_sum<2>(v);
+  warp_sum_pow2<2>(v, p);
   const float m = v[0] > 0.f ? __fdividef(v[1], v[0]) : 0.f;
   const float d = w.m - m;
   float q[1] = {fmaf(w.n * d, d, w.m2)};
-  warp_sum<1>(q);
+  warp_sum_pow2<1>(q, p);
   return Welford{v[0], m, q[0]};
 }
 
 // The same over the `nw` warps of a row group (buffering as group_sum): lane
-// k picks up warp k's triple (lanes >= nw hold the identity, count 0).
+// k picks up warp (k mod P)'s triple (the identity, count 0, past nw) and the
+// merge runs over groups of P lanes.
 __device__ __forceinline__ Welford group_welford(Welford w, float* sh, int nw, int wig, int lane,
                                                  int bar_id, int parity) {
-  w = warp_welford(w, lane);
+  w = warp_welford(w);
   if (nw == 1) return w;
   float* buf = sh + parity * nw * 3;
   if (lane == 0) {
@@ -233,9 +255,11 @@ __device__ __forceinline__ Welford group_welford(Welford w, float* sh, int nw, i
     buf[wig * 3 + 2] = w.m2;
   }
   named_barrier(bar_id, nw * 32);
+  const int P = pow2_ceil(nw);
+  const int src = lane & (P - 1);
   Welford x{0.f, 0.f, 0.f};
-  if (lane < nw) x = Welford{buf[3 * lane], buf[3 * lane + 1], buf[3 * lane + 2]};
-  return warp_welford(x, lane);
+  if (src < nw) x = Welford{buf[3 * src], buf[3 * src + 1], buf[3 * src + 2]};
+  return warp_welford(x, P);
 }
 
 // ---------------------------------------------------------------------------

@@ -21,11 +21,14 @@
 //
 // Statistics ("Skill: Write CUDA LayerNorm Kernel", Required reasoning process
 // steps 2-5; "Skill: Write a Triton LayerNorm Kernel" steps 3-7):
-// LayerNorm keeps a Welford triple (count, mean, M2) per thread, merges it
-// across lanes with shuffles and across warps through shared memory with the
-// parallel merge, and divides M2 by the full row length H.  Values are shifted
-// by the row's first element before accumulating (x - x0 is exact when the
-// two are close), so rows with a large common offset keep full precision.
+// LayerNorm: the register-row kernel holds the whole row, so it takes the
+// plain two-pass -- the row sum gives the mean, then the sum of squared
+// deviations from it gives M2 -- each a shuffle + shared-memory reduction.
+// The kernels that stream the row keep a Welford triple (count, mean, M2) per
+// thread and merge triples across lanes and warps with the parallel merge.
+// M2 is divided by the full row length H.  Values are shifted by the row's
+// first element before accumulating (x - x0 is exact when the two are close),
+// so rows with a large common offset keep full precision.
 // RMSNorm sums x^2.  rstd = rsqrt(var + eps): eps inside the square root.
 //
 // Fused add ("Skill: Write a Triton Fused Add+RMSNorm Kernel", steps 2-7):
@@ -118,8 +121,9 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
 
     float rstd, mean_d = 0.f;
     if constexpr (KIND == KIND_LN) {
-      // This thread's Welford triple (count, mean, M2) by two passes over its
-      // own values, then the parallel merge across the row group.
+      // The two-pass of the row, held in registers: the shifted sum gives the
+      // mean, then the squared deviations from it give M2 (no per-part counts
+      // or means to merge; both sums are plain group reductions).
       const float2 pv = splat2(pivot);
       float2 s2 = splat2(0.f);
 #pragma unroll
@@ -133,9 +137,10 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
           s2 = add2(s2, vs);
         }
       }
-      const float cnt = (float)(nvec * VEC);
-      const float mloc = nvec > 0 ? __fdividef(s2.x + s2.y, cnt) : 0.f;
-      const float2 ml = splat2(mloc);
+      float sm[1] = {s2.x + s2.y};
+      group_sum<1>(sm, sh, nw, wig, lane, bar_id, parity);
+      mean_d = sm[0] * inv_h;
+      const float2 ml = splat2(mean_d);
       float2 q2 = splat2(0.f);
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
@@ -150,9 +155,9 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
           q2 = add2(q2, vq);
         }
       }
-      const Welford w = group_welford(Welford{cnt, mloc, q2.x + q2.y}, sh, nw, wig, lane, bar_id, parity);
-      mean_d = w.m;
-      rstd = rsqrtf(w.m2 * inv_h + a.eps);
+      float m2[1] = {q2.x + q2.y};
+      group_sum<1>(m2, sh + 2 * nw, nw, wig, lane, bar_id, parity);
+      rstd = rsqrtf(m2[0] * inv_h + a.eps);
     } else {
       float2 s2 = splat2(0.f);
 #pragma unroll
