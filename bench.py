@@ -167,16 +167,18 @@ class ClockSampler:
 class Shape:
     """Device tensors of one (N, H) shape and argument tuples for the C ABI."""
 
-    def __init__(self, N, H, dev, seed, lib, extra=False):
+    def __init__(self, N, H, dev, seed, lib, extra=False, dtype="bf16"):
         import torch
         from rmsnorm_ln_fwd_gb300 import synth, ops
         self.N, self.H, self.lib, self.dev = N, H, lib, dev
-        host = synth.norm_inputs(N, H, "bf16", seed=seed, with_residual=True, with_dh_stream=extra)
+        host = synth.norm_inputs(N, H, dtype, seed=seed, with_residual=True, with_dh_stream=extra)
+        self.code = {"f32": 0, "bf16": 1, "f16": 2}[dtype]
+        self.esize = 4 if dtype == "f32" else 2
         self.host = host
         t = {k: v.to(dev) for k, v in host.items()}
         self.t = t
         e = torch.empty
-        bf = torch.bfloat16
+        bf = synth.DTYPES[dtype]
         self.y = e(N, H, dtype=bf, device=dev)
         self.yr = e(N, H, dtype=bf, device=dev)
         self.yf = e(N, H, dtype=bf, device=dev)
@@ -192,7 +194,7 @@ class Shape:
         self.dgr = e(H, dtype=bf, device=dev)
         self.wsb = ops.bwd_workspace_bytes(H, dev)
         self.ws = e((self.wsb + 3) // 4, dtype=torch.float32, device=dev)
-        self.bytes = {op: alg_bytes(op, N, H) for op in OPS}
+        self.bytes = {op: alg_bytes(op, N, H, bf.itemsize, bf.itemsize) for op in OPS}
         if extra:
             self.dxf = e(N, H, dtype=bf, device=dev)
             self.dresf = e(N, H, dtype=bf, device=dev)
@@ -200,7 +202,7 @@ class Shape:
 
     def call(self, op, stream):
         L, t, N, H = self.lib, self.t, self.N, self.H
-        BF = 1
+        BF = self.code
         if op == "ln_fwd":
             st = L.ln_forward(t["x"].data_ptr(), H, t["gamma"].data_ptr(), t["beta"].data_ptr(), self.y.data_ptr(),
                               H, self.mean.data_ptr(), self.rstd.data_ptr(), N, H, EPS, BF, BF, stream)
@@ -501,7 +503,7 @@ def run_sweep(args):
         if (N, H) not in cache:
             cache.clear()
             torch.cuda.empty_cache()
-            cache[(N, H)] = Shape(N, H, dev, seed=7, lib=lib, extra=True)
+            cache[(N, H)] = Shape(N, H, dev, seed=7, lib=lib, extra=True, dtype=args.dtype)
         s = cache[(N, H)]
         if op in FORWARD_OF:
             s.call(FORWARD_OF[op], stream.cuda_stream)
@@ -518,9 +520,9 @@ def run_sweep(args):
             ts.append((a, b))
         torch.cuda.synchronize()
         us = [a.elapsed_time(b) * 1e3 for a, b in ts]
-        byts = alg_bytes(op, N, H)
+        byts = s.bytes.get(op) or alg_bytes(op, N, H, s.esize, s.esize)
         med = statistics.median(us)
-        print(json.dumps({"op": op, "N": N, "H": H, "path": args.path, "us_median": round(med, 2),
+        print(json.dumps({"op": op, "N": N, "H": H, "dtype": args.dtype, "path": args.path, "us_median": round(med, 2),
                           "us_min": round(min(us), 2),
                           "gbs": round(byts / (med * 1e-6) / 1e9, 1), "frac": round(byts / (med * 1e-6) / 1e9 / peak, 3),
                           "bytes": byts, "peak": peak, "peak_kind": kind}), flush=True)
@@ -537,7 +539,7 @@ def run_profile_loop(args):
     nl._lib.set_kernel_path(args.path)
     N, H = (int(v) for v in args.shape.split("x"))
     dev = torch.device("cuda", 0)
-    s = Shape(N, H, dev, seed=3, lib=lib, extra=True)
+    s = Shape(N, H, dev, seed=3, lib=lib, extra=True, dtype=args.dtype)
     sh = torch.cuda.current_stream(dev).cuda_stream
     op = args.profile_op
     if op in FORWARD_OF:
@@ -560,6 +562,8 @@ def main():
     p.add_argument("--ref-rows", type=int, default=64)
     p.add_argument("--sweep", action="store_true", help="per-call timings over every configured shape")
     p.add_argument("--sweep-iters", type=int, default=50)
+    p.add_argument("--dtype", choices=["bf16", "f16", "f32"], default="bf16",
+                   help="row dtype of --sweep / --profile-op (the step itself is bf16)")
     p.add_argument("--path", type=int, default=0, help="kernel-family policy: 0 auto, 1 register rows, 2 loop, 3 bulk-copy pipeline")
     p.add_argument("--profile-op", choices=list(OPS + EXTRA_OPS), default=None)
     p.add_argument("--shape", default="8192x1024")

@@ -19,7 +19,8 @@
  * Dtypes.  `x_dtype` types the row tensors (x, residual, y, h_out, dy, dx);
  *   `w_dtype` types gamma, beta, dgamma, dbeta and must equal x_dtype or be
  *   NORM_F32.  All statistics and arithmetic are fp32; stored values are
- *   rounded to nearest, ties to even.
+ *   rounded to nearest, ties to even (an fp16 value past 65504 rounds to
+ *   infinity).
  * eps.  Added INSIDE the square root: rstd = 1/sqrt(var + eps).  eps must be
  *   finite and > 0.
  * Alignment.  Rows whose pointers and strides are 16-byte aligned take the
@@ -56,7 +57,10 @@ typedef enum {
   NORM_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
 } norm_status;
 
-typedef enum { NORM_F32 = 0, NORM_BF16 = 1 } norm_dtype;
+/* fp32, bfloat16 and IEEE binary16 ("Skill: Write a Triton LayerNorm Kernel",
+ * Inputs the agent should gather first, item 3: fp16, bf16 or fp32 inputs,
+ * statistics accumulated in fp32). */
+typedef enum { NORM_F32 = 0, NORM_BF16 = 1, NORM_F16 = 2 } norm_dtype;
 
 /*
  * LayerNorm forward.  "Skill: Write a Triton LayerNorm Kernel", Required

@@ -46,6 +46,7 @@ __all__ = [
     "two_pass_stats",
     "round_to_float32",
     "round_to_bfloat16",
+    "round_to_float16",
     "round_to_dtype",
 ]
 
@@ -324,6 +325,18 @@ def round_to_bfloat16(a):
     return out
 
 
+def round_to_float16(a):
+    """float32-representable values -> nearest IEEE binary16 (ties to even), as float64.
+
+    numpy's float32 -> float16 conversion is the rounding step: binary16 keeps
+    10 fraction bits, has subnormals down to 2^-24, and values from 65520 up
+    round to infinity.
+    """
+    f = np.asarray(a, dtype=np.float64).astype(np.float32)
+    with np.errstate(over="ignore"):
+        return f.astype(np.float16).astype(np.float64)
+
+
 def round_to_dtype(a, dtype):
     """Round float64 values to the storage dtype named by ``dtype``."""
     name = str(dtype).replace("torch.", "")
@@ -331,6 +344,8 @@ def round_to_dtype(a, dtype):
         return round_to_float32(a)
     if name in ("bfloat16", "bf16"):
         return round_to_bfloat16(a)
+    if name in ("float16", "f16", "fp16", "half"):
+        return round_to_float16(a)
     if name in ("float64", "f64"):
         return np.asarray(a, dtype=np.float64)
     raise ValueError(f"unsupported dtype {dtype!r}")

@@ -20,6 +20,7 @@ NORM_ERR_CUDA = 4
 
 NORM_F32 = 0
 NORM_BF16 = 1
+NORM_F16 = 2
 
 # name -> (restype, argtypes), one entry per function declared in include/norm.h
 _P = ctypes.c_void_p

@@ -1,12 +1,15 @@
 // Device helpers shared by the forward and backward kernels of libnorm.
 //
 // Everything here is bandwidth plumbing: 128-bit global loads/stores, bf16
-// packing, warp-shuffle reductions and the parallel Welford merge.  The
+// and fp16 packing, warp-shuffle reductions and the parallel Welford merge.  The
 // normalisation arithmetic itself lives in norm_fwd.cu / norm_bwd.cu.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <type_traits>
 #include <stdint.h>
 
 namespace normk {
@@ -18,6 +21,10 @@ struct F32 {
 };
 struct BF16 {
   using T = __nv_bfloat16;
+  static constexpr int VEC = 8;
+};
+struct F16 {
+  using T = __half;
   static constexpr int VEC = 8;
 };
 
@@ -47,7 +54,8 @@ __device__ __forceinline__ void st_vec(void* p, const uint4& v) {
 
 // ---------------------------------------------------------------------------
 // Packing: a 16-byte vector <-> VEC fp32 values (element 0 in the low bits).
-// bf16 -> fp32 is exact (a shift); fp32 -> bf16 rounds to nearest even.
+// bf16/fp16 -> fp32 is exact; fp32 -> bf16/fp16 rounds to nearest even (fp16
+// overflows to infinity past its largest finite value, as IEEE rounding does).
 // ---------------------------------------------------------------------------
 template <typename D>
 __device__ __forceinline__ void unpack(const uint4& u, float* f);
@@ -72,8 +80,24 @@ __device__ __forceinline__ void unpack<BF16>(const uint4& u, float* f) {
   f[7] = __uint_as_float(u.w & 0xffff0000u);
 }
 
+template <>
+__device__ __forceinline__ void unpack<F16>(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 b = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
@@ -92,11 +116,19 @@ __device__ __forceinline__ uint4 pack<BF16>(const float* f) {
                     pack_bf16x2(f[6], f[7]));
 }
 
+template <>
+__device__ __forceinline__ uint4 pack<F16>(const float* f) {
+  return make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+                    pack_f16x2(f[6], f[7]));
+}
+
 // Scalar element access (tails and the unaligned path).
 template <typename D>
 __device__ __forceinline__ float load_elem(const void* base, int64_t i) {
   if constexpr (sizeof(typename D::T) == 4) {
     return reinterpret_cast<const float*>(base)[i];
+  } else if constexpr (std::is_same<typename D::T, __half>::value) {
+    return __half2float(reinterpret_cast<const __half*>(base)[i]);
   } else {
     return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
   }
@@ -106,6 +138,8 @@ template <typename D>
 __device__ __forceinline__ void store_elem(void* base, int64_t i, float v) {
   if constexpr (sizeof(typename D::T) == 4) {
     reinterpret_cast<float*>(base)[i] = v;
+  } else if constexpr (std::is_same<typename D::T, __half>::value) {
+    reinterpret_cast<__half*>(base)[i] = __float2half_rn(v);
   } else {
     reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
   }
@@ -423,6 +457,14 @@ __device__ __forceinline__ void unpack2<BF16>(const uint4& u, float2* p) {
   p[3] = make_float2(__uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u));
 }
 
+template <>
+__device__ __forceinline__ void unpack2<F16>(const uint4& u, float2* p) {
+  p[0] = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  p[1] = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  p[2] = __half22float2(*reinterpret_cast<const __half2*>(&u.z));
+  p[3] = __half22float2(*reinterpret_cast<const __half2*>(&u.w));
+}
+
 template <typename D>
 __device__ __forceinline__ uint4 pack2(const float2* p);
 
@@ -436,6 +478,12 @@ template <>
 __device__ __forceinline__ uint4 pack2<BF16>(const float2* p) {
   return make_uint4(pack_bf16x2(p[0].x, p[0].y), pack_bf16x2(p[1].x, p[1].y), pack_bf16x2(p[2].x, p[2].y),
                     pack_bf16x2(p[3].x, p[3].y));
+}
+
+template <>
+__device__ __forceinline__ uint4 pack2<F16>(const float2* p) {
+  return make_uint4(pack_f16x2(p[0].x, p[0].y), pack_f16x2(p[1].x, p[1].y), pack_f16x2(p[2].x, p[2].y),
+                    pack_f16x2(p[3].x, p[3].y));
 }
 
 // gamma/beta for the full vector at column c as pairs (p == nullptr: fill).

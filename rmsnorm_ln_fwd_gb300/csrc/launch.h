@@ -8,7 +8,7 @@
 
 namespace normk {
 
-enum Dtype : int { DT_F32 = 0, DT_BF16 = 1 };
+enum Dtype : int { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
 enum Kind : int { KIND_LN = 0, KIND_RMS = 1, KIND_FUSED = 2 };
 
 // Kernel-family policy (norm_set_kernel_path).  AUTO: register rows when a

@@ -102,11 +102,11 @@ bool current_device_info(DeviceInfo* out) {
   return true;
 }
 
-size_t elem_size(norm_dtype d) { return d == NORM_BF16 ? 2 : 4; }
+size_t elem_size(norm_dtype d) { return d == NORM_F32 ? 4 : 2; }
 
 norm_status check_dtypes(norm_dtype x, norm_dtype w) {
-  const bool xv = x == NORM_F32 || x == NORM_BF16;
-  const bool wv = w == NORM_F32 || w == NORM_BF16;
+  const bool xv = x == NORM_F32 || x == NORM_BF16 || x == NORM_F16;
+  const bool wv = w == NORM_F32 || w == NORM_BF16 || w == NORM_F16;
   if (!xv || !wv) return NORM_ERR_UNSUPPORTED;
   if (w != x && w != NORM_F32) return NORM_ERR_UNSUPPORTED;
   return NORM_OK;
@@ -159,7 +159,9 @@ norm_status launch_result(const char* where, cudaError_t e) {
   return NORM_ERR_CUDA;
 }
 
-normk::Dtype to_dt(norm_dtype d) { return d == NORM_BF16 ? normk::DT_BF16 : normk::DT_F32; }
+normk::Dtype to_dt(norm_dtype d) {
+  return d == NORM_BF16 ? normk::DT_BF16 : (d == NORM_F16 ? normk::DT_F16 : normk::DT_F32);
+}
 
 norm_status forward_common(int kind, const void* x, int64_t ldx, const void* res, int64_t ldr,
                            const void* gamma, const void* beta, void* y, int64_t ldy, void* h,

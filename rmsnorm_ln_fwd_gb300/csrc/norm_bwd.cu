@@ -790,6 +790,13 @@ cudaError_t launch_backward(int kind, Dtype dt, BwdArgs a, void* dgamma, void* d
       default: return launch_bwd_typed<KIND_FUSED, BF16>(a, dgamma, nullptr, dev, s);
     }
   }
+  if (dt == DT_F16) {
+    switch (kind) {
+      case KIND_LN: return launch_bwd_typed<KIND_LN, F16>(a, dgamma, dbeta, dev, s);
+      case KIND_RMS: return launch_bwd_typed<KIND_RMS, F16>(a, dgamma, nullptr, dev, s);
+      default: return launch_bwd_typed<KIND_FUSED, F16>(a, dgamma, nullptr, dev, s);
+    }
+  }
   switch (kind) {
     case KIND_LN: return launch_bwd_typed<KIND_LN, F32>(a, dgamma, dbeta, dev, s);
     case KIND_RMS: return launch_bwd_typed<KIND_RMS, F32>(a, dgamma, nullptr, dev, s);

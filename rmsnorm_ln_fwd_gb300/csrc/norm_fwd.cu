@@ -646,6 +646,13 @@ cudaError_t launch_forward(int kind, Dtype dt, FwdArgs a, const DeviceInfo& dev,
       default: return launch_fwd_typed<KIND_FUSED, BF16>(a, dev, s);
     }
   }
+  if (dt == DT_F16) {
+    switch (kind) {
+      case KIND_LN: return launch_fwd_typed<KIND_LN, F16>(a, dev, s);
+      case KIND_RMS: return launch_fwd_typed<KIND_RMS, F16>(a, dev, s);
+      default: return launch_fwd_typed<KIND_FUSED, F16>(a, dev, s);
+    }
+  }
   switch (kind) {
     case KIND_LN: return launch_fwd_typed<KIND_LN, F32>(a, dev, s);
     case KIND_RMS: return launch_fwd_typed<KIND_RMS, F32>(a, dev, s);

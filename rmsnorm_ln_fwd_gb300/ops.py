@@ -16,14 +16,14 @@ import torch
 
 from . import _lib
 
-_DT = {torch.float32: _lib.NORM_F32, torch.bfloat16: _lib.NORM_BF16}
+_DT = {torch.float32: _lib.NORM_F32, torch.bfloat16: _lib.NORM_BF16, torch.float16: _lib.NORM_F16}
 
 
 def _dtype_code(t: torch.Tensor, what: str) -> int:
     try:
         return _DT[t.dtype]
     except KeyError:
-        raise TypeError(f"{what}: dtype {t.dtype} not supported (float32 or bfloat16)") from None
+        raise TypeError(f"{what}: dtype {t.dtype} not supported (float32, bfloat16 or float16)") from None
 
 
 def _rows(t: torch.Tensor, what: str):

@@ -20,7 +20,7 @@ import torch
 # not depend on which other tensors are drawn or on their shapes.
 _STREAM = {"x": 1, "gamma": 2, "beta": 3, "dy": 4, "residual": 5, "dh_stream": 6}
 
-DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
 def _gen(seed: int, role: str) -> torch.Generator:

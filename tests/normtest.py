@@ -7,10 +7,11 @@ Tolerances (the readings of the stated targets):
   per tensor, max_i |a_i - r_i| / max_i |r_i| (an elementwise ratio is
   undefined where r_i ~ 0).  rstd, never near 0, is checked elementwise; the
   saved mean, often near 0, against the RMS of its row.
-* bf16 outputs (y, dx): |a_i - r_i| <= ulp_bf16(r_i) + 2^-20 * S_i, i.e. one
-  bf16 ulp of the exact value plus the fp32 evaluation error of the expression,
-  S_i being the magnitude of the terms that are summed to form element i.
-* dgamma/dbeta in bf16: relative RMS error ||a - r||_2 / ||r||_2 <= 5e-3.
+* bf16 / fp16 outputs (y, dx): |a_i - r_i| <= ulp(r_i) + 2^-20 * S_i, i.e.
+  one ulp of the storage dtype at the exact value plus the fp32 evaluation
+  error of the expression, S_i being the magnitude of the terms that are
+  summed to form element i.  Equal values (infinities included) pass.
+* dgamma/dbeta in bf16 / fp16: relative RMS error ||a - r||_2 / ||r||_2 <= 5e-3.
 * the stored residual sum h: bit-exact.
 """
 
@@ -35,6 +36,13 @@ def bf16_ulp(r):
     return 2.0 ** (np.floor(np.log2(a)) - 7)
 
 
+def f16_ulp(r):
+    """Spacing of IEEE binary16 at |r| (10 fraction bits; 2^-24 below 2^-14)."""
+    a = np.maximum(np.abs(np.asarray(r, dtype=np.float64)), 2.0 ** -14)
+    a = np.where(np.isfinite(a), a, 65504.0)
+    return 2.0 ** (np.floor(np.log2(a)) - 10)
+
+
 def normwise_rel(got, ref):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
@@ -57,25 +65,36 @@ def check_f32(got, ref, what, tol=F32_TOL):
     return e
 
 
-def check_bf16(got, ref, scale, what):
+def check_bf16(got, ref, scale, what, ulp=bf16_ulp, allow_inf=False):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
-    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
-    err = np.abs(got - ref)
-    tol = bf16_ulp(ref) + BF16_SLACK * np.asarray(scale, dtype=np.float64)
+    if allow_inf:
+        assert not np.any(np.isnan(got)), f"{what}: NaN values"
+    else:
+        assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    with np.errstate(invalid="ignore"):
+        err = np.where(got == ref, 0.0, np.abs(got - ref))
+    err = np.where(np.isnan(err), np.inf, err)
+    tol = ulp(ref) + BF16_SLACK * np.asarray(scale, dtype=np.float64)
     bad = err > tol
     if np.any(bad):
         i = np.unravel_index(np.argmax(err - tol), err.shape)
-        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements beyond 1 bf16 ulp + fp32 slack; "
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements beyond 1 ulp + fp32 slack; "
                              f"worst at {i}: got {got[i]!r} want {ref[i]!r}")
-    strict = int(np.sum(err > bf16_ulp(ref)))
+    strict = int(np.sum(err > ulp(ref)))
     return strict
 
 
-def check_out(got, ref, scale, dtype, what):
+def check_out(got, ref, scale, dtype, what, allow_inf=False):
     if dtype == torch.float32:
         return check_f32(got, ref, what)
-    return check_bf16(got, ref, scale, what)
+    if dtype == torch.float16:
+        return check_bf16(got, ref, scale, what, ulp=f16_ulp, allow_inf=allow_inf)
+    return check_bf16(got, ref, scale, what, allow_inf=allow_inf)
+
+
+DT_NAME = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
+DT_ORACLE = {torch.float32: "float32", torch.bfloat16: "bfloat16", torch.float16: "float16"}
 
 
 def check_param(got, ref, dtype, what):

@@ -375,6 +375,27 @@ def pin_bf16_rounding(O):
     _close(O.round_to_float32(np.array([1.0 + 2.0 ** -30])), [1.0], 0, 0, "f32 rounding")
 
 
+def pin_f16_rounding(O):
+    r = _rng(6)
+    vals = np.concatenate([
+        r.standard_normal(20000) * 10.0 ** r.integers(-9, 6, 20000),
+        # exact ties: 1 + k*2^-11 sits halfway between binary16 neighbours for odd k
+        1.0 + np.arange(1, 64, 2) * 2.0 ** -11,
+        -(1.0 + np.arange(1, 64, 2) * 2.0 ** -11),
+        # subnormal ties (k*2^-25, k odd) and the overflow threshold
+        np.arange(1, 40, 2) * 2.0 ** -25,
+        [0.0, -0.0, 65504.0, 65519.99, 65520.0, 1e6, -1e6, 2.0 ** -24, 2.0 ** -26, np.inf, -np.inf],
+    ])
+    f32 = vals.astype(np.float32)
+    mine = O.round_to_float16(f32)
+    ref = torch.from_numpy(f32).to(torch.float16).double().numpy()
+    assert np.array_equal(mine, ref), "fp16 rounding differs from torch"
+    assert O.round_to_float16(np.array([65519.0]))[0] == 65504.0
+    assert np.isinf(O.round_to_float16(np.array([65520.0]))[0])
+    assert O.round_to_float16(np.array([3 * 2.0 ** -25]))[0] == 2.0 ** -23  # tie to even (2 units)
+    assert np.all(np.isnan(O.round_to_float16(np.array([np.nan], dtype=np.float32))))
+
+
 ALL_PINS = [
     pin_ln_forward_vs_torch,
     pin_rms_forward_vs_torch,
@@ -390,4 +411,5 @@ ALL_PINS = [
     pin_fused,
     pin_fused_backward_from_h,
     pin_bf16_rounding,
+    pin_f16_rounding,
 ]

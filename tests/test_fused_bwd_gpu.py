@@ -17,12 +17,13 @@ import torch
 
 import oracle as O
 import rmsnorm_ln_fwd_gb300 as nl
-from normtest import Guarded, check_out, check_param, np64, rms_dx_scale
+from normtest import DT_NAME, Guarded, check_out, check_param, np64, rms_dx_scale
 from rmsnorm_ln_fwd_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-BF, F32 = torch.bfloat16, torch.float32
+BF, F32, F16 = torch.bfloat16, torch.float32, torch.float16
+CODE = {F32: 0, BF: 1, F16: 2}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,7 +36,7 @@ def _gpu():
 
 
 def _inputs(N, H, dt, seed):
-    d = synth.norm_inputs(N, H, "bf16" if dt == BF else "f32", None, seed, with_beta=False,
+    d = synth.norm_inputs(N, H, DT_NAME[dt], None, seed, with_beta=False,
                           with_residual=True, with_dh_stream=True)
     return {k: v.to(DEV) for k, v in d.items()}
 
@@ -70,7 +71,7 @@ def fused_bwd_case(N, H, dt, eps=1e-6, seed=0, with_dh=True, residual_grad="sepa
     scale = rms_dx_scale(dyn, hn, gn, eps)
     if dhn is not None:
         scale = scale + np.abs(dhn)
-    if saved_rstd and dt == BF:
+    if saved_rstd and dt != F32:
         # dx = rstd*g - rstd^3*h*sum(g*h)/H: a relative rstd difference d per
         # row moves dx by at most 3*d times its terms' magnitude.
         r_h = O.rms_norm_forward(hn, None, eps)[1]
@@ -95,7 +96,7 @@ def fused_bwd_case(N, H, dt, eps=1e-6, seed=0, with_dh=True, residual_grad="sepa
 H_SWEEP = [1, 7, 8, 32, 33, 64, 256, 1000, 1024, 2049, 4096, 5120, 8192, 12288, 16384, 40000]
 
 
-@pytest.mark.parametrize("dt", [BF, F32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dt", [BF, F32, F16], ids=["bf16", "f32", "f16"])
 @pytest.mark.parametrize("H", H_SWEEP)
 def test_fused_bwd_sweep(H, dt):
     fused_bwd_case(37 if H > 8192 else 67, H, dt)
@@ -115,7 +116,7 @@ def test_fused_bwd_residual_grad_modes(mode, H, dt):
 
 @pytest.mark.parametrize("into", ["dy", "dh"])
 @pytest.mark.parametrize("mode", ["separate", "none", "same"])
-@pytest.mark.parametrize("H,dt", [(1024, BF), (1000, BF), (16384, BF), (512, F32)])
+@pytest.mark.parametrize("H,dt", [(1024, BF), (1000, BF), (16384, BF), (512, F32), (2048, F16)])
 def test_fused_bwd_in_place(into, mode, H, dt):
     fused_bwd_case(67, H, dt, residual_grad=mode, dx_into=into)
 
@@ -126,7 +127,8 @@ def test_fused_bwd_row_counts(N, H, dt):
     fused_bwd_case(N, H, dt)
 
 
-@pytest.mark.parametrize("H,dt", [(1024, BF), (4096, BF), (5120, BF), (1000, F32), (2048, F32)])
+@pytest.mark.parametrize("H,dt", [(1024, BF), (4096, BF), (5120, BF), (1000, F32), (2048, F32), (1024, F16),
+                                  (4096, F16)])
 def test_fused_bwd_training_chain(H, dt):
     """Forward then backward with the forward's own saved rstd."""
     fused_bwd_case(200, H, dt, saved_rstd=True)
@@ -170,7 +172,7 @@ def test_fused_bwd_strides_and_alignment(H, ld, off, dt):
     ws_bytes = nl.bwd_workspace_bytes(H)
     ws = torch.empty((ws_bytes + 3) // 4, dtype=torch.float32, device=DEV)
     dg = torch.empty(H, dtype=dt, device=DEV)
-    code = nl._lib.NORM_BF16 if dt == BF else nl._lib.NORM_F32
+    code = CODE[dt]
     st = lib.fused_add_rms_backward(dy.data_ptr(), ld, hs.data_ptr(), ld, rstd.data_ptr(), t["gamma"].data_ptr(),
                                     dh.data_ptr(), ld, dxs.data_ptr(), ld, drs.data_ptr(), ld + 8, dg.data_ptr(),
                                     ws.data_ptr(), ws_bytes, N, H, code, code,
@@ -185,7 +187,7 @@ def test_fused_bwd_strides_and_alignment(H, ld, off, dt):
     check_param(np64(dg), dgr, dt, f"strided dgamma {H}/{ld}+{off}")
 
 
-@pytest.mark.parametrize("H,dt", [(1024, BF), (1000, BF), (16384, BF), (40000, F32), (7, F32)])
+@pytest.mark.parametrize("H,dt", [(1024, BF), (1000, BF), (16384, BF), (40000, F32), (7, F32), (4096, F16)])
 def test_fused_bwd_guard_bands(H, dt):
     N, eps = 67, 1e-6
     t = _inputs(N, H, dt, 5)
@@ -195,7 +197,7 @@ def test_fused_bwd_guard_bands(H, dt):
     lib = nl._lib.load()
     ws_bytes = nl.bwd_workspace_bytes(H)
     ws = torch.empty((ws_bytes + 3) // 4, dtype=torch.float32, device=DEV)
-    code = nl._lib.NORM_BF16 if dt == BF else nl._lib.NORM_F32
+    code = CODE[dt]
     st = lib.fused_add_rms_backward(t["dy"].data_ptr(), H, h.data_ptr(), H, rstd.data_ptr(), t["gamma"].data_ptr(),
                                     t["dh_stream"].data_ptr(), H, gx.t.data_ptr(), H, gr.t.data_ptr(), H,
                                     gg.t.data_ptr(), ws.data_ptr(), ws_bytes, N, H, code, code,

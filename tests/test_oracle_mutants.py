@@ -132,6 +132,16 @@ def _bf16_truncate(a):
     return bits.view(np.float32).astype(np.float64)
 
 
+def _f16_truncate(a):
+    f = np.asarray(a, dtype=np.float64).astype(np.float32)
+    with np.errstate(over="ignore"):
+        h = f.astype(np.float16).astype(np.float32)
+    # step one binary16 unit toward zero wherever nearest rounding went away from zero
+    away = np.abs(h) > np.abs(f)
+    h = np.where(away, np.nextafter(h.astype(np.float16), np.float16(0)).astype(np.float32), h)
+    return h.astype(np.float64)
+
+
 MUTANTS = {
     "ln_unbiased_variance": dict(layer_norm_forward=_ln_fwd(var_div=lambda H: max(H - 1, 1))),
     "ln_eps_outside_sqrt": dict(layer_norm_forward=_ln_fwd(eps_outside=True)),
@@ -153,6 +163,7 @@ MUTANTS = {
     "welford_merge_wrong_weight": dict(welford_merge=_merge_wrong),
     "welford_recurrence_old_mean_twice": dict(welford_sequential=_welford_seq_wrong),
     "bf16_truncates": dict(round_to_bfloat16=_bf16_truncate),
+    "f16_truncates": dict(round_to_float16=_f16_truncate),
 }
 
 

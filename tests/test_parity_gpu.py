@@ -13,13 +13,14 @@ import torch
 
 import oracle as O
 import rmsnorm_ln_fwd_gb300 as nl
-from normtest import (Guarded, check_bf16, check_f32, check_mean, check_out, check_param, check_rstd, ln_dx_scale,
-                      ln_y_scale, np64, rms_dx_scale, rms_y_scale)
+from normtest import (DT_NAME, DT_ORACLE, Guarded, check_bf16, check_f32, check_mean, check_out, check_param,
+                      check_rstd, ln_dx_scale, ln_y_scale, np64, rms_dx_scale, rms_y_scale)
 from rmsnorm_ln_fwd_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-BF, F32 = torch.bfloat16, torch.float32
+BF, F32, F16 = torch.bfloat16, torch.float32, torch.float16
+DTS, DT_IDS = [BF, F32, F16], ["bf16", "f32", "f16"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -32,8 +33,7 @@ def _gpu():
 
 
 def _inputs(N, H, dt, seed=0, wdt=None, **kw):
-    d = synth.norm_inputs(N, H, "bf16" if dt == BF else "f32",
-                          None if wdt is None else ("bf16" if wdt == BF else "f32"), seed, **kw)
+    d = synth.norm_inputs(N, H, DT_NAME[dt], None if wdt is None else DT_NAME[wdt], seed, **kw)
     return {k: v.to(DEV) for k, v in d.items()}
 
 
@@ -81,7 +81,7 @@ def fused_case(N, H, dt, eps=1e-6, seed=0, wdt=None, inplace=None):
     y, h, rstd = nl.fused_add_rms_forward(t["x"], t["residual"], t["gamma"], eps, h_out=h_out)
     torch.cuda.synchronize()
     x, r, gn = np64(x0), np64(r0), np64(t["gamma"])
-    yr, hr, rr = O.fused_add_rms_norm_forward(x, r, gn, eps, "bfloat16" if dt == BF else "float32")
+    yr, hr, rr = O.fused_add_rms_norm_forward(x, r, gn, eps, DT_ORACLE[dt])
     assert np.array_equal(np64(h), hr), f"fused h {N}x{H}: not bit-exact"
     check_out(np64(y), yr, rms_y_scale(x + r, rr, gn), dt, f"fused y {N}x{H}")
     check_rstd(np64(rstd), rr, f"fused rstd {N}x{H}")
@@ -108,19 +108,19 @@ H_SWEEP = [1, 2, 7, 8, 31, 32, 33, 64, 127, 128, 255, 256, 512, 768, 1000, 1024,
            5120, 8192, 16383, 16384, 20480, 32768, 40000]
 
 
-@pytest.mark.parametrize("dt", [BF, F32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dt", DTS, ids=DT_IDS)
 @pytest.mark.parametrize("H", H_SWEEP)
 def test_ln_sweep(H, dt):
     ln_case(37, H, dt, seed=H)
 
 
-@pytest.mark.parametrize("dt", [BF, F32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dt", DTS, ids=DT_IDS)
 @pytest.mark.parametrize("H", H_SWEEP)
 def test_rms_sweep(H, dt):
     rms_case(37, H, dt, seed=H + 1)
 
 
-@pytest.mark.parametrize("dt", [BF, F32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dt", DTS, ids=DT_IDS)
 @pytest.mark.parametrize("H", H_SWEEP)
 def test_fused_sweep(H, dt):
     fused_case(37, H, dt, seed=H + 2)
@@ -128,7 +128,7 @@ def test_fused_sweep(H, dt):
 
 # P2's validation list: D in {64, 128, 512, 768, 1024, 2049}
 @pytest.mark.parametrize("H", [64, 128, 512, 768, 1024, 2049])
-@pytest.mark.parametrize("dt", [BF, F32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dt", DTS, ids=DT_IDS)
 def test_ln_page_validation_widths(H, dt):
     ln_case(64, H, dt, seed=7 + H)
 
@@ -150,15 +150,16 @@ def test_row_counts(N, H, dt):
 # parameter variants
 # ---------------------------------------------------------------------------
 
+@pytest.mark.parametrize("dt", [BF, F16], ids=["bf16", "f16"])
 @pytest.mark.parametrize("H", [1024, 5120, 1000])
-def test_bf16_rows_fp32_params(H):
-    ln_case(64, H, BF, wdt=F32, seed=3)
-    rms_case(64, H, BF, wdt=F32, seed=4)
-    fused_case(64, H, BF, wdt=F32, seed=5)
+def test_half_rows_fp32_params(H, dt):
+    ln_case(64, H, dt, wdt=F32, seed=3)
+    rms_case(64, H, dt, wdt=F32, seed=4)
+    fused_case(64, H, dt, wdt=F32, seed=5)
 
 
 @pytest.mark.parametrize("H", [256, 4096, 33])
-@pytest.mark.parametrize("dt", [BF, F32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dt", DTS, ids=DT_IDS)
 def test_no_affine(H, dt):
     ln_case(16, H, dt, gamma=False, beta=False, seed=11)
     ln_case(16, H, dt, gamma=True, beta=False, seed=12)
@@ -175,8 +176,39 @@ def test_stability_offset_rows_fp32():
     rms_case(8192, 1024, F32, x_offset=1000.0, x_scale=1e-2, seed=22)
 
 
+@pytest.mark.parametrize("H", [1024, 5120, 1000])
+def test_f16_small_activations(H):
+    """|x| ~ 1e-3 in fp16: x*x would underflow in fp16; the statistics are fp32."""
+    ln_case(64, H, F16, x_scale=1e-3, seed=61)
+    rms_case(64, H, F16, x_scale=1e-3, seed=62)
+
+
+@pytest.mark.parametrize("H", [1024, 1000])
+def test_f16_output_overflow(H):
+    """gamma = 40000 pushes |y| past 65504: those outputs round to +-inf,
+    exactly where the oracle's rounding of the exact value does."""
+    N, eps = 32, 1e-5
+    t = _inputs(N, H, F16, seed=63)
+    gamma = torch.full((H,), 40000.0, dtype=F16, device=DEV)
+    y, _, _ = nl.ln_forward(t["x"], gamma, t["beta"], eps)
+    yr_rms, _ = nl.rms_forward(t["x"], gamma, eps)
+    torch.cuda.synchronize()
+    x, bn = np64(t["x"]), np64(t["beta"])
+    for got, (ref, *_) in ((np64(y), O.layer_norm_forward(x, np64(gamma), bn, eps)),
+                           (np64(yr_rms), O.rms_norm_forward(x, np64(gamma), eps))):
+        want = O.round_to_float16(ref)
+        # away from the overflow threshold (65520) the inf pattern is decided
+        sure = np.abs(np.abs(ref) - 65520.0) > 64.0
+        assert np.any(np.isinf(want)), "case does not overflow"
+        assert np.array_equal(np.isinf(got) & sure, np.isinf(want) & sure)
+        assert np.array_equal(np.sign(got[np.isinf(got)]), np.sign(want[np.isinf(got)]))
+        fin = np.isfinite(want) & sure
+        err = np.abs(got[fin] - ref[fin])
+        assert np.all(err <= 2.0 * np.abs(ref[fin]) * 2.0 ** -11 + 1e-3), "finite outputs"
+
+
 @pytest.mark.parametrize("H", [1, 8, 1024, 5120, 40000])
-@pytest.mark.parametrize("dt", [BF, F32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dt", DTS, ids=DT_IDS)
 def test_zero_variance_rows(H, dt):
     """Constant rows: y = beta, rstd = eps^-1/2, dx = rstd*(g - mean(g))."""
     N, eps = 5, 1e-5
@@ -209,7 +241,7 @@ def _strided(src, ld, offset=0):
     return v
 
 
-@pytest.mark.parametrize("dt", [BF, F32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dt", DTS, ids=DT_IDS)
 @pytest.mark.parametrize("H,ld,off", [(1024, 1032, 0), (1024, 1027, 0), (1024, 1024, 1), (5120, 5123, 3),
                                       (96, 100, 2)])
 def test_strides_and_alignment(H, ld, off, dt):
@@ -238,7 +270,7 @@ def test_strides_and_alignment(H, ld, off, dt):
     hb = _strided(torch.zeros_like(t["x"]), ld, off)
     yf, h, _ = nl.fused_add_rms_forward(x, r, t["gamma"], 1e-6, h_out=hb)
     torch.cuda.synchronize()
-    yfr, hr, rfr = O.fused_add_rms_norm_forward(xn, np64(r), gn, 1e-6, "bfloat16" if dt == BF else "float32")
+    yfr, hr, rfr = O.fused_add_rms_norm_forward(xn, np64(r), gn, 1e-6, DT_ORACLE[dt])
     assert np.array_equal(np64(h), hr)
     check_out(np64(yf), yfr, rms_y_scale(xn + np64(r), rfr, gn), dt, "strided fused y")
 
@@ -260,7 +292,7 @@ def test_three_dim_input():
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("inplace", ["x", "residual"])
-@pytest.mark.parametrize("H,dt", [(4096, BF), (1000, BF), (40000, BF), (512, F32)])
+@pytest.mark.parametrize("H,dt", [(4096, BF), (1000, BF), (40000, BF), (512, F32), (4096, F16)])
 def test_fused_inplace(H, dt, inplace):
     fused_case(33, H, dt, seed=61, inplace=inplace)
 
@@ -286,7 +318,8 @@ def test_ln_inplace_y_and_dx(H, dt):
 # guard bands, determinism, empty inputs, error paths on the device
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("H,dt", [(1024, BF), (1000, BF), (5120, BF), (16384, BF), (40000, F32), (7, F32)])
+@pytest.mark.parametrize("H,dt", [(1024, BF), (1000, BF), (5120, BF), (16384, BF), (40000, F32), (7, F32),
+                                  (5120, F16), (1000, F16)])
 def test_guard_bands(H, dt):
     N, eps = 19, 1e-5
     t = _inputs(N, H, dt, seed=81)
@@ -294,7 +327,7 @@ def test_guard_bands(H, dt):
     mean = Guarded((N,), F32, DEV)
     rstd = Guarded((N,), F32, DEV)
     lib = nl.load_library()
-    code = 1 if dt == BF else 0
+    code = {F32: 0, BF: 1, F16: 2}[dt]
     st = lib.ln_forward(t["x"].data_ptr(), H, t["gamma"].data_ptr(), t["beta"].data_ptr(), y.t.data_ptr(), H,
                         mean.t.data_ptr(), rstd.t.data_ptr(), N, H, eps, code, code,
                         torch.cuda.current_stream().cuda_stream)
@@ -334,7 +367,7 @@ def test_deterministic(H, dt):
         assert torch.equal(a.view(torch.uint8) if a.dtype == BF else a, b.view(torch.uint8) if b.dtype == BF else b)
 
 
-@pytest.mark.parametrize("dt", [BF, F32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dt", DTS, ids=DT_IDS)
 def test_empty_rows(dt):
     H = 64
     x = torch.empty(0, H, dtype=dt, device=DEV)
@@ -375,7 +408,8 @@ def test_device_side_errors():
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("path", [1, 2, 3], ids=["rows", "loop", "staged"])
-@pytest.mark.parametrize("H,dt", [(1024, BF), (5120, BF), (16384, BF), (2048, F32), (256, F32), (96, BF)])
+@pytest.mark.parametrize("H,dt", [(1024, BF), (5120, BF), (16384, BF), (2048, F32), (256, F32), (96, BF),
+                                  (2048, F16), (16384, F16)])
 def test_forced_kernel_paths(path, H, dt):
     nl._lib.set_kernel_path(path)
     try:
