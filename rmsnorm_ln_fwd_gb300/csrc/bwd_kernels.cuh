@@ -1,0 +1,787 @@
+// Backward kernel templates and their launch logic, instantiated per row
+// dtype by norm_bwd_f32.cu, norm_bwd_bf16.cu and norm_bwd_f16.cu.
+//
+// Backward kernels: LayerNorm and RMSNorm grad_input plus the gamma/beta
+// gradients through a bounded fp32 partial reduction.
+//
+// Math ("Skill: Write CUDA LayerNorm Kernel", Required reasoning process
+// step 8; the RMSNorm form is derived from its forward):
+//   g = dy * gamma,  x_hat = (x - mean) * rstd   (RMSNorm: x * rstd)
+//   LayerNorm: dx = rstd * (g - sum(g)/H - x_hat * sum(g*x_hat)/H)
+//   RMSNorm:   dx = rstd * (g - x_hat * sum(g*x_hat)/H)
+//   dgamma = sum over rows of dy * x_hat,  dbeta = sum over rows of dy.
+// The saved fp32 mean can sit half an fp32 ulp away from the true mean; for
+// rows with a large common offset that is a visible constant shift of x_hat.
+// Because mean(x_hat) = 0 exactly, the kernel also sums x_hat and subtracts
+// its row mean, which removes that shift (one extra value in the same
+// reduction).
+//
+// Structure ("Rewrite Triton normalization backward kernel_1 (#499)",
+// Summary items 1-2): a fixed grid of P = 2 x SM-count CTAs grid-strides the
+// rows.  Each thread owns fixed columns, so its dgamma/dbeta accumulators stay
+// in fp32 registers across all rows it visits; at the end each CTA folds its
+// row groups into ONE partial row.  The partial buffer is therefore P x H,
+// independent of N, and a second small kernel sums it column-wise, casting to
+// the parameter dtype once at the store.
+
+#pragma once
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+#include "staged.cuh"
+
+namespace normk {
+
+
+// Register-row backward.  Persistent row groups walk rows row, row + stride,
+// ...; the next row's x, dy and saved statistics are loaded while the current
+// row computes.  Each thread owns fixed column vectors, so its dgamma/dbeta
+// accumulators stay in fp32 across all its rows: in registers (ACC_SMEM =
+// false), or, when one CTA covers a whole row (so every column has exactly one
+// owner thread), in shared memory, updated by plain read-modify-write, which
+// frees the registers for wide rows.  Elementwise math uses f32x2.
+template <int KIND, typename D, int VPT, int MAXT, int MINB, bool ACC_SMEM>
+__global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
+  using T = typename D::T;
+  constexpr int VEC = D::VEC;
+  constexpr int VP = VEC / 2;
+  constexpr bool LN = KIND == KIND_LN;
+  constexpr int NS = LN ? 3 : 1;  // values per row reduction
+  extern __shared__ __align__(16) float sh_dyn[];
+  const int tpr = a.tpr;
+  const int rpc = blockDim.x / tpr;
+  const int slot = threadIdx.x / tpr;
+  const int t = threadIdx.x - slot * tpr;
+  const int nw = tpr >> 5;
+  const int wig = t >> 5;
+  const int lane = threadIdx.x & 31;
+  const int H = a.H;
+  const int hv = H / VEC;
+  const float inv_h = 1.f / (float)H;
+  const bool w_f32 = a.w_f32 != 0;
+  float* sh = sh_dyn + slot * (2 * nw * NS);
+  const int bar_id = 1 + slot;
+  const int64_t stride = (int64_t)gridDim.x * rpc;
+  int nvec = 0;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
+
+  constexpr int VA = ACC_SMEM ? 1 : VPT;  // register accumulator vectors
+  float2 acc_g[VA][VP], acc_b[VA][VP];
+#pragma unroll
+  for (int v = 0; v < VA; ++v)
+#pragma unroll
+    for (int p = 0; p < VP; ++p) acc_g[v][p] = acc_b[v][p] = splat2(0.f);
+  constexpr bool FUSED = KIND == KIND_FUSED;
+  constexpr int VH = FUSED ? VPT : 1;  // stream-gradient vectors (fused only)
+  uint4 nx[VPT], nd[VPT];
+  float nrs = 0.f, nmu = 0.f;
+  auto fetch = [&](int64_t r) {
+    const T* xrow = reinterpret_cast<const T*>(a.x) + r * a.ldx;
+    const T* dyrow = reinterpret_cast<const T*>(a.dy) + r * a.lddy;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = (t + v * tpr) * VEC;
+      nx[v] = load_vec_or_zero<D>(xrow, c, H);
+      nd[v] = load_vec_or_zero<D>(dyrow, c, H);
+    }
+    nrs = a.rstd[r];
+    if (LN) nmu = a.mean[r];
+  };
+
+  int parity = 0;
+  int64_t row = (int64_t)blockIdx.x * rpc + slot;
+  if (row < a.N) fetch(row);  // first row in flight while gamma is staged
+
+  const int Hp = a.Hp;
+  // Shared memory: group scratch | fp32 gamma (thread-interleaved, shared by
+  // the row slots) | accumulators (ACC_SMEM, thread-interleaved: dgamma then
+  // dbeta) or the fold buffer of the row slots.
+  const int off_g = ((rpc * 2 * nw * NS) + 3) & ~3;
+  const int slots = VPT * VEC * tpr;  // floats of one thread-interleaved array
+  float4* gs = reinterpret_cast<float4*>(sh_dyn + off_g);
+  float* sh_acc = sh_dyn + off_g + slots;
+  float4* sacc_g = reinterpret_cast<float4*>(sh_acc);
+  float4* sacc_b = sacc_g + slots / 4;
+  if (slot == 0) stage_params<D, VPT>(gs, a.gamma, w_f32, 1.f, t, tpr, hv);
+  if constexpr (ACC_SMEM) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      float2 z[VP];
+#pragma unroll
+      for (int p = 0; p < VP; ++p) z[p] = splat2(0.f);
+      write_pairs<VEC>(sacc_g, v, t, tpr, z);
+      if (LN) write_pairs<VEC>(sacc_b, v, t, tpr, z);
+    }
+  }
+  __syncthreads();
+
+
+  for (; row < a.N; row += stride) {
+    const float r = nrs;
+    const float2 r2 = splat2(r);
+    float2 xh[VPT][VP];
+    uint4 dcur[VPT], hcur[VH];
+    {
+      // x_hat = x*rstd - mean*rstd: the rounding of mean*rstd shifts the whole
+      // row by one constant, which the recentring below removes.
+      const float2 b2 = splat2(LN ? -nmu * r : 0.f);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        float2 xv[VP];
+        unpack2<D>(nx[v], xv);
+#pragma unroll
+        for (int p = 0; p < VP; ++p) xh[v][p] = LN ? fma2(xv[p], r2, b2) : mul2(xv[p], r2);
+        dcur[v] = nd[v];
+      }
+    }
+    if (row + stride < a.N) fetch(row + stride);
+    if constexpr (FUSED) {
+      // The gradient through h is only added in pass 2: load it for this row
+      // now, in flight over the row reduction, rather than a row ahead.
+      if (a.dh_in) {
+        const T* hrow = reinterpret_cast<const T*>(a.dh_in) + row * a.lddh;
+#pragma unroll
+        for (int v = 0; v < VH; ++v) hcur[v] = load_vec_or_zero<D>(hrow, (t + v * tpr) * VEC, H);
+      }
+    }
+
+    // Pass 1: sum(g), sum(g*x_hat) and (LayerNorm) sum(x_hat), g = dy*gamma.
+    float2 sg = splat2(0.f), sgx = splat2(0.f), sx = splat2(0.f);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      if (v < nvec) {
+        float2 d[VP], gm[VP];
+        unpack2<D>(dcur[v], d);
+        read_pairs<VEC>(gs, v, t, tpr, gm);
+#pragma unroll
+        for (int p = 0; p < VP; ++p) {
+          const float2 g = mul2(d[p], gm[p]);
+          sgx = fma2(g, xh[v][p], sgx);
+          if (LN) {
+            sg = add2(sg, g);
+            sx = add2(sx, xh[v][p]);
+          }
+        }
+      }
+    }
+    float S[NS];
+    if (LN) {
+      S[0] = sg.x + sg.y;
+      S[1] = sgx.x + sgx.y;
+      S[NS - 1] = sx.x + sx.y;
+    } else {
+      S[0] = sgx.x + sgx.y;
+    }
+    group_sum<NS>(S, sh, nw, wig, lane, bar_id, parity);
+    // LayerNorm: mean(x_hat) is 0 exactly; its computed value s0 is the shift
+    // left by the saved mean's rounding, removed from x_hat here.
+    const float s0 = LN ? S[NS - 1] * inv_h : 0.f;
+    const float c1 = LN ? S[0] * inv_h : 0.f;
+    const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
+    const float2 s02 = splat2(s0), c12 = splat2(c1), nc22 = splat2(-c2);
+
+    // Pass 2: dx = rstd * (g - c1 - x_hat * c2) and the accumulators.
+    T* dxrow = reinterpret_cast<T*>(a.dx) + row * a.lddx;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      if (v < nvec) {
+        const int col = (t + v * tpr) * VEC;
+        float2 d[VP], gm[VP], out[VP];
+        unpack2<D>(dcur[v], d);
+        read_pairs<VEC>(gs, v, t, tpr, gm);
+        float2 ag[VP], ab[VP];
+        if constexpr (ACC_SMEM) {
+          read_pairs<VEC>(sacc_g, v, t, tpr, ag);
+          if (LN) read_pairs<VEC>(sacc_b, v, t, tpr, ab);
+        } else {
+#pragma unroll
+          for (int p = 0; p < VP; ++p) {
+            ag[p] = acc_g[ACC_SMEM ? 0 : v][p];
+            ab[p] = acc_b[ACC_SMEM ? 0 : v][p];
+          }
+        }
+#pragma unroll
+        for (int p = 0; p < VP; ++p) {
+          const float2 xc = LN ? sub2(xh[v][p], s02) : xh[v][p];
+          const float2 g = mul2(d[p], gm[p]);
+          out[p] = mul2(fma2(xc, nc22, LN ? sub2(g, c12) : g), r2);
+          ag[p] = fma2(d[p], xc, ag[p]);
+          if (LN) ab[p] = add2(ab[p], d[p]);
+        }
+        if constexpr (ACC_SMEM) {
+          write_pairs<VEC>(sacc_g, v, t, tpr, ag);
+          if (LN) write_pairs<VEC>(sacc_b, v, t, tpr, ab);
+        } else {
+#pragma unroll
+          for (int p = 0; p < VP; ++p) {
+            acc_g[ACC_SMEM ? 0 : v][p] = ag[p];
+            acc_b[ACC_SMEM ? 0 : v][p] = ab[p];
+          }
+        }
+        if constexpr (FUSED) {
+          // dL/dh = RMSNorm gradient + the gradient through h, for x and residual
+          if (a.dh_in) {
+            float2 e[VP];
+            unpack2<D>(hcur[v], e);
+#pragma unroll
+            for (int p = 0; p < VP; ++p) out[p] = add2(out[p], e[p]);
+          }
+          if (a.dx_twice) {
+#pragma unroll
+            for (int p = 0; p < VP; ++p) out[p] = add2(out[p], out[p]);
+          }
+        }
+        const uint4 packed = pack2<D>(out);
+        st_vec(dxrow + col, packed);
+        if constexpr (FUSED) {
+          if (a.dres) st_vec(reinterpret_cast<T*>(a.dres) + row * a.lddres + col, packed);
+        }
+      }
+    }
+    parity ^= 1;
+  }
+
+  if (a.ws == nullptr) return;
+  // Fold the CTA's row groups into partial row blockIdx.x.
+  float* pg = a.ws + (size_t)blockIdx.x * Hp;
+  float* pb = a.ws + ((size_t)gridDim.x + blockIdx.x) * Hp;
+  if constexpr (ACC_SMEM) {
+    // Each thread owns its accumulator slots: copy them straight out.
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      if (v < nvec) {
+        const int col = (t + v * tpr) * VEC;
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+          *reinterpret_cast<float4*>(pg + col + 4 * q) = sacc_g[(v * (VEC / 4) + q) * tpr + t];
+          if (LN) *reinterpret_cast<float4*>(pb + col + 4 * q) = sacc_b[(v * (VEC / 4) + q) * tpr + t];
+        }
+      }
+    }
+    return;
+  }
+  if (rpc == 1) {
+#pragma unroll
+    for (int v = 0; v < VA; ++v) {
+      if (v < nvec) {
+        const int col = (t + v * tpr) * VEC;
+#pragma unroll
+        for (int q = 0; q < VP / 2; ++q) {
+          *reinterpret_cast<float4*>(pg + col + 4 * q) =
+              make_float4(acc_g[v][2 * q].x, acc_g[v][2 * q].y, acc_g[v][2 * q + 1].x, acc_g[v][2 * q + 1].y);
+          if (LN)
+            *reinterpret_cast<float4*>(pb + col + 4 * q) =
+                make_float4(acc_b[v][2 * q].x, acc_b[v][2 * q].y, acc_b[v][2 * q + 1].x, acc_b[v][2 * q + 1].y);
+        }
+      }
+    }
+    return;
+  }
+  float* red_g = sh_acc;  // fold buffer: [Hp] dgamma then [Hp] dbeta
+  float* red_b = red_g + Hp;
+  for (int s2 = 0; s2 < rpc; ++s2) {
+    if (slot == s2) {
+#pragma unroll
+      for (int v = 0; v < VA; ++v) {
+        if (v < nvec) {
+          const int col = (t + v * tpr) * VEC;
+#pragma unroll
+          for (int p = 0; p < VP; ++p) {
+            float2* dg2 = reinterpret_cast<float2*>(red_g + col) + p;
+            float2* db2 = reinterpret_cast<float2*>(red_b + col) + p;
+            *dg2 = s2 == 0 ? acc_g[v][p] : add2(*dg2, acc_g[v][p]);
+            if (LN) *db2 = s2 == 0 ? acc_b[v][p] : add2(*db2, acc_b[v][p]);
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  for (int k = threadIdx.x * 4; k < H; k += blockDim.x * 4) {
+    *reinterpret_cast<float4*>(pg + k) = *reinterpret_cast<const float4*>(red_g + k);
+    if (LN) *reinterpret_cast<float4*>(pb + k) = *reinterpret_cast<const float4*>(red_b + k);
+  }
+}
+
+// Staged backward: the bulk-copy pipeline of staged.cuh with x and dy staged
+// per row.  Each consumer row group owns one row of every stage; each thread
+// owns VPT 16-byte column vectors (the same ones for every row), so its
+// dgamma/dbeta accumulators stay in registers for the whole row range.  The
+// saved mean/rstd of the group's next row are loaded one stage ahead.  At the
+// end the groups' accumulators are summed in shared memory (fixed order) into
+// this CTA's partial row, and the dependent reduction kernel is released.
+template <int KIND, typename D, int VPT>
+__global__ void __launch_bounds__(kStagedThreads, 1) bwd_staged_kernel(const BwdArgs a, const StageCfg c) {
+  using T = typename D::T;
+  constexpr int VEC = D::VEC;
+  constexpr bool LN = KIND == KIND_LN;
+  constexpr int NS = LN ? 3 : 1;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const StagedSmem m = staged_smem(smem, c);
+  staged_init(m, c);
+  int64_t lo, hi;
+  cta_rows(a.N, blockIdx.x, gridDim.x, lo, hi);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int H = a.H;
+  const int hv = H / VEC;
+  const int nwg = c.W / c.G;
+  const int g = warp / nwg;
+  const int wig = warp - g * nwg;
+  const int tpr = nwg * 32;
+  const int t = wig * 32 + lane;
+
+  float acc_g[VPT][VEC], acc_b[VPT][VEC];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) acc_g[v][i] = acc_b[v][i] = 0.f;
+
+  if (warp == c.W) {
+    if (lane == 0) {
+      const void* const src[2] = {a.x, a.dy};
+      const int64_t ld[2] = {a.ldx, a.lddy};
+      staged_produce<2>(m, c, src, ld, lo, hi, sizeof(T));
+    }
+    __syncwarp();  // reconverge before the CTA-wide barrier below
+  } else {
+    const float inv_h = 1.f / (float)H;
+    const bool w_f32 = a.w_f32 != 0;
+    float* sh = m.red + g * (2 * nwg * NS);
+    const int bar_id = 1 + g;
+    int parity = 0;
+    int k = 0;
+    float r_next = 0.f, mu_next = 0.f;
+    if (lo + g < hi) {
+      r_next = a.rstd[lo + g];
+      if (LN) mu_next = a.mean[lo + g];
+    }
+    for (int64_t row0 = lo; row0 < hi; row0 += c.G, ++k) {
+      const int s = k % c.S;
+      const int64_t row = row0 + g;
+      const float r = r_next, mu = mu_next;
+      if (row + c.G < hi) {  // statistics of this group's next row, one stage ahead
+        r_next = a.rstd[row + c.G];
+        if (LN) mu_next = a.mean[row + c.G];
+      }
+      const bool have = mbar_wait(&m.full[s], (k / c.S) & 1, c.err, m.abort);
+      if (row < hi) {
+        const T* xs = staged_row<T>(m, c, 2, s, 0, g);
+        const T* ds = staged_row<T>(m, c, 2, s, 1, g);
+        float S[NS];
+#pragma unroll
+        for (int q = 0; q < NS; ++q) S[q] = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int j = t + v * tpr;
+          if (j < hv) {
+            float xv[VEC], dv[VEC], gm[VEC];
+            unpack<D>(lds16(xs + j * VEC), xv);
+            unpack<D>(lds16(ds + j * VEC), dv);
+            load_param_vec<D>(a.gamma, j * VEC, w_f32, 1.f, gm);
+            // per-vector tree sums: short dependency chains
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) {
+              const float xh = LN ? (xv[i] - mu) * r : xv[i] * r;
+              const float gg = __fmul_rn(dv[i], gm[i]);
+              gm[i] = gg * xh;
+              dv[i] = gg;
+              xv[i] = xh;
+            }
+            if (LN) {
+              S[0] += tree_sum<VEC>(dv);
+              S[1] += tree_sum<VEC>(gm);
+              S[2] += tree_sum<VEC>(xv);
+            } else {
+              S[0] += tree_sum<VEC>(gm);
+            }
+          }
+        }
+        group_sum<NS>(S, sh, nwg, wig, lane, bar_id, parity);
+        const float s0 = LN ? S[2] * inv_h : 0.f;  // row mean of x_hat: removes the mean's rounding shift
+        const float c1 = LN ? S[0] * inv_h : 0.f;
+        const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
+        T* dxrow = reinterpret_cast<T*>(a.dx) + row * a.lddx;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int j = t + v * tpr;
+          if (j < hv) {
+            float xv[VEC], dv[VEC], gm[VEC], out[VEC];
+            unpack<D>(lds16(xs + j * VEC), xv);
+            unpack<D>(lds16(ds + j * VEC), dv);
+            load_param_vec<D>(a.gamma, j * VEC, w_f32, 1.f, gm);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) {
+              const float xc = LN ? (xv[i] - mu) * r - s0 : xv[i] * r;
+              const float gg = __fmul_rn(dv[i], gm[i]);
+              out[i] = r * (gg - c1 - xc * c2);
+              acc_g[v][i] = fmaf(dv[i], xc, acc_g[v][i]);
+              if (LN) acc_b[v][i] += dv[i];
+            }
+            if (have) store_vec<D>(dxrow, j * VEC, out);
+          }
+        }
+      }
+      parity ^= 1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m.empty[s]);
+    }
+  }
+  pdl_launch_dependents();
+  // Every copy has landed (consumers waited on all of them; the producer
+  // drained), so the ring is free: fold the groups into one partial row.
+  __syncthreads();
+  if (a.ws == nullptr) return;
+  const int Hp = a.Hp;
+  float* pg = a.ws + (size_t)blockIdx.x * Hp;
+  float* pb = a.ws + ((size_t)gridDim.x + blockIdx.x) * Hp;
+  const bool consumer = warp < c.W;
+  if (c.G == 1) {
+    if (consumer) {
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int j = t + v * tpr;
+        if (j < hv) {
+#pragma unroll
+          for (int q = 0; q < VEC / 4; ++q) {
+            *reinterpret_cast<float4*>(pg + j * VEC + 4 * q) = make_float4(
+                acc_g[v][4 * q], acc_g[v][4 * q + 1], acc_g[v][4 * q + 2], acc_g[v][4 * q + 3]);
+            if (LN)
+              *reinterpret_cast<float4*>(pb + j * VEC + 4 * q) = make_float4(
+                  acc_b[v][4 * q], acc_b[v][4 * q + 1], acc_b[v][4 * q + 2], acc_b[v][4 * q + 3]);
+          }
+        }
+      }
+    }
+    return;
+  }
+  float* red_g = reinterpret_cast<float*>(m.data);
+  float* red_b = red_g + Hp;
+  for (int g2 = 0; g2 < c.G; ++g2) {
+    if (consumer && g == g2) {
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int j = t + v * tpr;
+        if (j < hv) {
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) {
+            const int col = j * VEC + i;
+            red_g[col] = g2 == 0 ? acc_g[v][i] : red_g[col] + acc_g[v][i];
+            if (LN) red_b[col] = g2 == 0 ? acc_b[v][i] : red_b[col] + acc_b[v][i];
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  for (int col = threadIdx.x * 4; col < H; col += blockDim.x * 4) {
+    *reinterpret_cast<float4*>(pg + col) = *reinterpret_cast<const float4*>(red_g + col);
+    if (LN) *reinterpret_cast<float4*>(pb + col) = *reinterpret_cast<const float4*>(red_b + col);
+  }
+}
+
+constexpr int LOOP_THREADS = 256;
+
+// Any H, any alignment: one row per CTA iteration, two passes over the row.
+// The CTA's partial row lives in the workspace; column j is always handled by
+// thread j % LOOP_THREADS, so its read-modify-writes never race.
+template <int KIND, typename D>
+__global__ void __launch_bounds__(LOOP_THREADS) bwd_loop_kernel(const BwdArgs a) {
+  using T = typename D::T;
+  constexpr bool LN = KIND == KIND_LN;
+  constexpr int NS = LN ? 3 : 1;
+  constexpr int NW = LOOP_THREADS / 32;
+  __shared__ float sh[2 * NW * NS];
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  const int wig = t >> 5;
+  const int H = a.H;
+  const float inv_h = 1.f / (float)H;
+  const bool w_f32 = a.w_f32 != 0;
+  float* pg = a.ws ? a.ws + (size_t)blockIdx.x * a.Hp : nullptr;
+  float* pb = a.ws ? a.ws + ((size_t)gridDim.x + blockIdx.x) * a.Hp : nullptr;
+  if (pg) {
+    for (int j = t; j < a.Hp; j += LOOP_THREADS) {
+      pg[j] = 0.f;
+      if (LN) pb[j] = 0.f;
+    }
+  }
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < a.N; row += gridDim.x) {
+    const T* xrow = reinterpret_cast<const T*>(a.x) + row * a.ldx;
+    const T* dyrow = reinterpret_cast<const T*>(a.dy) + row * a.lddy;
+    const float r = a.rstd[row];
+    const float mu = LN ? a.mean[row] : 0.f;
+    float S[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) S[k] = 0.f;
+    for (int j = t; j < H; j += LOOP_THREADS) {
+      const float xv = load_elem<D>(xrow, j);
+      const float xh = LN ? (xv - mu) * r : xv * r;
+      const float g = __fmul_rn(load_elem<D>(dyrow, j), a.gamma ? load_param<D>(a.gamma, j, w_f32) : 1.f);
+      if (LN) {
+        S[0] += g;
+        S[1] = fmaf(g, xh, S[1]);
+        S[2] += xh;
+      } else {
+        S[0] = fmaf(g, xh, S[0]);
+      }
+    }
+    group_sum<NS>(S, sh, NW, wig, lane, 1, parity);
+    const float s0 = LN ? S[2] * inv_h : 0.f;
+    const float c1 = LN ? S[0] * inv_h : 0.f;
+    const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
+    T* dxrow = reinterpret_cast<T*>(a.dx) + row * a.lddx;
+    for (int j = t; j < H; j += LOOP_THREADS) {
+      const float xv = load_elem<D>(xrow, j);
+      const float dyv = load_elem<D>(dyrow, j);
+      const float xc = LN ? (xv - mu) * r - s0 : xv * r;
+      const float g = __fmul_rn(dyv, a.gamma ? load_param<D>(a.gamma, j, w_f32) : 1.f);
+      float dxv = r * (g - c1 - xc * c2);
+      if constexpr (KIND == KIND_FUSED) {
+        if (a.dh_in) dxv += load_elem<D>(reinterpret_cast<const T*>(a.dh_in) + row * a.lddh, j);
+        if (a.dx_twice) dxv += dxv;
+        if (a.dres) store_elem<D>(reinterpret_cast<T*>(a.dres) + row * a.lddres, j, dxv);
+      }
+      store_elem<D>(dxrow, j, dxv);
+      if (pg) {
+        pg[j] = fmaf(dyv, xc, pg[j]);
+        if (LN) pb[j] += dyv;
+      }
+    }
+    parity ^= 1;
+  }
+}
+
+// dgamma[j] = sum_p partial[0][p][j], dbeta[j] = sum_p partial[1][p][j]: 8
+// column vectors (32 columns) x 32 row groups per CTA, blockIdx.y picks the
+// parameter.  Each thread issues the loads of all its (up to kReduceRows)
+// partial rows before adding, so the kernel costs about one L2 round trip.
+// Fixed summation order, one rounding to the output dtype.
+constexpr int kReduceRows = 16;
+
+template <typename D>
+__global__ void __launch_bounds__(256) bwd_param_reduce_kernel(const float* ws, int P, int Hp, int H,
+                                                               void* dg, void* db, int w_f32) {
+  pdl_wait_primary();  // launched as a programmatic dependent of the main kernel
+  const int which = blockIdx.y;
+  void* out = which ? db : dg;
+  if (out == nullptr) return;
+  const float* src = ws + (size_t)which * P * Hp;
+  const int cl = threadIdx.x & 7;
+  const int rg = threadIdx.x >> 3;
+  const int col = (blockIdx.x * 8 + cl) * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (col < Hp) {
+    for (int p0 = rg; p0 < P; p0 += 32 * kReduceRows) {
+      float4 v[kReduceRows];
+#pragma unroll
+      for (int k = 0; k < kReduceRows; ++k) {
+        const int p = p0 + 32 * k;
+        v[k] = p < P ? *reinterpret_cast<const float4*>(src + (size_t)p * Hp + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < kReduceRows; ++k) {
+        acc.x += v[k].x;
+        acc.y += v[k].y;
+        acc.z += v[k].z;
+        acc.w += v[k].w;
+      }
+    }
+  }
+  __shared__ float4 sm[32][8];
+  sm[rg][cl] = acc;
+  __syncthreads();
+  if (rg == 0 && col < H) {
+    float4 s = sm[0][cl];
+    for (int k = 1; k < 32; ++k) {
+      const float4 v = sm[k][cl];
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    }
+    const float vals[4] = {s.x, s.y, s.z, s.w};
+    for (int i = 0; i < 4 && col + i < H; ++i) {
+      if (w_f32) {
+        reinterpret_cast<float*>(out)[col + i] = vals[i];
+      } else {
+        store_elem<D>(out, col + i, vals[i]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side configuration.
+// ---------------------------------------------------------------------------
+
+static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <int KIND, typename D, int VPT, int MAXT, int MINB, bool ACC_SMEM = false>
+static cudaError_t run_rows(const BwdArgs& a, int threads, int* P, int p_cap, size_t smem, const DeviceInfo& dev,
+                            cudaStream_t s) {
+  auto kern = bwd_rows_kernel<KIND, D, VPT, MAXT, MINB, ACC_SMEM>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  *P = std::max(1, std::min(p_cap, per_sm * dev.sm_count));
+  kern<<<*P, threads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+constexpr int kStagedMaxCols = 32;  // columns per consumer thread (register accumulators)
+
+template <int KIND, typename D, int VPT>
+static cudaError_t run_staged(const BwdArgs& a, const StageCfg& c, int P, size_t smem, cudaStream_t s) {
+  auto kern = bwd_staged_kernel<KIND, D, VPT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<P, kStagedThreads, smem, s>>>(a, c);
+  return cudaGetLastError();
+}
+
+template <int KIND, typename D>
+cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& dev,
+                                    cudaStream_t s) {
+  using T = typename D::T;
+  constexpr int VEC = D::VEC;
+  constexpr int VPT_MAX = 16 / VEC;  // 16 elements per thread
+  constexpr int NS = KIND == KIND_LN ? 3 : 1;
+  const size_t es = sizeof(T);
+  const size_t wes = a.w_f32 ? 4 : es;
+  const bool want = dg != nullptr || db != nullptr;
+  if (a.N == 0) {
+    if (dg && cudaMemsetAsync(dg, 0, (size_t)a.H * wes, s) != cudaSuccess) return cudaGetLastError();
+    if (db && cudaMemsetAsync(db, 0, (size_t)a.H * wes, s) != cudaSuccess) return cudaGetLastError();
+    return cudaSuccess;
+  }
+  if (!want) a.ws = nullptr;
+  a.Hp = bwd_partial_stride(a.H);
+  const int p_max = bwd_max_partials(dev);
+  bool aligned = aligned16(a.x) && aligned16(a.dy) && aligned16(a.dx) && (a.ldx * es) % 16 == 0 &&
+                 (a.lddy * es) % 16 == 0 && (a.lddx * es) % 16 == 0;
+  if (a.dh_in) aligned = aligned && aligned16(a.dh_in) && (a.lddh * es) % 16 == 0;
+  if (a.dres) aligned = aligned && aligned16(a.dres) && (a.lddres * es) % 16 == 0;
+  if (a.gamma) aligned = aligned && aligned16(a.gamma);
+  int P = 0;
+  cudaError_t err = cudaSuccess;
+  bool done = false;
+  // Register-row shape: narrow rows one warp each, wider rows 16 elements a
+  // thread with more warps (H <= 16384).
+  const bool vec_ok = aligned && a.H % VEC == 0;
+  const int Hv = a.H / VEC;
+  int vpt = VPT_MAX, tpr = 0;
+  if (Hv <= 32 * VPT_MAX) {
+    tpr = 32;
+    vpt = 1;
+    while (vpt * 32 < Hv) vpt *= 2;
+  } else {
+    tpr = ((Hv + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32;
+  }
+  const int rpc_rows = tpr <= 256 ? 256 / tpr : 1;
+  // group scratch | fp32 gamma | shared accumulators (one row slot) or the
+  // fold buffer of several row slots
+  const size_t rows_slots = (size_t)vpt * VEC * tpr;
+  size_t rows_smem_f = (size_t)((rpc_rows * 2 * (tpr / 32) * NS + 3) & ~3) + rows_slots;
+  if (rpc_rows == 1) rows_smem_f += (KIND == KIND_LN ? 2 : 1) * rows_slots;
+  else if (want) rows_smem_f += 2 * (size_t)a.Hp;
+  const size_t rows_smem = rows_smem_f * sizeof(float);
+  const bool rows_ok = vec_ok && tpr <= 1024 && rows_smem <= (size_t)dev.max_smem_optin;
+  // Staged shape.  17 warps leave at most 96 registers a thread (a
+  // sub-partition holds 5 warps).  LayerNorm keeps two accumulators per
+  // column, so it first tries shapes with at most 24 columns per thread.
+  StageCfg c{};
+  const bool staged_ok =
+      KIND != KIND_FUSED && vec_ok &&
+      ((KIND == KIND_LN && staged_config(a.H, (int)es, 2, dev.max_smem_optin, 24, &c)) ||
+       staged_config(a.H, (int)es, 2, dev.max_smem_optin, kStagedMaxCols, &c));
+  bool use_rows = false, use_staged = false;
+  switch (dev.path) {
+    case PATH_AUTO:
+      use_rows = rows_ok && tpr <= kRowsAutoMaxThreads;
+      use_staged = !use_rows && staged_ok;
+      use_rows = use_rows || (!use_staged && rows_ok);
+      break;
+    case PATH_ROWS: use_rows = rows_ok; break;
+    case PATH_STAGED:
+      use_staged = staged_ok;
+      use_rows = !use_staged && rows_ok;
+      break;
+    default: break;
+  }
+  if constexpr (KIND != KIND_FUSED) {
+   if (use_staged) {
+    c.err = dev.err;
+    c.contiguous = a.ldx == a.H && a.lddy == a.H;
+    const int stpr = 32 * (c.W / c.G);
+    const int svpt = (Hv + stpr - 1) / stpr;
+    P = (int)std::min<int64_t>((int64_t)dev.sm_count, (a.N + c.G - 1) / c.G);
+    const size_t smem = staged_smem_bytes(c, 2);
+    if (svpt <= 1) err = run_staged<KIND, D, 1>(a, c, P, smem, s);
+    else if (svpt <= 2) err = run_staged<KIND, D, 2>(a, c, P, smem, s);
+    else if (svpt <= 3) err = run_staged<KIND, D, 3>(a, c, P, smem, s);
+    else if (svpt <= 4) err = run_staged<KIND, D, 4>(a, c, P, smem, s);
+    else if constexpr (VEC == 4) {
+      if (svpt <= 6) err = run_staged<KIND, D, 6>(a, c, P, smem, s);
+      else err = run_staged<KIND, D, 8>(a, c, P, smem, s);
+    }
+    done = true;
+   }
+  }
+  // Register rows; the grid is persistent: as many CTAs as fit, at most
+  // 2 x SM count (the partial rows the workspace holds).
+  if (!done && use_rows) {
+    a.tpr = tpr;
+    const int rpc = rpc_rows;
+    const int threads = rpc * tpr;
+    const int p_cap = (int)std::min<int64_t>((a.N + rpc - 1) / rpc, p_max);
+    const size_t smem = rows_smem;
+    if (threads <= 256) {
+      switch (vpt) {
+        case 1: err = run_rows<KIND, D, 1, 256, 2>(a, threads, &P, p_cap, smem, dev, s); break;
+        case 2: err = run_rows<KIND, D, 2, 256, 2>(a, threads, &P, p_cap, smem, dev, s); break;
+        default:
+          if constexpr (VPT_MAX >= 4) err = run_rows<KIND, D, 4, 256, 2>(a, threads, &P, p_cap, smem, dev, s);
+          break;
+      }
+    } else if (threads <= 640) {
+      err = run_rows<KIND, D, VPT_MAX, 640, 1, true>(a, threads, &P, p_cap, smem, dev, s);
+    } else {
+      err = run_rows<KIND, D, VPT_MAX, 1024, 1, true>(a, threads, &P, p_cap, smem, dev, s);
+    }
+    done = true;
+  }
+  if (!done) {
+    P = (int)std::min<int64_t>(a.N, p_max);
+    bwd_loop_kernel<KIND, D><<<P, LOOP_THREADS, 0, s>>>(a);
+    err = cudaGetLastError();
+  }
+  if (err != cudaSuccess || !want) return err;
+  // The column reduction is a programmatic dependent of the main kernel: it
+  // is scheduled while the main kernel drains and waits for it on the device.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.Hp + 31) / 32, KIND == KIND_LN ? 2 : 1);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float* ws = a.ws;
+  void* dbeta = KIND == KIND_LN ? db : nullptr;
+  err = cudaLaunchKernelEx(&cfg, bwd_param_reduce_kernel<D>, ws, P, a.Hp, a.H, dg, dbeta, a.w_f32);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+}  // namespace normk

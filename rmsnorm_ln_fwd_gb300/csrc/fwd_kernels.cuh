@@ -1,0 +1,612 @@
+// Forward kernel templates and their launch logic, instantiated per row
+// dtype by norm_fwd_f32.cu, norm_fwd_bf16.cu and norm_fwd_f16.cu.
+//
+// Forward kernels: LayerNorm, RMSNorm and fused residual-add + RMSNorm.
+//
+// Three kernel families, tried in this order:
+//
+// * fwd_staged_kernel -- persistent, one CTA per SM; a producer warp streams
+//   rows through a shared-memory ring with bulk copies (see staged.cuh) and
+//   consumer row groups compute from shared memory.  Needs 16-byte aligned
+//   rows, H a multiple of the vector width and at least three stages of rows
+//   in shared memory.
+// * fwd_rows_kernel -- the row lives in registers.  A "row group" of `tpr`
+//   threads (one warp for narrow rows, up to 1024 threads for wide rows) owns
+//   one row at a time and prefetches its next; each thread holds VPT 16-byte
+//   vectors of it, so HBM is read exactly once and written exactly once.  Vector v of thread t covers
+//   columns [(v*tpr + t)*VEC, +VEC): consecutive threads touch consecutive
+//   16-byte chunks, so every warp-wide access is fully coalesced.  Needs
+//   16-byte aligned rows and H a multiple of the vector width.
+// * fwd_loop_kernel -- any H and any alignment: one CTA per row, a strided
+//   loop over the row, a statistics pass and an output pass (the second read
+//   mostly hits L2).  Per-thread statistics use Welford's recurrence.  The
+//   fused kernel stores h in the output pass, after re-forming the fp32 sum.
+//
+// Statistics ("Skill: Write CUDA LayerNorm Kernel", Required reasoning process
+// steps 2-5; "Skill: Write a Triton LayerNorm Kernel" steps 3-7):
+// LayerNorm: the register-row kernel holds the whole row, so it takes the
+// plain two-pass -- the row sum gives the mean, then the sum of squared
+// deviations from it gives M2 -- each a shuffle + shared-memory reduction.
+// The kernels that stream the row keep a Welford triple (count, mean, M2) per
+// thread and merge triples across lanes and warps with the parallel merge.
+// M2 is divided by the full row length H.  Values are shifted by the row's
+// first element before accumulating (x - x0 is exact when the two are close),
+// so rows with a large common offset keep full precision.
+// RMSNorm sums x^2.  rstd = rsqrt(var + eps): eps inside the square root.
+//
+// Fused add ("Skill: Write a Triton Fused Add+RMSNorm Kernel", steps 2-7):
+// h = x + residual in fp32, h stored (rounded to the row dtype) before the
+// reduction, y computed from the fp32 h.  Each element of h is written by the
+// thread that read that element of x and residual, so h_out may alias either.
+
+#pragma once
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+#include "staged.cuh"
+
+namespace normk {
+
+// Register-row kernel.  Persistent row groups of `tpr` threads walk rows
+// row, row + stride, ...; while a group computes one row, the 16-byte loads
+// of its next row are already in flight (software pipelining), so each warp
+// keeps two rows' worth of HBM reads outstanding.  Each row is unpacked once
+// into fp32 pairs and every elementwise step uses packed f32x2 instructions.
+template <int KIND, typename D, int VPT, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
+  using T = typename D::T;
+  constexpr int VEC = D::VEC;
+  constexpr int VP = VEC / 2;
+  extern __shared__ __align__(16) float sh_dyn[];
+  const int tpr = a.tpr;
+  const int rpc = blockDim.x / tpr;
+  const int slot = threadIdx.x / tpr;
+  const int t = threadIdx.x - slot * tpr;
+  const int nw = tpr >> 5;
+  const int wig = t >> 5;
+  const int lane = threadIdx.x & 31;
+  const int H = a.H;
+  const int hv = H / VEC;
+  const float inv_h = 1.f / (float)H;
+  const bool w_f32 = a.w_f32 != 0;
+  float* sh = sh_dyn + slot * (2 * nw * 3);
+  const int bar_id = 1 + slot;
+  const int64_t stride = (int64_t)gridDim.x * rpc;
+  int nvec = 0;  // vectors of each row this thread owns
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
+  uint4 nx[VPT], nr[VPT];
+  float npivot = 0.f;
+  auto fetch = [&](int64_t r) {
+    const T* xrow = reinterpret_cast<const T*>(a.x) + r * a.ldx;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) nx[v] = load_vec_or_zero<D>(xrow, (t + v * tpr) * VEC, H);
+    if constexpr (KIND == KIND_FUSED) {
+      const T* rrow = reinterpret_cast<const T*>(a.res) + r * a.ldr;
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) nr[v] = load_vec_or_zero<D>(rrow, (t + v * tpr) * VEC, H);
+    }
+    if constexpr (KIND == KIND_LN) npivot = load_elem<D>(xrow, 0);
+  };
+
+  int parity = 0;
+  int64_t row = (int64_t)blockIdx.x * rpc + slot;
+  if (row < a.N) fetch(row);  // first row in flight while the parameters are staged
+
+  // gamma (and beta) as fp32, thread-interleaved, shared by the row slots.
+  float4* gs = reinterpret_cast<float4*>(sh_dyn + ((rpc * 2 * nw * 3 + 3) & ~3));
+  float4* bs = gs + VPT * (VEC / 4) * tpr;
+  if (slot == 0) {
+    stage_params<D, VPT>(gs, a.gamma, w_f32, 1.f, t, tpr, hv);
+    if constexpr (KIND == KIND_LN) stage_params<D, VPT>(bs, a.beta, w_f32, 0.f, t, tpr, hv);
+  }
+  __syncthreads();
+
+  for (; row < a.N; row += stride) {
+    // Unpack the current row (it arrived while the previous row computed).
+    float2 f[VPT][VP];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) unpack2<D>(nx[v], f[v]);
+    const float pivot = npivot;
+    if constexpr (KIND == KIND_FUSED) {
+      T* hrow = reinterpret_cast<T*>(a.h) + row * a.ldh;
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        float2 r[VP];
+        unpack2<D>(nr[v], r);
+#pragma unroll
+        for (int p = 0; p < VP; ++p) f[v][p] = add2(f[v][p], r[p]);
+        if (v < nvec) st_vec(reinterpret_cast<T*>(hrow) + (t + v * tpr) * VEC, pack2<D>(f[v]));
+      }
+    }
+    // Issue the next row's loads before computing this one.
+    if (row + stride < a.N) fetch(row + stride);
+
+    float rstd, mean_d = 0.f;
+    if constexpr (KIND == KIND_LN) {
+      // The two-pass of the row, held in registers: the shifted sum gives the
+      // mean, then the squared deviations from it give M2 (no per-part counts
+      // or means to merge; both sums are plain group reductions).
+      const float2 pv = splat2(pivot);
+      float2 s2 = splat2(0.f);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        if (v < nvec) {
+#pragma unroll
+          for (int p = 0; p < VP; ++p) f[v][p] = sub2(f[v][p], pv);
+          float2 vs = f[v][0];
+#pragma unroll
+          for (int p = 1; p < VP; ++p) vs = add2(vs, f[v][p]);
+          s2 = add2(s2, vs);
+        }
+      }
+      float sm[1] = {s2.x + s2.y};
+      group_sum<1>(sm, sh, nw, wig, lane, bar_id, parity);
+      mean_d = sm[0] * inv_h;
+      const float2 ml = splat2(mean_d);
+      float2 q2 = splat2(0.f);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        if (v < nvec) {
+          float2 e = sub2(f[v][0], ml);
+          float2 vq = mul2(e, e);
+#pragma unroll
+          for (int p = 1; p < VP; ++p) {
+            e = sub2(f[v][p], ml);
+            vq = fma2(e, e, vq);
+          }
+          q2 = add2(q2, vq);
+        }
+      }
+      float m2[1] = {q2.x + q2.y};
+      group_sum<1>(m2, sh + 2 * nw, nw, wig, lane, bar_id, parity);
+      rstd = rsqrtf(m2[0] * inv_h + a.eps);
+    } else {
+      float2 s2 = splat2(0.f);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        if (v < nvec) {
+          float2 vq = mul2(f[v][0], f[v][0]);
+#pragma unroll
+          for (int p = 1; p < VP; ++p) vq = fma2(f[v][p], f[v][p], vq);
+          s2 = add2(s2, vq);
+        }
+      }
+      float ss[1] = {s2.x + s2.y};
+      group_sum<1>(ss, sh, nw, wig, lane, bar_id, parity);
+      rstd = rsqrtf(ss[0] * inv_h + a.eps);
+    }
+    if (t == 0) {
+      if constexpr (KIND == KIND_LN) {
+        if (a.mean) a.mean[row] = pivot + mean_d;
+      }
+      if (a.rstd) a.rstd[row] = rstd;
+    }
+
+    T* yrow = reinterpret_cast<T*>(a.y) + row * a.ldy;
+    const float2 r2 = splat2(rstd);
+    const float2 b2 = splat2(-mean_d * rstd);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      if (v < nvec) {
+        const int col = (t + v * tpr) * VEC;
+        float2 gm[VP], out[VP];
+        read_pairs<VEC>(gs, v, t, tpr, gm);
+        if constexpr (KIND == KIND_LN) {
+          float2 be[VP];
+          read_pairs<VEC>(bs, v, t, tpr, be);
+#pragma unroll
+          for (int p = 0; p < VP; ++p) out[p] = fma2(fma2(f[v][p], r2, b2), gm[p], be[p]);
+        } else {
+#pragma unroll
+          for (int p = 0; p < VP; ++p) out[p] = mul2(mul2(f[v][p], r2), gm[p]);
+        }
+        st_vec(yrow + col, pack2<D>(out));
+      }
+    }
+    parity ^= 1;
+  }
+}
+
+
+// Consumers copy their VPT vectors of the row from shared memory into packed
+// registers, release the stage at once (the producer can refill it while they
+// compute), unpack it once into fp32 pairs and run every pass from registers
+// with f32x2 math; gamma/beta are read from fp32 copies staged once per CTA in
+// shared memory (thread-interleaved, conflict-free).
+template <int KIND, typename D, int VPT>
+__global__ void __launch_bounds__(kStagedThreads, 1) fwd_staged_kernel(const FwdArgs a, const StageCfg c) {
+  using T = typename D::T;
+  constexpr int VEC = D::VEC;
+  constexpr int VP = VEC / 2;
+  constexpr int NT = KIND == KIND_FUSED ? 2 : 1;  // staged tensors: x (and residual)
+  extern __shared__ __align__(128) unsigned char smem[];
+  const StagedSmem m = staged_smem(smem, c);
+  staged_init(m, c);
+  int64_t lo, hi;
+  cta_rows(a.N, blockIdx.x, gridDim.x, lo, hi);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == c.W) {
+    if (lane == 0) {
+      if constexpr (NT == 2) {
+        const void* const src[2] = {a.x, a.res};
+        const int64_t ld[2] = {a.ldx, a.ldr};
+        staged_produce<2>(m, c, src, ld, lo, hi, sizeof(T));
+      } else {
+        const void* const src[1] = {a.x};
+        const int64_t ld[1] = {a.ldx};
+        staged_produce<1>(m, c, src, ld, lo, hi, sizeof(T));
+      }
+    }
+    return;
+  }
+
+  const int H = a.H;
+  const int hv = H / VEC;
+  const float inv_h = 1.f / (float)H;
+  const bool w_f32 = a.w_f32 != 0;
+  const int nwg = c.W / c.G;  // warps per row group
+  const int g = warp / nwg;
+  const int wig = warp - g * nwg;
+  const int tpr = nwg * 32;
+  const int t = wig * 32 + lane;
+  float* sh = m.red + g * (2 * nwg * 3);
+  const int bar_id = 1 + g;
+  int nvec = 0;  // vectors of each row this thread owns
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
+  // fp32 gamma (and beta), staged by row group 0 while the first copies fly.
+  float4* gs = m.par;
+  float4* bs = gs + VPT * (VEC / 4) * tpr;
+  if (g == 0) {
+    stage_params<D, VPT>(gs, a.gamma, w_f32, 1.f, t, tpr, hv);
+    if constexpr (KIND == KIND_LN) stage_params<D, VPT>(bs, a.beta, w_f32, 0.f, t, tpr, hv);
+  }
+  named_barrier(15, c.W * 32);  // consumers only (group barriers use ids 1..G, G <= 8 when used)
+
+  int parity = 0;
+  int k = 0;
+  for (int64_t row0 = lo; row0 < hi; row0 += c.G, ++k) {
+    const int s = k % c.S;
+    const bool have = mbar_wait(&m.full[s], (k / c.S) & 1, c.err, m.abort);
+    const int64_t row = row0 + g;
+    const bool mine = row < hi;  // uniform across the row group
+    uint4 xr[VPT], rr[VPT];
+    float pivot = 0.f;
+    if (mine) {
+      const T* xs = staged_row<T>(m, c, NT, s, 0, g);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int j = t + v * tpr;
+        xr[v] = j < hv ? lds16(xs + j * VEC) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      if constexpr (NT == 2) {
+        const T* rs = staged_row<T>(m, c, NT, s, 1, g);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int j = t + v * tpr;
+          rr[v] = j < hv ? lds16(rs + j * VEC) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      if constexpr (KIND == KIND_LN) pivot = load_elem<D>(xs, 0);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&m.empty[s]);  // the row is in registers: the stage may be refilled
+    const int par = parity;
+    parity ^= 1;
+    if (!mine) continue;
+
+    float2 f[VPT][VP];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) unpack2<D>(xr[v], f[v]);
+    if constexpr (KIND == KIND_FUSED) {
+      T* hrow = reinterpret_cast<T*>(a.h) + row * a.ldh;
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        float2 r[VP];
+        unpack2<D>(rr[v], r);
+#pragma unroll
+        for (int p = 0; p < VP; ++p) f[v][p] = add2(f[v][p], r[p]);
+        if (v < nvec && have) st_vec(hrow + (t + v * tpr) * VEC, pack2<D>(f[v]));
+      }
+    }
+    float rstd, mean_d = 0.f;
+    if constexpr (KIND == KIND_LN) {
+      const float2 pv = splat2(pivot);
+      float2 s2 = splat2(0.f);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        if (v < nvec) {
+#pragma unroll
+          for (int p = 0; p < VP; ++p) f[v][p] = sub2(f[v][p], pv);
+          float2 vs = f[v][0];
+#pragma unroll
+          for (int p = 1; p < VP; ++p) vs = add2(vs, f[v][p]);
+          s2 = add2(s2, vs);
+        }
+      }
+      const float cnt = (float)(nvec * VEC);
+      const float mloc = nvec > 0 ? __fdividef(s2.x + s2.y, cnt) : 0.f;
+      const float2 ml = splat2(mloc);
+      float2 q2 = splat2(0.f);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        if (v < nvec) {
+          float2 e = sub2(f[v][0], ml);
+          float2 vq = mul2(e, e);
+#pragma unroll
+          for (int p = 1; p < VP; ++p) {
+            e = sub2(f[v][p], ml);
+            vq = fma2(e, e, vq);
+          }
+          q2 = add2(q2, vq);
+        }
+      }
+      const Welford w = group_welford(Welford{cnt, mloc, q2.x + q2.y}, sh, nwg, wig, lane, bar_id, par);
+      mean_d = w.m;
+      rstd = rsqrtf(w.m2 * inv_h + a.eps);
+    } else {
+      float2 s2 = splat2(0.f);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        if (v < nvec) {
+          float2 vq = mul2(f[v][0], f[v][0]);
+#pragma unroll
+          for (int p = 1; p < VP; ++p) vq = fma2(f[v][p], f[v][p], vq);
+          s2 = add2(s2, vq);
+        }
+      }
+      float ss[1] = {s2.x + s2.y};
+      group_sum<1>(ss, sh, nwg, wig, lane, bar_id, par);
+      rstd = rsqrtf(ss[0] * inv_h + a.eps);
+    }
+    if (t == 0 && have) {
+      if constexpr (KIND == KIND_LN) {
+        if (a.mean) a.mean[row] = pivot + mean_d;
+      }
+      if (a.rstd) a.rstd[row] = rstd;
+    }
+    T* yrow = reinterpret_cast<T*>(a.y) + row * a.ldy;
+    const float2 r2 = splat2(rstd);
+    const float2 b2 = splat2(-mean_d * rstd);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      if (v < nvec) {
+        const int col = (t + v * tpr) * VEC;
+        float2 gm[VP], out[VP];
+        read_pairs<VEC>(gs, v, t, tpr, gm);
+        if constexpr (KIND == KIND_LN) {
+          float2 be[VP];
+          read_pairs<VEC>(bs, v, t, tpr, be);
+#pragma unroll
+          for (int p = 0; p < VP; ++p) out[p] = fma2(fma2(f[v][p], r2, b2), gm[p], be[p]);
+        } else {
+#pragma unroll
+          for (int p = 0; p < VP; ++p) out[p] = mul2(mul2(f[v][p], r2), gm[p]);
+        }
+        if (have) st_vec(yrow + col, pack2<D>(out));
+      }
+    }
+  }
+}
+
+constexpr int LOOP_THREADS = 256;
+
+template <int KIND, typename D>
+__global__ void __launch_bounds__(LOOP_THREADS) fwd_loop_kernel(const FwdArgs a) {
+  using T = typename D::T;
+  __shared__ float sh[2 * (LOOP_THREADS / 32) * 3];
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  const int wig = t >> 5;
+  constexpr int NW = LOOP_THREADS / 32;
+  const int H = a.H;
+  const bool w_f32 = a.w_f32 != 0;
+  int parity = 0;
+
+  for (int64_t row = blockIdx.x; row < a.N; row += gridDim.x) {
+    const T* xrow = reinterpret_cast<const T*>(a.x) + row * a.ldx;
+    float rstd, mean_d = 0.f, pivot = 0.f;
+    if constexpr (KIND == KIND_LN) {
+      pivot = load_elem<D>(xrow, 0);
+      // Welford's online recurrence ("Skill: Write CUDA LayerNorm Kernel",
+      // step 2) over this thread's strided elements.
+      Welford w{0.f, 0.f, 0.f};
+      for (int j = t; j < H; j += LOOP_THREADS) {
+        const float d = load_elem<D>(xrow, j) - pivot;
+        w.n += 1.f;
+        const float old = w.m;
+        w.m = old + (d - old) / w.n;
+        w.m2 = fmaf(d - old, d - w.m, w.m2);
+      }
+      w = group_welford(w, sh, NW, wig, lane, 1, parity);
+      mean_d = w.m;
+      rstd = rsqrtf(w.m2 / (float)H + a.eps);
+    } else {
+      float ss[1] = {0.f};
+      if constexpr (KIND == KIND_FUSED) {
+        // h is only summed here; it is stored in the second pass, so that
+        // pass can still re-form the fp32 sum when h_out aliases an input.
+        const T* rrow = reinterpret_cast<const T*>(a.res) + row * a.ldr;
+        for (int j = t; j < H; j += LOOP_THREADS) {
+          const float h = load_elem<D>(xrow, j) + load_elem<D>(rrow, j);
+          ss[0] = fmaf(h, h, ss[0]);
+        }
+      } else {
+        for (int j = t; j < H; j += LOOP_THREADS) {
+          const float v = load_elem<D>(xrow, j);
+          ss[0] = fmaf(v, v, ss[0]);
+        }
+      }
+      group_sum<1>(ss, sh, NW, wig, lane, 1, parity);
+      rstd = rsqrtf(ss[0] / (float)H + a.eps);
+    }
+    if (t == 0) {
+      if constexpr (KIND == KIND_LN) {
+        if (a.mean) a.mean[row] = pivot + mean_d;
+      }
+      if (a.rstd) a.rstd[row] = rstd;
+    }
+
+    T* yrow = reinterpret_cast<T*>(a.y) + row * a.ldy;
+    for (int j = t; j < H; j += LOOP_THREADS) {
+      const float g = a.gamma ? load_param<D>(a.gamma, j, w_f32) : 1.f;
+      float out;
+      if constexpr (KIND == KIND_LN) {
+        const float b = a.beta ? load_param<D>(a.beta, j, w_f32) : 0.f;
+        out = fmaf((load_elem<D>(xrow, j) - pivot - mean_d) * rstd, g, b);
+      } else if constexpr (KIND == KIND_FUSED) {
+        // Element j of x and residual is read, and h_out[j] written, by this
+        // thread only, so storing h here is safe when h_out aliases an input.
+        const float h = load_elem<D>(xrow, j) + load_elem<D>(reinterpret_cast<const T*>(a.res) + row * a.ldr, j);
+        store_elem<D>(reinterpret_cast<T*>(a.h) + row * a.ldh, j, h);
+        out = (h * rstd) * g;
+      } else {
+        out = (load_elem<D>(xrow, j) * rstd) * g;
+      }
+      store_elem<D>(yrow, j, out);
+    }
+    parity ^= 1;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side configuration.
+// ---------------------------------------------------------------------------
+
+static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Persistent grid for the row kernels: as many CTAs as fit on the GPU at
+// once (queried per kernel), or fewer when there are fewer row groups.
+template <typename K>
+static int64_t persistent_blocks(K kern, int threads, size_t smem, const DeviceInfo& dev, int64_t want) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  return std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)per_sm * dev.sm_count));
+}
+
+template <typename K>
+static cudaError_t launch_rows(K kern, const FwdArgs& a, int threads, size_t smem, const DeviceInfo& dev,
+                               int64_t groups, cudaStream_t s) {
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<(unsigned)persistent_blocks(kern, threads, smem, dev, groups), threads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int KIND, typename D, int VPT>
+static cudaError_t run_rows(const FwdArgs& a, int threads, int rpc, size_t smem, const DeviceInfo& dev,
+                            cudaStream_t s) {
+  const int64_t groups = (a.N + rpc - 1) / rpc;
+  if (threads <= 256)
+    return launch_rows(fwd_rows_kernel<KIND, D, VPT, 256, (VPT * D::VEC > 16 ? 2 : 3)>, a, threads, smem, dev,
+                       groups, s);
+  if (threads <= 640) return launch_rows(fwd_rows_kernel<KIND, D, VPT, 640, 1>, a, threads, smem, dev, groups, s);
+  return launch_rows(fwd_rows_kernel<KIND, D, VPT, 1024, 1>, a, threads, smem, dev, groups, s);
+}
+
+template <int KIND, typename D, int VPT>
+static cudaError_t run_staged(const FwdArgs& a, const StageCfg& c, int64_t blocks, size_t smem, cudaStream_t s) {
+  auto kern = fwd_staged_kernel<KIND, D, VPT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)blocks, kStagedThreads, smem, s>>>(a, c);
+  return cudaGetLastError();
+}
+
+template <int KIND, typename D>
+cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream_t s) {
+  using T = typename D::T;
+  constexpr int VEC = D::VEC;
+  // Elements a thread: 32 for bf16 LayerNorm/RMSNorm (halves the per-row
+  // reduction overhead per element), else 16 (fused keeps two rows' inputs in
+  // flight; fp32 takes twice the registers per element).
+  constexpr int VPT_MAX = (KIND != KIND_FUSED && VEC == 8) ? 4 : 16 / VEC;
+  const size_t es = sizeof(T);
+  bool aligned = aligned16(a.x) && aligned16(a.y) && (a.ldx * es) % 16 == 0 && (a.ldy * es) % 16 == 0;
+  if (a.gamma) aligned = aligned && aligned16(a.gamma);
+  if (a.beta) aligned = aligned && aligned16(a.beta);
+  if (KIND == KIND_FUSED) {
+    aligned = aligned && aligned16(a.res) && aligned16(a.h) && (a.ldr * es) % 16 == 0 &&
+              (a.ldh * es) % 16 == 0;
+  }
+  // Register-row shape: narrow rows one warp each (VPT = smallest power of
+  // two covering H), wider rows 16 elements a thread with more warps.
+  const bool vec_ok = aligned && a.H % VEC == 0;
+  const int Hv = a.H / VEC;
+  int vpt = VPT_MAX, tpr = 0;
+  if (Hv <= 32 * VPT_MAX) {
+    tpr = 32;
+    vpt = 1;
+    while (vpt * 32 < Hv) vpt *= 2;
+  } else {
+    tpr = ((Hv + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32;
+  }
+  const int rpc_rows = tpr <= 256 ? 256 / tpr : 1;
+  // group scratch, then fp32 gamma (and beta) for vpt vectors of tpr threads
+  const size_t rows_smem = (((size_t)rpc_rows * 2 * (tpr / 32) * 3 + 3) & ~(size_t)3) * sizeof(float) +
+                           (KIND == KIND_LN ? 2 : 1) * (size_t)vpt * VEC * tpr * sizeof(float);
+  const bool rows_ok = vec_ok && tpr <= 1024 && rows_smem <= (size_t)dev.max_smem_optin;
+  StageCfg c{};
+  constexpr int NT = KIND == KIND_FUSED ? 2 : 1;
+  // Staged consumers keep at most 8 packed vectors of each tensor, and fp32
+  // copies of gamma (and beta) in shared memory.
+  const bool staged_ok = vec_ok && staged_config(a.H, (int)es, NT, dev.max_smem_optin, (8 / NT) * VEC, &c,
+                                                 KIND == KIND_LN ? 2 : 1);
+  bool use_rows = false, use_staged = false;
+  switch (dev.path) {
+    case PATH_AUTO:
+      use_rows = rows_ok && tpr <= kRowsAutoMaxThreads;
+      use_staged = !use_rows && staged_ok;
+      use_rows = use_rows || (!use_staged && rows_ok);
+      break;
+    case PATH_ROWS: use_rows = rows_ok; break;
+    case PATH_STAGED:
+      use_staged = staged_ok;
+      use_rows = !use_staged && rows_ok;
+      break;
+    default: break;
+  }
+  if (use_staged) {
+    c.err = dev.err;
+    c.contiguous = a.ldx == a.H && (NT == 1 || a.ldr == a.H);
+    const int stpr = 32 * (c.W / c.G);
+    const int svpt = (Hv + stpr - 1) / stpr;
+    const size_t smem = staged_smem_bytes(c, NT);
+    const int64_t blocks = std::min<int64_t>((int64_t)dev.sm_count, (a.N + c.G - 1) / c.G);
+    if (svpt <= 1) return run_staged<KIND, D, 1>(a, c, blocks, smem, s);
+    if (svpt <= 2) return run_staged<KIND, D, 2>(a, c, blocks, smem, s);
+    if (svpt <= 3) return run_staged<KIND, D, 3>(a, c, blocks, smem, s);
+    if (svpt <= 4) return run_staged<KIND, D, 4>(a, c, blocks, smem, s);
+    if constexpr (NT == 1) {
+      if (svpt <= 5) return run_staged<KIND, D, 5>(a, c, blocks, smem, s);
+      if (svpt <= 6) return run_staged<KIND, D, 6>(a, c, blocks, smem, s);
+      return run_staged<KIND, D, 8>(a, c, blocks, smem, s);
+    }
+  }
+  if (use_rows) {
+    a.tpr = tpr;
+    const int rpc = rpc_rows;
+    const int threads = rpc * tpr;
+    const size_t smem = rows_smem;
+    switch (vpt) {
+      case 1: return run_rows<KIND, D, 1>(a, threads, rpc, smem, dev, s);
+      case 2: return run_rows<KIND, D, 2>(a, threads, rpc, smem, dev, s);
+      default:
+        if constexpr (VPT_MAX >= 4) return run_rows<KIND, D, 4>(a, threads, rpc, smem, dev, s);
+        break;
+    }
+  }
+  const int64_t blocks = std::min<int64_t>(a.N, (int64_t)dev.sm_count * 8);
+  fwd_loop_kernel<KIND, D><<<(unsigned)blocks, LOOP_THREADS, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace normk

@@ -95,6 +95,13 @@ constexpr int kStagedThreads = (kStagedConsumerWarps + 1) * 32;
 int bwd_max_partials(const DeviceInfo& dev);
 inline int bwd_partial_stride(int H) { return (H + 3) & ~3; }
 
+// Per-dtype launch logic, defined in fwd_kernels.cuh / bwd_kernels.cuh and
+// instantiated in norm_fwd_<dtype>.cu / norm_bwd_<dtype>.cu.
+template <int KIND, typename D>
+cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream_t s);
+template <int KIND, typename D>
+cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& dev, cudaStream_t s);
+
 cudaError_t launch_forward(int kind, Dtype dt, FwdArgs a, const DeviceInfo& dev, cudaStream_t s);
 cudaError_t launch_backward(int kind, Dtype dt, BwdArgs a, void* dgamma, void* dbeta,
                             const DeviceInfo& dev, cudaStream_t s);
