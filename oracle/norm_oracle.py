@@ -38,6 +38,8 @@ __all__ = [
     "fused_add_rms_norm_forward",
     "layer_norm_backward",
     "rms_norm_backward",
+    "layer_norm_backward_from_output",
+    "rms_norm_backward_from_output",
     "fused_add_rms_norm_backward",
     "fused_add_rms_norm_backward_from_h",
     "welford_sequential",
@@ -260,6 +262,60 @@ def rms_norm_backward(dy, x, gamma=None, eps=1e-5):
     mean_sq = (x * x).sum(axis=1) / H
     rstd = 1.0 / np.sqrt(mean_sq + eps)
     x_hat = x * rstd[:, None]
+    g = dy * gm[None, :]
+    c2 = (g * x_hat).sum(axis=1) / H
+    dx = rstd[:, None] * (g - x_hat * c2[:, None])
+    dgamma = (dy * x_hat).sum(axis=0)
+    return dx, dgamma
+
+
+def layer_norm_backward_from_output(dy, y, rstd, gamma=None, beta=None):
+    """LayerNorm backward from the saved output -> (dx, dgamma, dbeta), float64.
+
+    The step 8 formulas of "Skill: Write CUDA LayerNorm Kernel" (as in
+    ``layer_norm_backward``), with x_hat recovered from the forward's output
+    instead of recomputed from x: y = x_hat*gamma + beta gives
+    x_hat = (y - beta) / gamma.  "Rewrite Triton normalization backward
+    kernel_1 (#499)", Benchmark harness, has the backward read the forward's
+    saved output.  ``rstd`` is the forward's saved 1/sqrt(var + eps) per row
+    (it cannot be recovered from y).  Columns with gamma = 0 carry no
+    information about x_hat and give non-finite results there.
+    """
+    dy = _f64_2d(dy)
+    y = _f64_2d(y)
+    if dy.shape != y.shape:
+        raise ValueError("dy and y must have the same shape")
+    H = y.shape[1]
+    gm = _param(gamma, H, 1.0)
+    bt = _param(beta, H, 0.0)
+    rstd = np.asarray(rstd, dtype=np.float64).reshape(-1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        x_hat = (y - bt[None, :]) / gm[None, :]
+    g = dy * gm[None, :]
+    sum_g = g.sum(axis=1)
+    sum_g_xhat = (g * x_hat).sum(axis=1)
+    dx = (rstd[:, None] / H) * (H * g - sum_g[:, None] - x_hat * sum_g_xhat[:, None])
+    dgamma = (dy * x_hat).sum(axis=0)
+    dbeta = dy.sum(axis=0)
+    return dx, dgamma, dbeta
+
+
+def rms_norm_backward_from_output(dy, y, rstd, gamma=None):
+    """RMSNorm backward from the saved output -> (dx, dgamma), float64.
+
+    The ``rms_norm_backward`` formulas with x_hat = y / gamma recovered from
+    the forward's output y = x_hat*gamma; ``rstd`` is the forward's saved
+    1/sqrt(mean(x^2) + eps).
+    """
+    dy = _f64_2d(dy)
+    y = _f64_2d(y)
+    if dy.shape != y.shape:
+        raise ValueError("dy and y must have the same shape")
+    H = y.shape[1]
+    gm = _param(gamma, H, 1.0)
+    rstd = np.asarray(rstd, dtype=np.float64).reshape(-1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        x_hat = y / gm[None, :]
     g = dy * gm[None, :]
     c2 = (g * x_hat).sum(axis=1) / H
     dx = rstd[:, None] * (g - x_hat * c2[:, None])

@@ -354,6 +354,36 @@ def pin_fused_backward_from_h(O):
         _close(dg_s, tdg, 1e-9, 1e-11, "from-h dgamma vs autograd")
 
 
+def pin_backward_from_output(O):
+    """The saved-output form of the backward.
+
+    * Fed the exact forward output and rstd, it equals the x form (pinned
+      above by autograd and finite differences), with and without gamma/beta.
+    * It is a function of (dy, y, rstd, gamma, beta) alone: a row rescaled in
+      rstd scales dx by the same factor and leaves dgamma, dbeta unchanged.
+    """
+    for i, (N, H) in enumerate(SHAPES):
+        eps = 1e-5
+        x, gamma, beta, dy, _ = _case(130 + i, N, H)
+        for g, b in ((gamma, beta), (None, None), (gamma, None)):
+            y, _, rstd = O.layer_norm_forward(x, g, b, eps)
+            want = O.layer_norm_backward(dy, x, g, eps)
+            got = O.layer_norm_backward_from_output(dy, y, rstd, g, b)
+            for a_, w_, nm in zip(got, want, ("dx", "dgamma", "dbeta")):
+                _close(a_, w_, 1e-10, 1e-12, f"LN from-output {nm}")
+            yr, rr = O.rms_norm_forward(x, g, eps)
+            want = O.rms_norm_backward(dy, x, g, eps)
+            got = O.rms_norm_backward_from_output(dy, yr, rr, g)
+            for a_, w_, nm in zip(got, want, ("dx", "dgamma")):
+                _close(a_, w_, 1e-10, 1e-12, f"RMS from-output {nm}")
+        y, _, rstd = O.layer_norm_forward(x, gamma, beta, eps)
+        k = np.linspace(0.5, 2.0, N)
+        a1 = O.layer_norm_backward_from_output(dy, y, rstd, gamma, beta)
+        a2 = O.layer_norm_backward_from_output(dy, y, rstd * k, gamma, beta)
+        _close(a2[0], a1[0] * k[:, None], 1e-12, 1e-12, "dx linear in rstd")
+        _close(a2[1], a1[1], 0, 0, "dgamma independent of rstd")
+
+
 # --------------------------------------------------------------------------
 # storage rounding
 # --------------------------------------------------------------------------
@@ -412,4 +442,5 @@ ALL_PINS = [
     pin_fused_backward_from_h,
     pin_bf16_rounding,
     pin_f16_rounding,
+    pin_backward_from_output,
 ]

@@ -17,7 +17,7 @@ import torch
 
 import oracle as O
 import rmsnorm_ln_fwd_gb300 as nl
-from normtest import DT_NAME, Guarded, check_out, check_param, np64, rms_dx_scale
+from normtest import DT_NAME, DT_ORACLE, Guarded, check_out, check_param, np64, rms_dx_scale
 from rmsnorm_ln_fwd_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -42,15 +42,21 @@ def _inputs(N, H, dt, seed):
 
 
 def _stored_h(t, eps):
-    """h and rstd as the training forward leaves them."""
+    """h and rstd as the training forward leaves them, and the oracle's own h
+    and rstd (the oracle side never takes an input from the CUDA path; the two
+    h agree bit for bit, which is checked here)."""
     _, h, rstd = nl.fused_add_rms_forward(t["x"], t["residual"], t["gamma"], eps)
-    return h, rstd
+    torch.cuda.synchronize()
+    _, hr, rr = O.fused_add_rms_norm_forward(np64(t["x"]), np64(t["residual"]), np64(t["gamma"]), eps,
+                                             DT_ORACLE[h.dtype])
+    assert np.array_equal(np64(h), hr), "stored h differs from the oracle's"
+    return h, rstd, hr, rr
 
 
 def fused_bwd_case(N, H, dt, eps=1e-6, seed=0, with_dh=True, residual_grad="separate", dx_into=None,
                    saved_rstd=False, gamma=True):
     t = _inputs(N, H, dt, seed)
-    h, rstd_fwd = _stored_h(t, eps)
+    h, rstd_fwd, hn, rr = _stored_h(t, eps)
     g = t["gamma"] if gamma else None
     # rstd of the stored h itself (the training forward's rstd is of the
     # unrounded fp32 sum; identical for fp32 rows)
@@ -63,7 +69,7 @@ def fused_bwd_case(N, H, dt, eps=1e-6, seed=0, with_dh=True, residual_grad="sepa
     dx, dres, dg = nl.fused_add_rms_backward(dy, h, rstd, g, dh, residual_grad=residual_grad, dx=dx_buf)
     torch.cuda.synchronize()
 
-    hn, dyn = np64(h), np64(dy0)
+    dyn = np64(dy0)
     gn = None if g is None else np64(g)
     dhn = None if dh0 is None else np64(dh0)
     dhr, dgr = O.fused_add_rms_norm_backward_from_h(dyn, hn, gn, eps, dhn)
@@ -73,9 +79,11 @@ def fused_bwd_case(N, H, dt, eps=1e-6, seed=0, with_dh=True, residual_grad="sepa
         scale = scale + np.abs(dhn)
     if saved_rstd and dt != F32:
         # dx = rstd*g - rstd^3*h*sum(g*h)/H: a relative rstd difference d per
-        # row moves dx by at most 3*d times its terms' magnitude.
+        # row moves dx by at most 3*d times its terms' magnitude.  d is the
+        # oracle's: rstd of the exact sum against rstd of the stored h (the
+        # saved fp32 rstd sits within 2^-22 of the former).
         r_h = O.rms_norm_forward(hn, None, eps)[1]
-        d = np.abs(np64(rstd_fwd) / r_h - 1.0)
+        d = np.abs(rr / r_h - 1.0) + 2.0 ** -22
         scale = scale * (1.0 + 3.0 * d[:, None] * 2.0 ** 20)
     what = f"fused bwd {N}x{H} dh={with_dh} res={residual_grad} into={dx_into}"
     check_out(np64(dx), mult * dhr, mult * scale, dt, what + " dx")
@@ -163,7 +171,7 @@ def _strided(src, ld, offset=0):
 def test_fused_bwd_strides_and_alignment(H, ld, off, dt):
     N, eps = 67, 1e-6
     t = _inputs(N, H, dt, 3)
-    h, _ = _stored_h(t, eps)
+    h, _, hn, _ = _stored_h(t, eps)
     rstd = nl.rms_forward(h, t["gamma"], eps)[1]
     dy, hs, dh = _strided(t["dy"], ld, off), _strided(h, ld, off), _strided(t["dh_stream"], ld, off)
     dxs = _strided(torch.zeros_like(h), ld, off)
@@ -179,7 +187,7 @@ def test_fused_bwd_strides_and_alignment(H, ld, off, dt):
                                     torch.cuda.current_stream().cuda_stream)
     nl._lib.check("fused_add_rms_backward", st)
     torch.cuda.synchronize()
-    hn, dyn, dhn, gn = np64(h), np64(t["dy"]), np64(t["dh_stream"]), np64(t["gamma"])
+    dyn, dhn, gn = np64(t["dy"]), np64(t["dh_stream"]), np64(t["gamma"])
     dhr, dgr = O.fused_add_rms_norm_backward_from_h(dyn, hn, gn, eps, dhn)
     scale = rms_dx_scale(dyn, hn, gn, eps) + np.abs(dhn)
     check_out(np64(dxs), dhr, scale, dt, f"strided dx {H}/{ld}+{off}")
@@ -191,7 +199,7 @@ def test_fused_bwd_strides_and_alignment(H, ld, off, dt):
 def test_fused_bwd_guard_bands(H, dt):
     N, eps = 67, 1e-6
     t = _inputs(N, H, dt, 5)
-    h, _ = _stored_h(t, eps)
+    h, _, hn, _ = _stored_h(t, eps)
     rstd = nl.rms_forward(h, t["gamma"], eps)[1]
     gx, gr, gg = Guarded((N, H), dt, DEV), Guarded((N, H), dt, DEV), Guarded((H,), dt, DEV)
     lib = nl._lib.load()
@@ -205,7 +213,7 @@ def test_fused_bwd_guard_bands(H, dt):
     nl._lib.check("fused_add_rms_backward", st)
     torch.cuda.synchronize()
     assert gx.ok() and gr.ok() and gg.ok(), "write outside an output"
-    hn, dyn, dhn, gn = np64(h), np64(t["dy"]), np64(t["dh_stream"]), np64(t["gamma"])
+    dyn, dhn, gn = np64(t["dy"]), np64(t["dh_stream"]), np64(t["gamma"])
     dhr, dgr = O.fused_add_rms_norm_backward_from_h(dyn, hn, gn, eps, dhn)
     check_out(np64(gx.t), dhr, rms_dx_scale(dyn, hn, gn, eps) + np.abs(dhn), dt, f"guarded dx {H}")
     assert torch.equal(gx.t, gr.t)
@@ -215,7 +223,7 @@ def test_fused_bwd_guard_bands(H, dt):
 @pytest.mark.parametrize("H,dt", [(1024, BF), (5120, BF), (2049, F32)])
 def test_fused_bwd_deterministic(H, dt):
     t = _inputs(300, H, dt, 7)
-    h, rstd = _stored_h(t, 1e-6)
+    h, rstd, _, _ = _stored_h(t, 1e-6)
     a = nl.fused_add_rms_backward(t["dy"], h, rstd, t["gamma"], t["dh_stream"])
     b = nl.fused_add_rms_backward(t["dy"], h, rstd, t["gamma"], t["dh_stream"])
     torch.cuda.synchronize()

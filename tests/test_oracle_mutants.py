@@ -106,6 +106,20 @@ def _fused_from_h_forgets_stream():
     return f
 
 
+def _ln_from_y_forgets_beta():
+    def f(dy, y, rstd, gamma=None, beta=None):
+        return R.layer_norm_backward_from_output(dy, y, rstd, gamma, None)
+    return f
+
+
+def _rms_from_y_times_gamma():
+    def f(dy, y, rstd, gamma=None):
+        H = np.asarray(y).shape[1]
+        gm = np.ones(H) if gamma is None else np.asarray(gamma, dtype=np.float64)
+        return R.rms_norm_backward_from_output(dy, np.asarray(y) * gm * gm, rstd, gamma)
+    return f
+
+
 def _merge_wrong(a, b):
     na, ma, m2a = a
     nb, mb, m2b = b
@@ -159,6 +173,8 @@ MUTANTS = {
     "rms_bwd_dgamma_of_x": dict(rms_norm_backward=_rms_bwd(dgamma_of_x=True)),
     "fused_normalises_x_not_h": dict(fused_add_rms_norm_forward=_fused_from_x()),
     "fused_bwd_halves_dres": dict(fused_add_rms_norm_backward=_fused_bwd_half()),
+    "ln_from_output_forgets_beta": dict(layer_norm_backward_from_output=_ln_from_y_forgets_beta()),
+    "rms_from_output_multiplies_gamma": dict(rms_norm_backward_from_output=_rms_from_y_times_gamma()),
     "fused_bwd_from_h_forgets_stream": dict(fused_add_rms_norm_backward_from_h=_fused_from_h_forgets_stream()),
     "welford_merge_wrong_weight": dict(welford_merge=_merge_wrong),
     "welford_recurrence_old_mean_twice": dict(welford_sequential=_welford_seq_wrong),
