@@ -48,8 +48,9 @@ METRIC = "LN/RMSNorm fwd+bwd achieved HBM GB/s and % of GB300 peak; bwd µs per 
 OPS = ("ln_fwd", "ln_bwd", "rms_fwd", "rms_bwd", "fused_fwd")
 # Measured by --sweep / --profile-op, not part of the step: the fused-add
 # backward (dx and dres from the stored h, plus the residual-stream gradient).
-EXTRA_OPS = ("fused_bwd",)
-LAUNCHES = {"ln_fwd": 1, "rms_fwd": 1, "fused_fwd": 1, "ln_bwd": 2, "rms_bwd": 2, "fused_bwd": 2}
+EXTRA_OPS = ("fused_bwd", "ln_bwd_y", "rms_bwd_y")
+LAUNCHES = {"ln_fwd": 1, "rms_fwd": 1, "fused_fwd": 1, "ln_bwd": 2, "rms_bwd": 2, "fused_bwd": 2, "ln_bwd_y": 2,
+            "rms_bwd_y": 2}
 
 
 def alg_bytes(op: str, N: int, H: int, e: int = 2, ew: int = 2) -> int:
@@ -63,6 +64,9 @@ def alg_bytes(op: str, N: int, H: int, e: int = 2, ew: int = 2) -> int:
         "rms_bwd": 3 * nh + 4 * N + H * ew + H * ew,
         # reads dy, h, the stream gradient; writes dx and dres
         "fused_bwd": 5 * nh + 4 * N + H * ew + H * ew,
+        # from the saved output: reads dy, y, rstd, gamma (and beta)
+        "ln_bwd_y": 3 * nh + 4 * N + 2 * H * ew + 2 * H * ew,
+        "rms_bwd_y": 3 * nh + 4 * N + H * ew + H * ew,
     }[op]
 
 
@@ -218,6 +222,15 @@ class Shape:
             st = L.rms_backward(t["dy"].data_ptr(), H, t["x"].data_ptr(), H, self.rstd_r.data_ptr(),
                                 t["gamma"].data_ptr(), self.dxr.data_ptr(), H, self.dgr.data_ptr(),
                                 self.ws.data_ptr(), self.wsb, N, H, BF, BF, stream)
+        elif op == "ln_bwd_y":
+            st = L.ln_backward_from_output(t["dy"].data_ptr(), H, self.y.data_ptr(), H, self.rstd.data_ptr(),
+                                           t["gamma"].data_ptr(), t["beta"].data_ptr(), self.dxf.data_ptr(), H,
+                                           self.dg.data_ptr(), self.db.data_ptr(), self.ws.data_ptr(), self.wsb, N,
+                                           H, BF, BF, stream)
+        elif op == "rms_bwd_y":
+            st = L.rms_backward_from_output(t["dy"].data_ptr(), H, self.yr.data_ptr(), H, self.rstd_r.data_ptr(),
+                                            t["gamma"].data_ptr(), self.dxf.data_ptr(), H, self.dgr.data_ptr(),
+                                            self.ws.data_ptr(), self.wsb, N, H, BF, BF, stream)
         elif op == "fused_bwd":
             st = L.fused_add_rms_backward(t["dy"].data_ptr(), H, self.h.data_ptr(), H, self.rstd_f.data_ptr(),
                                           t["gamma"].data_ptr(), t["dh_stream"].data_ptr(), H, self.dxf.data_ptr(),
@@ -481,9 +494,11 @@ SWEEP = [("ln_fwd", 8192, 1024), ("rms_fwd", 8192, 1024), ("ln_bwd", 8192, 1024)
          ("fused_fwd", 16384, 4096), ("ln_bwd", 32768, 1024), ("rms_bwd", 32768, 1024), ("ln_bwd", 16384, 2048),
          ("rms_bwd", 16384, 2048), ("ln_fwd", 2048, 16384), ("rms_fwd", 2048, 16384), ("ln_bwd", 2048, 16384),
          ("rms_bwd", 2048, 16384), ("ln_fwd", 512, 16384), ("rms_fwd", 512, 16384), ("ln_bwd", 512, 16384),
-         ("rms_bwd", 512, 16384), ("fused_bwd", 8192, 1024), ("fused_bwd", 8192, 5120), ("fused_bwd", 16384, 4096)]
+         ("rms_bwd", 512, 16384), ("fused_bwd", 8192, 1024), ("fused_bwd", 8192, 5120), ("fused_bwd", 16384, 4096),
+         ("ln_bwd_y", 8192, 1024), ("ln_bwd_y", 8192, 5120), ("rms_bwd_y", 8192, 1024), ("rms_bwd_y", 8192, 5120)]
 
-FORWARD_OF = {"ln_bwd": "ln_fwd", "rms_bwd": "rms_fwd", "fused_bwd": "fused_fwd"}
+FORWARD_OF = {"ln_bwd": "ln_fwd", "rms_bwd": "rms_fwd", "fused_bwd": "fused_fwd", "ln_bwd_y": "ln_fwd",
+              "rms_bwd_y": "rms_fwd"}
 
 
 def run_sweep(args):

@@ -195,6 +195,36 @@ norm_status ln_backward_static_workspace(const void* dy, int64_t lddy, const voi
                                          norm_dtype x_dtype, norm_dtype w_dtype, norm_stream_t stream);
 
 /*
+ * LayerNorm backward from the forward's saved output instead of x.
+ * "Rewrite Triton normalization backward kernel_1 (#499)", Benchmark harness:
+ * the backward reads the output the forward saved.  x_hat is recovered as
+ * (y - beta) / gamma and the formulas of ln_backward run on it with the saved
+ * rstd ("Skill: Write CUDA LayerNorm Kernel", Required reasoning process
+ * step 8).  x and mean are not needed.
+ * y [N x ldy]: the forward's output (ln_forward's y, same gamma and beta).
+ * rstd [N] fp32: the forward's saved rstd.  gamma, beta [H] or NULL (ones,
+ *   zeros).  A column whose gamma is 0 holds no trace of x_hat: its dx and
+ *   dgamma come out non-finite (IEEE division by zero); nothing is checked.
+ * dx, dgamma, dbeta, workspace: as ln_backward; dx may be exactly dy and must
+ *   not overlap y.  x_hat recovered from a rounded y carries that rounding
+ *   (2^-9 relative for bf16, 2^-11 for fp16) into dx and dgamma.
+ */
+norm_status ln_backward_from_output(const void* dy, int64_t lddy, const void* y, int64_t ldy, const float* rstd,
+                                    const void* gamma, const void* beta, void* dx, int64_t lddx, void* dgamma,
+                                    void* dbeta, void* workspace, size_t workspace_bytes, int64_t N, int64_t H,
+                                    norm_dtype x_dtype, norm_dtype w_dtype, norm_stream_t stream);
+
+/*
+ * RMSNorm backward from the saved output: x_hat = y / gamma, then the
+ * formulas of rms_backward with the saved rstd.  Arguments as
+ * ln_backward_from_output without beta/dbeta.
+ */
+norm_status rms_backward_from_output(const void* dy, int64_t lddy, const void* y, int64_t ldy, const float* rstd,
+                                     const void* gamma, void* dx, int64_t lddx, void* dgamma, void* workspace,
+                                     size_t workspace_bytes, int64_t N, int64_t H, norm_dtype x_dtype,
+                                     norm_dtype w_dtype, norm_stream_t stream);
+
+/*
  * Fused residual add + RMSNorm backward.  "Skill: Write a Triton Fused
  * Add+RMSNorm Kernel", Required reasoning process steps 9-10: the backward
  * reads the stored sum h and rstd; the RMSNorm gradient with respect to h,

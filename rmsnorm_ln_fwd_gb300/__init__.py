@@ -12,8 +12,10 @@ from .ops import (  # noqa: F401
     fused_add_rms_backward,
     fused_add_rms_forward,
     ln_backward,
+    ln_backward_from_output,
     ln_forward,
     rms_backward,
+    rms_backward_from_output,
     rms_forward,
 )
 
@@ -24,6 +26,8 @@ __all__ = [
     "fused_add_rms_backward",
     "ln_backward",
     "rms_backward",
+    "ln_backward_from_output",
+    "rms_backward_from_output",
     "bwd_workspace_bytes",
     "NormError",
     "load_library",

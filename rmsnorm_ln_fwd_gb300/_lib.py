@@ -35,6 +35,10 @@ SIGNATURES = {
     "ln_backward": (_I, [_P, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P, _P, _P, ctypes.c_size_t, _I64, _I64,
                          _I, _I, _P]),
     "rms_backward": (_I, [_P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _P, ctypes.c_size_t, _I64, _I64, _I, _I, _P]),
+    "ln_backward_from_output": (_I, [_P, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P, _P, _P, ctypes.c_size_t, _I64,
+                                     _I64, _I, _I, _P]),
+    "rms_backward_from_output": (_I, [_P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _P, ctypes.c_size_t, _I64, _I64,
+                                      _I, _I, _P]),
     "fused_add_rms_backward": (_I, [_P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I64, _P, _I64, _P, _P,
                                     ctypes.c_size_t, _I64, _I64, _I, _I, _P]),
     "ln_backward_static_workspace": (_I, [_P, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P, _P, _I64, _I64, _I, _I,

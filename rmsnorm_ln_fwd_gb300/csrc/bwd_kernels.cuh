@@ -47,8 +47,10 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
   using T = typename D::T;
   constexpr int VEC = D::VEC;
   constexpr int VP = VEC / 2;
-  constexpr bool LN = KIND == KIND_LN;
-  constexpr int NS = LN ? 3 : 1;  // values per row reduction
+  constexpr bool LN = kind_is_ln(KIND);
+  constexpr bool FROM_Y = kind_from_y(KIND);   // x is the forward's output y
+  constexpr bool RECENTER = KIND == KIND_LN;   // see the recentring note above
+  constexpr int NS = LN ? (RECENTER ? 3 : 2) : 1;  // values per row reduction
   extern __shared__ __align__(16) float sh_dyn[];
   const int tpr = a.tpr;
   const int rpc = blockDim.x / tpr;
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
       nd[v] = load_vec_or_zero<D>(dyrow, c, H);
     }
     nrs = a.rstd[r];
-    if (LN) nmu = a.mean[r];
+    if (LN && !FROM_Y) nmu = a.mean[r];
   };
 
   int parity = 0;
@@ -97,15 +99,25 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
 
   const int Hp = a.Hp;
   // Shared memory: group scratch | fp32 gamma (thread-interleaved, shared by
-  // the row slots) | accumulators (ACC_SMEM, thread-interleaved: dgamma then
-  // dbeta) or the fold buffer of the row slots.
+  // the row slots) | from the output: 1/gamma and (LayerNorm) beta, likewise |
+  // accumulators (ACC_SMEM, thread-interleaved: dgamma then dbeta) or the fold
+  // buffer of the row slots.
+  constexpr int NPY = FROM_Y ? (LN ? 2 : 1) : 0;
   const int off_g = ((rpc * 2 * nw * NS) + 3) & ~3;
   const int slots = VPT * VEC * tpr;  // floats of one thread-interleaved array
   float4* gs = reinterpret_cast<float4*>(sh_dyn + off_g);
-  float* sh_acc = sh_dyn + off_g + slots;
+  float4* gis = gs + slots / 4;
+  float4* bes = gis + slots / 4;
+  float* sh_acc = sh_dyn + off_g + (1 + NPY) * slots;
   float4* sacc_g = reinterpret_cast<float4*>(sh_acc);
   float4* sacc_b = sacc_g + slots / 4;
-  if (slot == 0) stage_params<D, VPT>(gs, a.gamma, w_f32, 1.f, t, tpr, hv);
+  if (slot == 0) {
+    stage_params<D, VPT>(gs, a.gamma, w_f32, 1.f, t, tpr, hv);
+    if constexpr (FROM_Y) {
+      stage_inv_params<D, VPT>(gis, a.gamma, w_f32, t, tpr, hv);
+      if (LN) stage_params<D, VPT>(bes, a.beta, w_f32, 0.f, t, tpr, hv);
+    }
+  }
   if constexpr (ACC_SMEM) {
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
@@ -124,7 +136,19 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
     const float2 r2 = splat2(r);
     float2 xh[VPT][VP];
     uint4 dcur[VPT], hcur[VH];
-    {
+    if constexpr (FROM_Y) {
+      // x_hat = (y - beta) / gamma, from the forward's output.
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        float2 yv[VP], gi[VP], be[VP];
+        unpack2<D>(nx[v], yv);
+        read_pairs<VEC>(gis, v, t, tpr, gi);
+        if (LN) read_pairs<VEC>(bes, v, t, tpr, be);
+#pragma unroll
+        for (int p = 0; p < VP; ++p) xh[v][p] = mul2(LN ? sub2(yv[p], be[p]) : yv[p], gi[p]);
+        dcur[v] = nd[v];
+      }
+    } else {
       // x_hat = x*rstd - mean*rstd: the rounding of mean*rstd shifts the whole
       // row by one constant, which the recentring below removes.
       const float2 b2 = splat2(LN ? -nmu * r : 0.f);
@@ -160,10 +184,8 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
         for (int p = 0; p < VP; ++p) {
           const float2 g = mul2(d[p], gm[p]);
           sgx = fma2(g, xh[v][p], sgx);
-          if (LN) {
-            sg = add2(sg, g);
-            sx = add2(sx, xh[v][p]);
-          }
+          if (LN) sg = add2(sg, g);
+          if (RECENTER) sx = add2(sx, xh[v][p]);
         }
       }
     }
@@ -171,14 +193,15 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
     if (LN) {
       S[0] = sg.x + sg.y;
       S[1] = sgx.x + sgx.y;
-      S[NS - 1] = sx.x + sx.y;
+      if constexpr (RECENTER) S[NS - 1] = sx.x + sx.y;
     } else {
       S[0] = sgx.x + sgx.y;
     }
     group_sum<NS>(S, sh, nw, wig, lane, bar_id, parity);
     // LayerNorm: mean(x_hat) is 0 exactly; its computed value s0 is the shift
-    // left by the saved mean's rounding, removed from x_hat here.
-    const float s0 = LN ? S[NS - 1] * inv_h : 0.f;
+    // left by the saved mean's rounding, removed from x_hat here.  (From the
+    // output there is no saved mean: x_hat is taken as recovered.)
+    const float s0 = RECENTER ? S[NS - 1] * inv_h : 0.f;
     const float c1 = LN ? S[0] * inv_h : 0.f;
     const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
     const float2 s02 = splat2(s0), c12 = splat2(c1), nc22 = splat2(-c2);
@@ -205,7 +228,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
         }
 #pragma unroll
         for (int p = 0; p < VP; ++p) {
-          const float2 xc = LN ? sub2(xh[v][p], s02) : xh[v][p];
+          const float2 xc = RECENTER ? sub2(xh[v][p], s02) : xh[v][p];
           const float2 g = mul2(d[p], gm[p]);
           out[p] = mul2(fma2(xc, nc22, LN ? sub2(g, c12) : g), r2);
           ag[p] = fma2(d[p], xc, ag[p]);
@@ -491,8 +514,10 @@ constexpr int LOOP_THREADS = 256;
 template <int KIND, typename D>
 __global__ void __launch_bounds__(LOOP_THREADS) bwd_loop_kernel(const BwdArgs a) {
   using T = typename D::T;
-  constexpr bool LN = KIND == KIND_LN;
-  constexpr int NS = LN ? 3 : 1;
+  constexpr bool LN = kind_is_ln(KIND);
+  constexpr bool FROM_Y = kind_from_y(KIND);
+  constexpr bool RECENTER = KIND == KIND_LN;
+  constexpr int NS = LN ? (RECENTER ? 3 : 2) : 1;
   constexpr int NW = LOOP_THREADS / 32;
   __shared__ float sh[2 * NW * NS];
   const int t = threadIdx.x;
@@ -514,31 +539,39 @@ __global__ void __launch_bounds__(LOOP_THREADS) bwd_loop_kernel(const BwdArgs a)
     const T* xrow = reinterpret_cast<const T*>(a.x) + row * a.ldx;
     const T* dyrow = reinterpret_cast<const T*>(a.dy) + row * a.lddy;
     const float r = a.rstd[row];
-    const float mu = LN ? a.mean[row] : 0.f;
+    const float mu = (LN && !FROM_Y) ? a.mean[row] : 0.f;
+    // x_hat of column j: from x and the saved statistics, or from the output
+    auto x_hat = [&](float xv, int j) {
+      if constexpr (FROM_Y) {
+        const float gj = a.gamma ? load_param<D>(a.gamma, j, w_f32) : 1.f;
+        const float bj = (LN && a.beta) ? load_param<D>(a.beta, j, w_f32) : 0.f;
+        return (xv - bj) / gj;
+      } else {
+        return LN ? (xv - mu) * r : xv * r;
+      }
+    };
     float S[NS];
 #pragma unroll
     for (int k = 0; k < NS; ++k) S[k] = 0.f;
     for (int j = t; j < H; j += LOOP_THREADS) {
-      const float xv = load_elem<D>(xrow, j);
-      const float xh = LN ? (xv - mu) * r : xv * r;
+      const float xh = x_hat(load_elem<D>(xrow, j), j);
       const float g = __fmul_rn(load_elem<D>(dyrow, j), a.gamma ? load_param<D>(a.gamma, j, w_f32) : 1.f);
       if (LN) {
         S[0] += g;
         S[1] = fmaf(g, xh, S[1]);
-        S[2] += xh;
+        if constexpr (RECENTER) S[NS - 1] += xh;
       } else {
         S[0] = fmaf(g, xh, S[0]);
       }
     }
     group_sum<NS>(S, sh, NW, wig, lane, 1, parity);
-    const float s0 = LN ? S[2] * inv_h : 0.f;
+    const float s0 = RECENTER ? S[NS - 1] * inv_h : 0.f;
     const float c1 = LN ? S[0] * inv_h : 0.f;
     const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
     T* dxrow = reinterpret_cast<T*>(a.dx) + row * a.lddx;
     for (int j = t; j < H; j += LOOP_THREADS) {
-      const float xv = load_elem<D>(xrow, j);
       const float dyv = load_elem<D>(dyrow, j);
-      const float xc = LN ? (xv - mu) * r - s0 : xv * r;
+      const float xc = x_hat(load_elem<D>(xrow, j), j) - s0;
       const float g = __fmul_rn(dyv, a.gamma ? load_param<D>(a.gamma, j, w_f32) : 1.f);
       float dxv = r * (g - c1 - xc * c2);
       if constexpr (KIND == KIND_FUSED) {
@@ -654,7 +687,10 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   using T = typename D::T;
   constexpr int VEC = D::VEC;
   constexpr int VPT_MAX = 16 / VEC;  // 16 elements per thread
-  constexpr int NS = KIND == KIND_LN ? 3 : 1;
+  constexpr bool LN = kind_is_ln(KIND);
+  constexpr bool FROM_Y = kind_from_y(KIND);
+  constexpr int NS = KIND == KIND_LN ? 3 : (LN ? 2 : 1);
+  constexpr int NPY = FROM_Y ? (LN ? 2 : 1) : 0;  // staged 1/gamma, beta arrays
   const size_t es = sizeof(T);
   const size_t wes = a.w_f32 ? 4 : es;
   const bool want = dg != nullptr || db != nullptr;
@@ -671,6 +707,7 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   if (a.dh_in) aligned = aligned && aligned16(a.dh_in) && (a.lddh * es) % 16 == 0;
   if (a.dres) aligned = aligned && aligned16(a.dres) && (a.lddres * es) % 16 == 0;
   if (a.gamma) aligned = aligned && aligned16(a.gamma);
+  if (FROM_Y && LN && a.beta) aligned = aligned && aligned16(a.beta);
   int P = 0;
   cudaError_t err = cudaSuccess;
   bool done = false;
@@ -687,11 +724,11 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
     tpr = ((Hv + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32;
   }
   const int rpc_rows = tpr <= 256 ? 256 / tpr : 1;
-  // group scratch | fp32 gamma | shared accumulators (one row slot) or the
-  // fold buffer of several row slots
+  // group scratch | fp32 gamma (| 1/gamma | beta) | shared accumulators (one
+  // row slot) or the fold buffer of several row slots
   const size_t rows_slots = (size_t)vpt * VEC * tpr;
-  size_t rows_smem_f = (size_t)((rpc_rows * 2 * (tpr / 32) * NS + 3) & ~3) + rows_slots;
-  if (rpc_rows == 1) rows_smem_f += (KIND == KIND_LN ? 2 : 1) * rows_slots;
+  size_t rows_smem_f = (size_t)((rpc_rows * 2 * (tpr / 32) * NS + 3) & ~3) + (1 + NPY) * rows_slots;
+  if (rpc_rows == 1) rows_smem_f += (LN ? 2 : 1) * rows_slots;
   else if (want) rows_smem_f += 2 * (size_t)a.Hp;
   const size_t rows_smem = rows_smem_f * sizeof(float);
   const bool rows_ok = vec_ok && tpr <= 1024 && rows_smem <= (size_t)dev.max_smem_optin;
@@ -700,7 +737,7 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   // column, so it first tries shapes with at most 24 columns per thread.
   StageCfg c{};
   const bool staged_ok =
-      KIND != KIND_FUSED && vec_ok &&
+      KIND != KIND_FUSED && !FROM_Y && vec_ok &&
       ((KIND == KIND_LN && staged_config(a.H, (int)es, 2, dev.max_smem_optin, 24, &c)) ||
        staged_config(a.H, (int)es, 2, dev.max_smem_optin, kStagedMaxCols, &c));
   bool use_rows = false, use_staged = false;
@@ -717,7 +754,7 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
       break;
     default: break;
   }
-  if constexpr (KIND != KIND_FUSED) {
+  if constexpr (KIND != KIND_FUSED && !FROM_Y) {
    if (use_staged) {
     c.err = dev.err;
     c.contiguous = a.ldx == a.H && a.lddy == a.H;
@@ -768,7 +805,7 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   // The column reduction is a programmatic dependent of the main kernel: it
   // is scheduled while the main kernel drains and waits for it on the device.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.Hp + 31) / 32, KIND == KIND_LN ? 2 : 1);
+  cfg.gridDim = dim3((a.Hp + 31) / 32, LN ? 2 : 1);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
@@ -778,7 +815,7 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const float* ws = a.ws;
-  void* dbeta = KIND == KIND_LN ? db : nullptr;
+  void* dbeta = LN ? db : nullptr;
   err = cudaLaunchKernelEx(&cfg, bwd_param_reduce_kernel<D>, ws, P, a.Hp, a.H, dg, dbeta, a.w_f32);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();

@@ -529,6 +529,29 @@ __device__ __forceinline__ void stage_params(float4* dst, const void* p, bool w_
   }
 }
 
+// Reciprocals 1/gamma in the same layout (1 where gamma is absent; columns
+// past the row get 0).  IEEE division: gamma = 0 gives infinity.
+template <typename D, int VPT>
+__device__ __forceinline__ void stage_inv_params(float4* dst, const void* p, bool w_f32, int t, int tpr, int hv) {
+  constexpr int VEC = D::VEC;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int j = t + v * tpr;
+    float2 pr[VEC / 2];
+    if (j < hv) {
+      load_param_pairs<D>(p, j * VEC, w_f32, 1.f, pr);
+#pragma unroll
+      for (int i = 0; i < VEC / 2; ++i) pr[i] = make_float2(1.f / pr[i].x, 1.f / pr[i].y);
+    } else {
+#pragma unroll
+      for (int i = 0; i < VEC / 2; ++i) pr[i] = splat2(0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < VEC / 4; ++q)
+      dst[(v * (VEC / 4) + q) * tpr + t] = make_float4(pr[2 * q].x, pr[2 * q].y, pr[2 * q + 1].x, pr[2 * q + 1].y);
+  }
+}
+
 // The VEC/2 pairs of vector v of this thread from a thread-interleaved array.
 template <int VEC>
 __device__ __forceinline__ void read_pairs(const float4* src, int v, int t, int tpr, float2* out) {

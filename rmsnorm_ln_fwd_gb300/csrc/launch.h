@@ -9,7 +9,12 @@
 namespace normk {
 
 enum Dtype : int { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
-enum Kind : int { KIND_LN = 0, KIND_RMS = 1, KIND_FUSED = 2 };
+enum Kind : int { KIND_LN = 0, KIND_RMS = 1, KIND_FUSED = 2, KIND_LN_Y = 3, KIND_RMS_Y = 4 };
+
+// Backward kinds that recover x_hat from the forward's saved output y
+// (x_hat = (y - beta)/gamma, RMSNorm y/gamma) instead of from x and mean.
+__host__ __device__ constexpr bool kind_from_y(int k) { return k == KIND_LN_Y || k == KIND_RMS_Y; }
+__host__ __device__ constexpr bool kind_is_ln(int k) { return k == KIND_LN || k == KIND_LN_Y; }
 
 // Kernel-family policy (norm_set_kernel_path).  AUTO: register rows when a
 // row needs at most kRowsAutoMaxThreads threads, else the bulk-copy pipeline,
@@ -46,7 +51,9 @@ struct FwdArgs {
   int tpr;      // threads per row (filled in by the launcher)
 };
 
-// Backward: LayerNorm (KIND_LN) or RMSNorm (KIND_RMS).
+// Backward: LayerNorm (KIND_LN) or RMSNorm (KIND_RMS) from x and the saved
+// statistics, the same from the saved output (KIND_LN_Y, KIND_RMS_Y), or the
+// fused add + RMSNorm from the stored sum (KIND_FUSED).
 struct BwdArgs {
   const void* dy;
   int64_t lddy;
@@ -59,6 +66,8 @@ struct BwdArgs {
   int64_t lddx;
   float* ws;  // [2][P][Hp] fp32 partial rows (dgamma, dbeta), or null
   int Hp;     // partial row stride in floats (H rounded up to 4)
+  // Backward from the saved output (KIND_LN_Y, KIND_RMS_Y; x is y):
+  const void* beta;  // LN_Y: the forward's beta, or null (zeros)
   // Fused add + RMSNorm backward only (KIND_FUSED; x is the stored h):
   const void* dh_in;  // gradient arriving through h (the residual stream), or null
   int64_t lddh;

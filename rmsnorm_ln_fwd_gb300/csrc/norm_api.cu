@@ -222,7 +222,7 @@ norm_status backward_common(int kind, const void* dy, int64_t lddy, const void* 
                             int64_t lddx, void* dgamma, void* dbeta, void* ws, size_t ws_bytes,
                             int64_t N, int64_t H, norm_dtype xd, norm_dtype wd, norm_stream_t stream,
                             const void* dh_in = nullptr, int64_t lddh = 0, void* dres = nullptr,
-                            int64_t lddres = 0) {
+                            int64_t lddres = 0, const void* beta = nullptr) {
   norm_status st = check_dtypes(xd, wd);
   if (st != NORM_OK) return st;
   if (!shape_ok(N, H)) return NORM_ERR_INVALID_VALUE;
@@ -286,6 +286,7 @@ norm_status backward_common(int kind, const void* dy, int64_t lddy, const void* 
   a.N = N;
   a.H = (int)H;
   a.w_f32 = wd == NORM_F32;
+  a.beta = beta;
   a.dh_in = dh_in;
   a.lddh = lddh;
   a.dres = dx_twice ? nullptr : dres;
@@ -341,6 +342,22 @@ norm_status rms_backward(const void* dy, int64_t lddy, const void* x, int64_t ld
                          size_t workspace_bytes, int64_t N, int64_t H, norm_dtype x_dtype, norm_dtype w_dtype,
                          norm_stream_t stream) {
   return backward_common(normk::KIND_RMS, dy, lddy, x, ldx, nullptr, rstd, gamma, dx, lddx, dgamma, nullptr,
+                         workspace, workspace_bytes, N, H, x_dtype, w_dtype, stream);
+}
+
+norm_status ln_backward_from_output(const void* dy, int64_t lddy, const void* y, int64_t ldy, const float* rstd,
+                                    const void* gamma, const void* beta, void* dx, int64_t lddx, void* dgamma,
+                                    void* dbeta, void* workspace, size_t workspace_bytes, int64_t N, int64_t H,
+                                    norm_dtype x_dtype, norm_dtype w_dtype, norm_stream_t stream) {
+  return backward_common(normk::KIND_LN_Y, dy, lddy, y, ldy, nullptr, rstd, gamma, dx, lddx, dgamma, dbeta,
+                         workspace, workspace_bytes, N, H, x_dtype, w_dtype, stream, nullptr, 0, nullptr, 0, beta);
+}
+
+norm_status rms_backward_from_output(const void* dy, int64_t lddy, const void* y, int64_t ldy, const float* rstd,
+                                     const void* gamma, void* dx, int64_t lddx, void* dgamma, void* workspace,
+                                     size_t workspace_bytes, int64_t N, int64_t H, norm_dtype x_dtype,
+                                     norm_dtype w_dtype, norm_stream_t stream) {
+  return backward_common(normk::KIND_RMS_Y, dy, lddy, y, ldy, nullptr, rstd, gamma, dx, lddx, dgamma, nullptr,
                          workspace, workspace_bytes, N, H, x_dtype, w_dtype, stream);
 }
 

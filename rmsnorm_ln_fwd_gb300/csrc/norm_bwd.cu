@@ -16,6 +16,8 @@ cudaError_t launch_backward(int kind, Dtype dt, BwdArgs a, void* dgamma, void* d
     switch (kind) {
       case KIND_LN: return launch_bwd_typed<KIND_LN, BF16>(a, dgamma, dbeta, dev, s);
       case KIND_RMS: return launch_bwd_typed<KIND_RMS, BF16>(a, dgamma, nullptr, dev, s);
+      case KIND_LN_Y: return launch_bwd_typed<KIND_LN_Y, BF16>(a, dgamma, dbeta, dev, s);
+      case KIND_RMS_Y: return launch_bwd_typed<KIND_RMS_Y, BF16>(a, dgamma, nullptr, dev, s);
       default: return launch_bwd_typed<KIND_FUSED, BF16>(a, dgamma, nullptr, dev, s);
     }
   }
@@ -23,12 +25,16 @@ cudaError_t launch_backward(int kind, Dtype dt, BwdArgs a, void* dgamma, void* d
     switch (kind) {
       case KIND_LN: return launch_bwd_typed<KIND_LN, F16>(a, dgamma, dbeta, dev, s);
       case KIND_RMS: return launch_bwd_typed<KIND_RMS, F16>(a, dgamma, nullptr, dev, s);
+      case KIND_LN_Y: return launch_bwd_typed<KIND_LN_Y, F16>(a, dgamma, dbeta, dev, s);
+      case KIND_RMS_Y: return launch_bwd_typed<KIND_RMS_Y, F16>(a, dgamma, nullptr, dev, s);
       default: return launch_bwd_typed<KIND_FUSED, F16>(a, dgamma, nullptr, dev, s);
     }
   }
   switch (kind) {
     case KIND_LN: return launch_bwd_typed<KIND_LN, F32>(a, dgamma, dbeta, dev, s);
     case KIND_RMS: return launch_bwd_typed<KIND_RMS, F32>(a, dgamma, nullptr, dev, s);
+    case KIND_LN_Y: return launch_bwd_typed<KIND_LN_Y, F32>(a, dgamma, dbeta, dev, s);
+    case KIND_RMS_Y: return launch_bwd_typed<KIND_RMS_Y, F32>(a, dgamma, nullptr, dev, s);
     default: return launch_bwd_typed<KIND_FUSED, F32>(a, dgamma, nullptr, dev, s);
   }
 }

@@ -7,5 +7,7 @@ namespace normk {
 template cudaError_t launch_bwd_typed<KIND_LN, F32>(BwdArgs, void*, void*, const DeviceInfo&, cudaStream_t);
 template cudaError_t launch_bwd_typed<KIND_RMS, F32>(BwdArgs, void*, void*, const DeviceInfo&, cudaStream_t);
 template cudaError_t launch_bwd_typed<KIND_FUSED, F32>(BwdArgs, void*, void*, const DeviceInfo&, cudaStream_t);
+template cudaError_t launch_bwd_typed<KIND_LN_Y, F32>(BwdArgs, void*, void*, const DeviceInfo&, cudaStream_t);
+template cudaError_t launch_bwd_typed<KIND_RMS_Y, F32>(BwdArgs, void*, void*, const DeviceInfo&, cudaStream_t);
 
 }  // namespace normk

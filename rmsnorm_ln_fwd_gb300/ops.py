@@ -252,3 +252,58 @@ def fused_add_rms_backward(dy, h, rstd, gamma=None, dh_in=None, *, need_param_gr
                                         wsb, N, H, xc, wc, _stream(h.device))
     _lib.check("fused_add_rms_backward", st)
     return out, (dres if residual_grad == "separate" else (out if residual_grad == "same" else None)), dgamma
+
+
+def ln_backward_from_output(dy, y, rstd, gamma=None, beta=None, *, need_param_grads: bool = True,
+                            beta_grad: bool = True, workspace=None, dx=None, param_dtype=None):
+    """LayerNorm backward from the forward's output y (x_hat = (y - beta)/gamma)
+    and saved rstd.  Returns (dx, dgamma, dbeta)."""
+    dyv, N, H, lddy = _rows(dy, "dy")
+    yv, Ny, Hy, ldy = _rows(y, "y")
+    if (Ny, Hy) != (N, H) or dy.dtype != y.dtype:
+        raise ValueError("dy must match y")
+    xc = _dtype_code(y, "y")
+    gamma, beta = _vec(gamma, H, "gamma"), _vec(beta, H, "beta")
+    wdt = gamma.dtype if gamma is not None else (beta.dtype if beta is not None else (param_dtype or y.dtype))
+    wc = _w_code(_DT[wdt], gamma, beta)
+    out = torch.empty_like(y, memory_format=torch.contiguous_format) if dx is None else dx
+    ov, _, _, lddx = _rows(out, "dx")
+    dgamma = torch.empty(H, device=y.device, dtype=wdt) if need_param_grads else None
+    dbeta = torch.empty(H, device=y.device, dtype=wdt) if (need_param_grads and beta_grad) else None
+    ws, wsb = (None, 0)
+    if need_param_grads:
+        ws, wsb = _workspace(workspace, H, y.device)
+    lib = _lib.load()
+    with torch.cuda.device(y.device):
+        st = lib.ln_backward_from_output(dyv.data_ptr(), lddy, yv.data_ptr(), ldy, rstd.data_ptr(), _ptr(gamma),
+                                         _ptr(beta), ov.data_ptr(), lddx, _ptr(dgamma), _ptr(dbeta), _ptr(ws), wsb,
+                                         N, H, xc, wc, _stream(y.device))
+    _lib.check("ln_backward_from_output", st)
+    return out, dgamma, dbeta
+
+
+def rms_backward_from_output(dy, y, rstd, gamma=None, *, need_param_grads: bool = True, workspace=None, dx=None,
+                             param_dtype=None):
+    """RMSNorm backward from the forward's output y (x_hat = y/gamma) and saved
+    rstd.  Returns (dx, dgamma)."""
+    dyv, N, H, lddy = _rows(dy, "dy")
+    yv, Ny, Hy, ldy = _rows(y, "y")
+    if (Ny, Hy) != (N, H) or dy.dtype != y.dtype:
+        raise ValueError("dy must match y")
+    xc = _dtype_code(y, "y")
+    gamma = _vec(gamma, H, "gamma")
+    wdt = gamma.dtype if gamma is not None else (param_dtype or y.dtype)
+    wc = _DT[wdt]
+    out = torch.empty_like(y, memory_format=torch.contiguous_format) if dx is None else dx
+    ov, _, _, lddx = _rows(out, "dx")
+    dgamma = torch.empty(H, device=y.device, dtype=wdt) if need_param_grads else None
+    ws, wsb = (None, 0)
+    if need_param_grads:
+        ws, wsb = _workspace(workspace, H, y.device)
+    lib = _lib.load()
+    with torch.cuda.device(y.device):
+        st = lib.rms_backward_from_output(dyv.data_ptr(), lddy, yv.data_ptr(), ldy, rstd.data_ptr(), _ptr(gamma),
+                                          ov.data_ptr(), lddx, _ptr(dgamma), _ptr(ws), wsb, N, H, xc, wc,
+                                          _stream(y.device))
+    _lib.check("rms_backward_from_output", st)
+    return out, dgamma

@@ -38,7 +38,8 @@ def declared_functions():
 def test_header_declares_the_five_ops():
     names = set(declared_functions())
     for op in ["ln_forward", "rms_forward", "fused_add_rms_forward", "ln_backward", "rms_backward",
-               "fused_add_rms_backward", "norm_bwd_workspace_bytes", "norm_status_str"]:
+               "fused_add_rms_backward", "ln_backward_from_output", "rms_backward_from_output",
+               "norm_bwd_workspace_bytes", "norm_status_str"]:
         assert op in names
 
 
@@ -153,6 +154,29 @@ def test_fused_backward_validation(lib):
     assert _fbwd(lib, dres=A + 2, lddres=64) == INVALID     # dres partly over dy
     assert _fbwd(lib, dres=0x500000, lddres=10) == INVALID  # short dres stride
     assert _fbwd(lib, dh=0x500000, lddh=64, dres=0x500000 + 2, lddres=64) == INVALID  # dres partly over dh
+
+
+def test_from_output_validation(lib):
+    def ln(**kw):
+        a = dict(dy=A, lddy=64, y=B, ldy=64, rstd=C, g=None, b=None, dx=D, lddx=64, dg=None, db=None, ws=None,
+                 wsb=0, N=4, H=64, xd=BF16, wd=BF16)
+        a.update(kw)
+        return lib.ln_backward_from_output(a["dy"], a["lddy"], a["y"], a["ldy"], a["rstd"], a["g"], a["b"], a["dx"],
+                                           a["lddx"], a["dg"], a["db"], a["ws"], a["wsb"], a["N"], a["H"], a["xd"],
+                                           a["wd"], None)
+    assert ln(wd=9) == UNSUPPORTED
+    assert ln(xd=F32, wd=BF16) == UNSUPPORTED
+    assert ln(rstd=None) == INVALID
+    assert ln(y=None) == INVALID
+    assert ln(dx=B) == INVALID          # dx over y
+    assert ln(dx=A + 2) == INVALID      # dx partly over dy
+    assert ln(ldy=10) == INVALID
+    assert ln(H=0) == INVALID
+    assert ln(dg=0x500000, db=0x500000 + 4) == INVALID
+    assert lib.rms_backward_from_output(A, 64, B, 64, None, None, D, 64, None, None, 0, 4, 64, BF16, BF16,
+                                        None) == INVALID
+    assert lib.rms_backward_from_output(A, 64, B, 64, C, None, B + 8, 64, None, None, 0, 4, 64, BF16, BF16,
+                                        None) == INVALID
 
 
 def test_selftest_limit_validation(lib):
