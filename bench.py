@@ -48,9 +48,9 @@ METRIC = "LN/RMSNorm fwd+bwd achieved HBM GB/s and % of GB300 peak; bwd µs per 
 OPS = ("ln_fwd", "ln_bwd", "rms_fwd", "rms_bwd", "fused_fwd")
 # Measured by --sweep / --profile-op, not part of the step: the fused-add
 # backward (dx and dres from the stored h, plus the residual-stream gradient).
-EXTRA_OPS = ("fused_bwd", "ln_bwd_y", "rms_bwd_y")
+EXTRA_OPS = ("fused_bwd", "ln_bwd_y", "rms_bwd_y", "fused_fwd_ip")
 LAUNCHES = {"ln_fwd": 1, "rms_fwd": 1, "fused_fwd": 1, "ln_bwd": 2, "rms_bwd": 2, "fused_bwd": 2, "ln_bwd_y": 2,
-            "rms_bwd_y": 2}
+            "rms_bwd_y": 2, "fused_fwd_ip": 1}
 
 
 def alg_bytes(op: str, N: int, H: int, e: int = 2, ew: int = 2) -> int:
@@ -64,6 +64,8 @@ def alg_bytes(op: str, N: int, H: int, e: int = 2, ew: int = 2) -> int:
         "rms_bwd": 3 * nh + 4 * N + H * ew + H * ew,
         # reads dy, h, the stream gradient; writes dx and dres
         "fused_bwd": 5 * nh + 4 * N + H * ew + H * ew,
+        # the fused add updating the residual stream in place (h_out = x)
+        "fused_fwd_ip": 4 * nh + H * ew + 4 * N,
         # from the saved output: reads dy, y, rstd, gamma (and beta)
         "ln_bwd_y": 3 * nh + 4 * N + 2 * H * ew + 2 * H * ew,
         "rms_bwd_y": 3 * nh + 4 * N + H * ew + H * ew,
@@ -231,6 +233,10 @@ class Shape:
             st = L.rms_backward_from_output(t["dy"].data_ptr(), H, self.yr.data_ptr(), H, self.rstd_r.data_ptr(),
                                             t["gamma"].data_ptr(), self.dxf.data_ptr(), H, self.dgr.data_ptr(),
                                             self.ws.data_ptr(), self.wsb, N, H, BF, BF, stream)
+        elif op == "fused_fwd_ip":
+            st = L.fused_add_rms_forward(t["x"].data_ptr(), H, t["residual"].data_ptr(), H, t["gamma"].data_ptr(),
+                                         self.yf.data_ptr(), H, t["x"].data_ptr(), H, self.rstd_f.data_ptr(), N, H,
+                                         EPS_FUSED, BF, BF, stream)
         elif op == "fused_bwd":
             st = L.fused_add_rms_backward(t["dy"].data_ptr(), H, self.h.data_ptr(), H, self.rstd_f.data_ptr(),
                                           t["gamma"].data_ptr(), t["dh_stream"].data_ptr(), H, self.dxf.data_ptr(),
@@ -459,11 +465,11 @@ def oracle_step(samples):
         O.fused_add_rms_norm_forward(x, res, g, EPS_FUSED, "bfloat16")
 
 
-def oracle_samples(rows):
+def oracle_samples(rows, seed=0):
     from rmsnorm_ln_fwd_gb300 import synth
     out = []
     for i, (N, H) in enumerate(SHAPES):
-        c = synth.norm_inputs(rows, H, "bf16", seed=i, with_residual=True)
+        c = synth.norm_inputs(rows, H, "bf16", seed=seed * len(SHAPES) + i, with_residual=True)
         f = {k: v.double().numpy() for k, v in c.items()}
         out.append((f["x"], f["dy"], f["residual"], f["gamma"], f["beta"]))
     return out
@@ -473,10 +479,9 @@ def sample_bytes(rows):
     return sum(alg_bytes(op, rows, H) for _, H in SHAPES for op in OPS)
 
 
-def cpu_baseline(args, target_s=None):
-    target_s = args.cpu_seconds if target_s is None else target_s
-    rows = args.cpu_rows
-    samples = oracle_samples(rows)
+def _cpu_worker(rows, target_s, seed):
+    """Repeat the oracle over one row sample for target_s seconds -> (reps, s)."""
+    samples = oracle_samples(rows, seed)
     t0 = time.perf_counter()
     reps = 0
     while True:
@@ -484,11 +489,27 @@ def cpu_baseline(args, target_s=None):
         reps += 1
         if time.perf_counter() - t0 >= target_s:
             break
-    dt = time.perf_counter() - t0
-    gbs = reps * sample_bytes(rows) / dt / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{rows} of 8192 rows per width, all 10 calls, {reps} repetitions, {dt:.1f} s, "
-                      f"numpy fp64 single-threaded"}
+    return reps, time.perf_counter() - t0
+
+
+def cpu_baseline(args, target_s=None):
+    """The oracle as it stands, on one core and then on every host core (one
+    process per core, each on its own row sample; spawned, never forked after
+    CUDA is up).  The JSON value is the all-core figure."""
+    import multiprocessing as mp
+    target_s = args.cpu_seconds if target_s is None else target_s
+    rows = args.cpu_rows
+    reps, dt = _cpu_worker(rows, target_s, 0)
+    single = reps * sample_bytes(rows) / dt / 1e9
+    cores = os.cpu_count() or 1
+    with mp.get_context("spawn").Pool(cores) as pool:
+        res = pool.starmap(_cpu_worker, [(rows, target_s, i) for i in range(cores)])
+    multi = sum(r / t for r, t in res) * sample_bytes(rows) / 1e9
+    return {"value": round(multi, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} of 8192 rows per width, all 10 calls, repeated for {target_s:.0f} s in each of "
+                      f"{cores} processes (one per core, own sample each); numpy fp64",
+            "single_core": {"value": round(single, 4), "unit": "GB/s", "cores": 1,
+                            "sample": f"the same loop in one process: {reps} repetitions in {dt:.1f} s"}}
 
 
 def run_reference(args):
@@ -526,7 +547,9 @@ SWEEP = [("ln_fwd", 8192, 1024), ("rms_fwd", 8192, 1024), ("ln_bwd", 8192, 1024)
          ("rms_bwd", 16384, 2048), ("ln_fwd", 2048, 16384), ("rms_fwd", 2048, 16384), ("ln_bwd", 2048, 16384),
          ("rms_bwd", 2048, 16384), ("ln_fwd", 512, 16384), ("rms_fwd", 512, 16384), ("ln_bwd", 512, 16384),
          ("rms_bwd", 512, 16384), ("fused_bwd", 8192, 1024), ("fused_bwd", 8192, 5120), ("fused_bwd", 16384, 4096),
-         ("ln_bwd_y", 8192, 1024), ("ln_bwd_y", 8192, 5120), ("rms_bwd_y", 8192, 1024), ("rms_bwd_y", 8192, 5120)]
+         ("ln_bwd_y", 8192, 1024), ("ln_bwd_y", 8192, 5120), ("rms_bwd_y", 8192, 1024), ("rms_bwd_y", 8192, 5120),
+         # in place over x (last: it rewrites the shape's x on every call)
+         ("fused_fwd_ip", 16384, 4096)]
 
 FORWARD_OF = {"ln_bwd": "ln_fwd", "rms_bwd": "rms_fwd", "fused_bwd": "fused_fwd", "ln_bwd_y": "ln_fwd",
               "rms_bwd_y": "rms_fwd"}
