@@ -307,6 +307,14 @@ constexpr unsigned kErrWaitTimeout = 1u;
 constexpr unsigned kErrBadCopy = 2u;  // a bulk copy failed its bounds check and was skipped
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
+// The register-row LayerNorm/RMSNorm forward keeps the next row's loads in
+// registers; beyond that, the row this many strides ahead is requested into
+// L2 by one bulk prefetch per row group (0: off).
+#ifndef NORM_L2_PREFETCH_ROWS
+#define NORM_L2_PREFETCH_ROWS 2
+#endif
+constexpr int kL2PrefetchRows = NORM_L2_PREFETCH_ROWS;
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -372,6 +380,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
 
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
 // global to this CTA's shared memory; completion is counted on `bar`.
+// Ask L2 to start fetching `bytes` (a multiple of 16, 16-byte aligned source)
+// of global memory that a later load will want; nothing to wait for.
+__device__ __forceinline__ void l2_prefetch_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(

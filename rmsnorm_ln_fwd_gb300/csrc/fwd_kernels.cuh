@@ -121,8 +121,16 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
         if (v < nvec) st_vec(reinterpret_cast<T*>(hrow) + (t + v * tpr) * VEC, pack2<D>(f[v]));
       }
     }
-    // Issue the next row's loads before computing this one.
+    // Issue the next row's loads before computing this one.  LayerNorm and
+    // RMSNorm also ask L2 for a row further ahead (measured: it shortens the
+    // wide-row forward; the fused add, already near the HBM roof, and the
+    // backward, bound by the shared-memory pipe, lose with it).
     if (row + stride < a.N) fetch(row + stride);
+    if constexpr (kL2PrefetchRows > 1 && KIND != KIND_FUSED) {
+      const int64_t pr = row + kL2PrefetchRows * stride;
+      if (t == 0 && pr < a.N)
+        l2_prefetch_bulk(reinterpret_cast<const T*>(a.x) + pr * a.ldx, (uint32_t)(H * sizeof(T)));
+    }
 
     float rstd, mean_d = 0.f;
     if constexpr (KIND == KIND_LN) {
