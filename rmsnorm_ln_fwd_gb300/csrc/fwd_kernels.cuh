@@ -24,9 +24,9 @@
 //
 // Statistics ("Skill: Write CUDA LayerNorm Kernel", Required reasoning process
 // steps 2-5; "Skill: Write a Triton LayerNorm Kernel" steps 3-7):
-// LayerNorm: the register-row kernel holds the whole row, so it takes the
-// plain two-pass -- the row sum gives the mean, then the sum of squared
-// deviations from it gives M2 -- each a shuffle + shared-memory reduction.
+// LayerNorm: the register-row kernel holds the whole row and reduces the
+// shifted sums sum(d), sum(d^2) together, taking the exact second pass over
+// the registers only when the pivot sits far from the mean (see the kernel).
 // The kernels that stream the row keep a Welford triple (count, mean, M2) per
 // thread and merge triples across lanes and warps with the parallel merge.
 // M2 is divided by the full row length H.  Values are shifted by the row's
@@ -88,7 +88,16 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
 #pragma unroll
       for (int v = 0; v < VPT; ++v) nr[v] = load_vec_or_zero<D>(rrow, (t + v * tpr) * VEC, H);
     }
-    if constexpr (KIND == KIND_LN) npivot = load_elem<D>(xrow, 0);
+    if constexpr (KIND == KIND_LN) {
+      // The shift: the mean of the row's first 16-byte vector (one broadcast
+      // load), so that one outlying first element does not set it.
+      float f0[VEC];
+      unpack<D>(ld_cached(xrow), f0);
+      float sum0 = 0.f;
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) sum0 += f0[i];
+      npivot = sum0 * (1.f / VEC);
+    }
   };
 
   int parity = 0;
@@ -134,43 +143,53 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
 
     float rstd, mean_d = 0.f;
     if constexpr (KIND == KIND_LN) {
-      // The two-pass of the row, held in registers: the shifted sum gives the
-      // mean, then the squared deviations from it give M2 (no per-part counts
-      // or means to merge; both sums are plain group reductions).
+      // Shifted sums of the row held in registers: with d = x - x0,
+      // M2 = sum(d^2) - mean(d)*sum(d) in one reduction.  Its rounding error is
+      // about eps_f32 * (M2 + H*mean(d)^2); while mean(d)^2 <= 4*M2/H (the
+      // pivot within two standard deviations of the mean) that stays at the
+      // fp32 noise of M2 itself.  Otherwise the row takes the exact second
+      // pass, sum((d - mean(d))^2), a second reduction.  Every thread holds
+      // the same reduced values, so the branch is uniform.
       const float2 pv = splat2(pivot);
-      float2 s2 = splat2(0.f);
+      float2 s2 = splat2(0.f), q2 = splat2(0.f);
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
         if (v < nvec) {
 #pragma unroll
           for (int p = 0; p < VP; ++p) f[v][p] = sub2(f[v][p], pv);
           float2 vs = f[v][0];
-#pragma unroll
-          for (int p = 1; p < VP; ++p) vs = add2(vs, f[v][p]);
-          s2 = add2(s2, vs);
-        }
-      }
-      float sm[1] = {s2.x + s2.y};
-      group_sum<1>(sm, sh, nw, wig, lane, bar_id, parity);
-      mean_d = sm[0] * inv_h;
-      const float2 ml = splat2(mean_d);
-      float2 q2 = splat2(0.f);
-#pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        if (v < nvec) {
-          float2 e = sub2(f[v][0], ml);
-          float2 vq = mul2(e, e);
+          float2 vq = mul2(f[v][0], f[v][0]);
 #pragma unroll
           for (int p = 1; p < VP; ++p) {
-            e = sub2(f[v][p], ml);
-            vq = fma2(e, e, vq);
+            vs = add2(vs, f[v][p]);
+            vq = fma2(f[v][p], f[v][p], vq);
           }
+          s2 = add2(s2, vs);
           q2 = add2(q2, vq);
         }
       }
-      float m2[1] = {q2.x + q2.y};
-      group_sum<1>(m2, sh + 2 * nw, nw, wig, lane, bar_id, parity);
-      rstd = rsqrtf(m2[0] * inv_h + a.eps);
+      float sq[2] = {s2.x + s2.y, q2.x + q2.y};
+      group_sum<2>(sq, sh, nw, wig, lane, bar_id, parity);
+      mean_d = sq[0] * inv_h;
+      float m2 = fmaf(-mean_d, sq[0], sq[1]);
+      if (mean_d * mean_d * (float)H > 4.f * m2) {
+        const float2 ml = splat2(mean_d);
+        float2 e2 = splat2(0.f);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          if (v < nvec) {
+#pragma unroll
+            for (int p = 0; p < VP; ++p) {
+              const float2 e = sub2(f[v][p], ml);
+              e2 = fma2(e, e, e2);
+            }
+          }
+        }
+        float mm[1] = {e2.x + e2.y};
+        group_sum<1>(mm, sh + 4 * nw, nw, wig, lane, bar_id, parity);
+        m2 = mm[0];
+      }
+      rstd = rsqrtf(fmaxf(m2, 0.f) * inv_h + a.eps);
     } else {
       float2 s2 = splat2(0.f);
 #pragma unroll

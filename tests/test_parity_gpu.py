@@ -207,6 +207,37 @@ def test_f16_output_overflow(H):
         assert np.all(err <= 2.0 * np.abs(ref[fin]) * 2.0 ** -11 + 1e-3), "finite outputs"
 
 
+@pytest.mark.parametrize("H", [64, 1024, 5120])
+@pytest.mark.parametrize("dt", [BF, F32], ids=["bf16", "f32"])
+def test_ln_pivot_far_from_mean(H, dt):
+    """Rows whose first element (the kernels' shift) sits far from the mean:
+    an outlier in column 0, or the whole row offset except column 0.  Both the
+    one-reduction statistics and the exact second pass get exercised."""
+    N, eps = 48, 1e-5
+    t = _inputs(N, H, dt, seed=91)
+    x = t["x"].clone()
+    x[0::3, 0] = 40.0               # outlier pivot
+    x[1::3, 1:] += 25.0             # pivot 25 below the rest of the row
+    y, mean, rstd = nl.ln_forward(x, t["gamma"], t["beta"], eps)
+    dx, dg, db = nl.ln_backward(t["dy"], x, mean, rstd, t["gamma"])
+    torch.cuda.synchronize()
+    xn, gn, bn, dyn = np64(x), np64(t["gamma"]), np64(t["beta"]), np64(t["dy"])
+    yr, mr, rr = O.layer_norm_forward(xn, gn, bn, eps)
+    dxr, dgr, dbr = O.layer_norm_backward(dyn, xn, gn, eps)
+    # The kernels sum x - s for a shift s taken from the row's first 16-byte
+    # vector; the fp32 rounding of the mean then scales with |s - mean| as
+    # well as with the spread, so that distance joins the error scale of y.
+    vec = 4 if dt == F32 else 8
+    far = np.max(np.abs(xn[:, :vec] - mr[:, None]), axis=1)
+    y_scale = ln_y_scale(xn, mr, rr, gn, bn) + (far * rr)[:, None] * np.abs(gn)[None, :]
+    check_out(np64(y), yr, y_scale, dt, "pivot y")
+    check_mean(np64(mean), mr, xn, "pivot mean")
+    check_rstd(np64(rstd), rr, "pivot rstd")
+    check_out(np64(dx), dxr, ln_dx_scale(dyn, xn, gn, eps), dt, "pivot dx")
+    check_param(np64(dg), dgr, dt, "pivot dgamma")
+    check_param(np64(db), dbr, dt, "pivot dbeta")
+
+
 @pytest.mark.parametrize("H", [1, 8, 1024, 5120, 40000])
 @pytest.mark.parametrize("dt", DTS, ids=DT_IDS)
 def test_zero_variance_rows(H, dt):
