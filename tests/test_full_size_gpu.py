@@ -1,0 +1,164 @@
+"""The measured configurations at their full sizes, in the launch configuration
+the benchmark times (the auto kernel choice), against the fp64 oracle.
+
+Row-local outputs (y, mean, rstd, dx) are checked on a sample of rows -- the
+first, the last and 30 drawn at random -- by running the oracle on those rows
+alone.  The parameter gradients sum over every row, so the oracle computes
+them at full size; the fused add's stored h is checked bit for bit everywhere.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import rmsnorm_ln_fwd_gb300 as nl
+from normtest import (DT_NAME, DT_ORACLE, check_mean, check_out, check_param, check_rstd, ln_dx_scale, ln_y_scale,
+                      np64, rms_dx_scale, rms_y_scale)
+from rmsnorm_ln_fwd_gb300 import synth
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+DEV = "cuda:0"
+BF, F32 = torch.bfloat16, torch.float32
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from rmsnorm_ln_fwd_gb300 import _build
+    _build.build()
+    nl.load_library()
+
+
+def _rows(N, seed):
+    r = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, N - 1], r.choice(N, size=min(30, N), replace=False)]))
+
+
+def _col_sums(dy, xhat):
+    """Full-size dgamma/dbeta in fp64, streamed over row blocks."""
+    dg = np.zeros(dy.shape[1])
+    db = np.zeros(dy.shape[1])
+    for i in range(0, dy.shape[0], 2048):
+        d = dy[i:i + 2048].astype(np.float64)
+        dg += (d * xhat(i, i + 2048)).sum(axis=0)
+        db += d.sum(axis=0)
+    return dg, db
+
+
+CONFIGS = [(8192, 1024, BF), (8192, 5120, BF), (32768, 1024, BF), (16384, 2048, BF), (2048, 16384, BF),
+           (512, 16384, BF), (8192, 1024, F32)]
+
+
+@pytest.mark.parametrize("N,H,dt", CONFIGS, ids=[f"{n}x{h}{DT_NAME[d]}" for n, h, d in CONFIGS])
+def test_ln_full_size(N, H, dt):
+    eps = 1e-5
+    c = synth.norm_inputs(N, H, DT_NAME[dt], seed=1)
+    t = {k: v.to(DEV) for k, v in c.items()}
+    y, mean, rstd = nl.ln_forward(t["x"], t["gamma"], t["beta"], eps)
+    dx, dg, db = nl.ln_backward(t["dy"], t["x"], mean, rstd, t["gamma"])
+    torch.cuda.synchronize()
+    rows = _rows(N, N + H)
+    x, dy = c["x"].double().numpy(), c["dy"].double().numpy()
+    g, b = c["gamma"].double().numpy(), c["beta"].double().numpy()
+    xs, dys = x[rows], dy[rows]
+    yr, mr, rr = O.layer_norm_forward(xs, g, b, eps)
+    dxr, _, _ = O.layer_norm_backward(dys, xs, g, eps)
+    what = f"ln {N}x{H}"
+    check_out(np64(y[rows]), yr, ln_y_scale(xs, mr, rr, g, b), dt, what + " y rows")
+    check_mean(np64(mean[rows]), mr, xs, what + " mean rows")
+    check_rstd(np64(rstd[rows]), rr, what + " rstd rows")
+    check_out(np64(dx[rows]), dxr, ln_dx_scale(dys, xs, g, eps), dt, what + " dx rows")
+    mean_all, var_all = O.two_pass_stats(x)
+    r_all = 1.0 / np.sqrt(var_all + eps)
+    dgr, dbr = _col_sums(dy, lambda i, j: (x[i:j] - mean_all[i:j, None]) * r_all[i:j, None])
+    check_param(np64(dg), dgr, dt, what + " dgamma")
+    check_param(np64(db), dbr, dt, what + " dbeta")
+
+
+@pytest.mark.parametrize("N,H,dt", CONFIGS, ids=[f"{n}x{h}{DT_NAME[d]}" for n, h, d in CONFIGS])
+def test_rms_full_size(N, H, dt):
+    eps = 1e-5
+    c = synth.norm_inputs(N, H, DT_NAME[dt], seed=2, with_beta=False)
+    t = {k: v.to(DEV) for k, v in c.items()}
+    y, rstd = nl.rms_forward(t["x"], t["gamma"], eps)
+    dx, dg = nl.rms_backward(t["dy"], t["x"], rstd, t["gamma"])
+    torch.cuda.synchronize()
+    rows = _rows(N, N + H + 1)
+    x, dy, g = c["x"].double().numpy(), c["dy"].double().numpy(), c["gamma"].double().numpy()
+    xs, dys = x[rows], dy[rows]
+    yr, rr = O.rms_norm_forward(xs, g, eps)
+    dxr, _ = O.rms_norm_backward(dys, xs, g, eps)
+    what = f"rms {N}x{H}"
+    check_out(np64(y[rows]), yr, rms_y_scale(xs, rr, g), dt, what + " y rows")
+    check_rstd(np64(rstd[rows]), rr, what + " rstd rows")
+    check_out(np64(dx[rows]), dxr, rms_dx_scale(dys, xs, g, eps), dt, what + " dx rows")
+    r_all = 1.0 / np.sqrt((x * x).mean(axis=1) + eps)
+    dgr, _ = _col_sums(dy, lambda i, j: x[i:j] * r_all[i:j, None])
+    check_param(np64(dg), dgr, dt, what + " dgamma")
+
+
+def test_fused_full_size_16384x4096():
+    N, H, eps = 16384, 4096, 1e-6
+    c = synth.norm_inputs(N, H, "bf16", seed=3, with_beta=False, with_dy=False, with_residual=True)
+    t = {k: v.to(DEV) for k, v in c.items()}
+    y, h, rstd = nl.fused_add_rms_forward(t["x"], t["residual"], t["gamma"], eps)
+    torch.cuda.synchronize()
+    x, res, g = c["x"].double().numpy(), c["residual"].double().numpy(), c["gamma"].double().numpy()
+    hn = np64(h)
+    for i in range(0, N, 2048):   # every element of the stored sum, bit for bit
+        want = O.round_to_dtype(O.round_to_float32(x[i:i + 2048] + res[i:i + 2048]), "bfloat16")
+        assert np.array_equal(hn[i:i + 2048], want), f"h rows {i}..: not bit-exact"
+    rows = _rows(N, 7)
+    yr, hr, rr = O.fused_add_rms_norm_forward(x[rows], res[rows], g, eps, DT_ORACLE[BF])
+    check_out(np64(y[rows]), yr, rms_y_scale(x[rows] + res[rows], rr, g), BF, "fused y rows")
+    check_rstd(np64(rstd[rows]), rr, "fused rstd rows")
+
+
+def test_fused_backward_full_size_16384x4096():
+    """The fused add's backward from the stored h (with the stream gradient)."""
+    N, H, eps = 16384, 4096, 1e-6
+    c = synth.norm_inputs(N, H, "bf16", seed=4, with_beta=False, with_residual=True, with_dh_stream=True)
+    t = {k: v.to(DEV) for k, v in c.items()}
+    _, h, _ = nl.fused_add_rms_forward(t["x"], t["residual"], t["gamma"], eps)
+    _, rstd_h = nl.rms_forward(h, t["gamma"], eps)   # rstd of the stored h
+    dx, dres, dg = nl.fused_add_rms_backward(t["dy"], h, rstd_h, t["gamma"], t["dh_stream"])
+    torch.cuda.synchronize()
+    x, res = c["x"].double().numpy(), c["residual"].double().numpy()
+    dy, dh, g = c["dy"].double().numpy(), c["dh_stream"].double().numpy(), c["gamma"].double().numpy()
+    rows = _rows(N, 9)
+    hs = O.round_to_dtype(O.round_to_float32(x[rows] + res[rows]), "bfloat16")
+    dhr, _ = O.fused_add_rms_norm_backward_from_h(dy[rows], hs, g, eps, dh[rows])
+    check_out(np64(dx[rows]), dhr, rms_dx_scale(dy[rows], hs, g, eps) + np.abs(dh[rows]), BF, "fused bwd dx rows")
+    assert torch.equal(dx, dres)
+
+    def h_hat(i, j):
+        hb = O.round_to_dtype(O.round_to_float32(x[i:j] + res[i:j]), "bfloat16")
+        return hb / np.sqrt((hb * hb).mean(axis=1, keepdims=True) + eps)
+    dgr, _ = _col_sums(dy, h_hat)
+    check_param(np64(dg), dgr, BF, "fused bwd dgamma")
+
+
+def test_ln_backward_from_output_full_size_8192x5120():
+    """The backward from the saved output at full size.  Its inputs y and
+    rstd are drawn from the generator (any y and positive rstd are valid
+    inputs), and both sides take the same values."""
+    N, H = 8192, 5120
+    c = synth.norm_inputs(N, H, "bf16", seed=5)
+    t = {k: v.to(DEV) for k, v in c.items()}
+    rstd = (0.5 + synth.normal((N,), 5, "residual").abs()).to(DEV)
+    dx, dg, db = nl.ln_backward_from_output(t["dy"], t["x"], rstd, t["gamma"], t["beta"])
+    torch.cuda.synchronize()
+    y, dy = c["x"].double().numpy(), c["dy"].double().numpy()
+    g, b, r = c["gamma"].double().numpy(), c["beta"].double().numpy(), np64(rstd)
+    rows = _rows(N, 11)
+    dxr, _, _ = O.layer_norm_backward_from_output(dy[rows], y[rows], r[rows], g, b)
+    xh = (y[rows] - b) / g
+    gg = dy[rows] * g
+    scale = r[rows, None] * (np.abs(gg) + np.abs(gg).mean(1, keepdims=True) +
+                             np.abs(xh) * np.abs(gg * xh).mean(1, keepdims=True))
+    check_out(np64(dx[rows]), dxr, scale, BF, "from-output dx rows")
+    dgr, dbr = _col_sums(dy, lambda i, j: (y[i:j] - b) / g)
+    check_param(np64(dg), dgr, BF, "from-output dgamma")
+    check_param(np64(db), dbr, BF, "from-output dbeta")
