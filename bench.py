@@ -325,6 +325,7 @@ def run_ours(args):
         mean_us = statistics.fmean(per_call[i]) * 1e3
         gbs = s.bytes[op] / (mean_us * 1e-6) / 1e9
         breakdown[f"{op}_{s.N}x{s.H}"] = {"us_median": round(us, 2), "us_mean": round(mean_us, 2),
+                                          "us_min": round(min(per_call[i]) * 1e3, 2),
                                           "gbs": round(gbs, 1), "frac": round(gbs / peak, 3),
                                           "bytes": s.bytes[op], "launches": LAUNCHES[op]}
     # the call with the largest share of the step
