@@ -2,7 +2,10 @@
 // dtype by norm_bwd_f32.cu, norm_bwd_bf16.cu and norm_bwd_f16.cu.
 //
 // Backward kernels: LayerNorm and RMSNorm grad_input plus the gamma/beta
-// gradients through a bounded fp32 partial reduction.
+// gradients through a bounded fp32 partial reduction; the same from the
+// forward's saved output (x_hat = (y - beta)/gamma); and the fused add's
+// backward from the stored sum h (KIND_FUSED: RMSNorm math on h, the gradient
+// arriving through h added, written to both inputs' gradients).
 //
 // Math ("Skill: Write CUDA LayerNorm Kernel", Required reasoning process
 // step 8; the RMSNorm form is derived from its forward):
@@ -17,10 +20,10 @@
 // reduction).
 //
 // Structure ("Rewrite Triton normalization backward kernel_1 (#499)",
-// Summary items 1-2): a fixed grid of P = 2 x SM-count CTAs grid-strides the
-// rows.  Each thread owns fixed columns, so its dgamma/dbeta accumulators stay
-// in fp32 registers across all rows it visits; at the end each CTA folds its
-// row groups into ONE partial row.  The partial buffer is therefore P x H,
+// Summary items 1-2): a fixed grid of at most P = 2 x SM-count CTAs
+// grid-strides the rows.  Each thread owns fixed columns, so its dgamma/dbeta
+// accumulators stay in fp32 (registers or shared memory) across all rows it
+// visits; at the end each CTA folds its row groups into ONE partial row.  The partial buffer is therefore P x H,
 // independent of N, and a second small kernel sums it column-wise, casting to
 // the parameter dtype once at the store.
 
@@ -33,7 +36,6 @@
 #include "staged.cuh"
 
 namespace normk {
-
 
 // Register-row backward.  Persistent row groups walk rows row, row + stride,
 // ...; the next row's x, dy and saved statistics are loaded while the current

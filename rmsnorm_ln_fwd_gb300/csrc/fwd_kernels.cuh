@@ -3,20 +3,22 @@
 //
 // Forward kernels: LayerNorm, RMSNorm and fused residual-add + RMSNorm.
 //
-// Three kernel families, tried in this order:
+// Three kernel families (launch_fwd_typed picks one per call: register rows
+// while a row needs at most 640 threads, then the bulk-copy pipeline, then
+// register rows up to 1024 threads, then the loop):
 //
-// * fwd_staged_kernel -- persistent, one CTA per SM; a producer warp streams
-//   rows through a shared-memory ring with bulk copies (see staged.cuh) and
-//   consumer row groups compute from shared memory.  Needs 16-byte aligned
-//   rows, H a multiple of the vector width and at least three stages of rows
-//   in shared memory.
 // * fwd_rows_kernel -- the row lives in registers.  A "row group" of `tpr`
 //   threads (one warp for narrow rows, up to 1024 threads for wide rows) owns
 //   one row at a time and prefetches its next; each thread holds VPT 16-byte
-//   vectors of it, so HBM is read exactly once and written exactly once.  Vector v of thread t covers
-//   columns [(v*tpr + t)*VEC, +VEC): consecutive threads touch consecutive
-//   16-byte chunks, so every warp-wide access is fully coalesced.  Needs
-//   16-byte aligned rows and H a multiple of the vector width.
+//   vectors of it, so HBM is read exactly once and written exactly once.
+//   Vector v of thread t covers columns [(v*tpr + t)*VEC, +VEC): consecutive
+//   threads touch consecutive 16-byte chunks, so every warp-wide access is
+//   fully coalesced.  Needs 16-byte aligned rows and H a multiple of the
+//   vector width.
+// * fwd_staged_kernel -- persistent, one CTA per SM; a producer warp streams
+//   rows through a shared-memory ring with bulk copies (see staged.cuh) and
+//   consumer row groups compute from shared memory.  Same alignment needs,
+//   and at least three stages of rows in shared memory.
 // * fwd_loop_kernel -- any H and any alignment: one CTA per row, a strided
 //   loop over the row, a statistics pass and an output pass (the second read
 //   mostly hits L2).  Per-thread statistics use Welford's recurrence.  The
@@ -29,9 +31,10 @@
 // the registers only when the pivot sits far from the mean (see the kernel).
 // The kernels that stream the row keep a Welford triple (count, mean, M2) per
 // thread and merge triples across lanes and warps with the parallel merge.
-// M2 is divided by the full row length H.  Values are shifted by the row's
-// first element before accumulating (x - x0 is exact when the two are close),
-// so rows with a large common offset keep full precision.
+// M2 is divided by the full row length H.  Values are shifted before
+// accumulating (by the mean of the row's first 16-byte vector in the register
+// kernel, by the first element in the others; x - s is exact when the two are
+// close), so rows with a large common offset keep full precision.
 // RMSNorm sums x^2.  rstd = rsqrt(var + eps): eps inside the square root.
 //
 // Fused add ("Skill: Write a Triton Fused Add+RMSNorm Kernel", steps 2-7):
