@@ -162,3 +162,35 @@ def test_ln_backward_from_output_full_size_8192x5120():
     dgr, dbr = _col_sums(dy, lambda i, j: (y[i:j] - b) / g)
     check_param(np64(dg), dgr, BF, "from-output dgamma")
     check_param(np64(db), dbr, BF, "from-output dbeta")
+
+
+def test_beyond_2pow31_elements():
+    """N*H just past 2^31 elements (bf16, H = 1024): row offsets need 64-bit
+    arithmetic.  The rows repeat a seeded 4096-row block, so the oracle works
+    on that block: sampled rows (the last ones among them) row by row, and the
+    parameter gradients as block sums weighted by how often each row occurs."""
+    H, B, eps = 1024, 4096, 1e-5
+    N = (1 << 31) // H + 3
+    c = synth.norm_inputs(B, H, "bf16", seed=6)
+    reps = (N + B - 1) // B
+    x = c["x"].to(DEV).repeat(reps, 1)[:N]
+    dy = c["dy"].to(DEV).repeat(reps, 1)[:N]
+    gamma, beta = c["gamma"].to(DEV), c["beta"].to(DEV)
+    y, mean, rstd = nl.ln_forward(x, gamma, beta, eps)
+    dx, dg, db = nl.ln_backward(dy, x, mean, rstd, gamma)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([[0, N - 1, N - 2, N - 3], np.random.default_rng(12).choice(N, 28)]))
+    idx = torch.as_tensor(rows, device=DEV)
+    xb, dyb = c["x"].double().numpy(), c["dy"].double().numpy()
+    g, b = c["gamma"].double().numpy(), c["beta"].double().numpy()
+    xs, dys = xb[rows % B], dyb[rows % B]
+    yr, mr, rr = O.layer_norm_forward(xs, g, b, eps)
+    dxr, _, _ = O.layer_norm_backward(dys, xs, g, eps)
+    check_out(np64(y.index_select(0, idx)), yr, ln_y_scale(xs, mr, rr, g, b), BF, "2^31 y rows")
+    check_rstd(np64(rstd.index_select(0, idx)), rr, "2^31 rstd rows")
+    check_out(np64(dx.index_select(0, idx)), dxr, ln_dx_scale(dys, xs, g, eps), BF, "2^31 dx rows")
+    count = np.full(B, N // B, dtype=np.float64)
+    count[:N % B] += 1
+    _, dgb, dbb = O.layer_norm_backward(dyb * count[:, None], xb, g, eps)
+    check_param(np64(dg), dgb, BF, "2^31 dgamma")
+    check_param(np64(db), dbb, BF, "2^31 dbeta")
