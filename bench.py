@@ -549,6 +549,9 @@ SWEEP = [("ln_fwd", 8192, 1024), ("rms_fwd", 8192, 1024), ("ln_bwd", 8192, 1024)
          ("rms_bwd", 2048, 16384), ("ln_fwd", 512, 16384), ("rms_fwd", 512, 16384), ("ln_bwd", 512, 16384),
          ("rms_bwd", 512, 16384), ("fused_bwd", 8192, 1024), ("fused_bwd", 8192, 5120), ("fused_bwd", 16384, 4096),
          ("ln_bwd_y", 8192, 1024), ("ln_bwd_y", 8192, 5120), ("rms_bwd_y", 8192, 1024), ("rms_bwd_y", 8192, 5120),
+         # the backward shapes "Rewrite Triton normalization backward kernel_1 (#499)" times (Results table)
+         ("ln_bwd", 1024, 8192), ("ln_bwd", 2048, 4096), ("ln_bwd", 16384, 1024), ("ln_bwd", 4096, 4096),
+         ("ln_bwd", 8192, 4096), ("rms_bwd", 4096, 4096), ("rms_bwd", 2048, 4096), ("rms_bwd", 16384, 1024),
          # in place over x (last: it rewrites the shape's x on every call)
          ("fused_fwd_ip", 16384, 4096)]
 

@@ -1,0 +1,83 @@
+"""The benchmark's own checks: the algorithmic byte counts against the
+formulas written out independently here, and (on a GPU) the JSON line's
+schema for both arms."""
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+@pytest.mark.parametrize("N,H,e,ew", [(8192, 1024, 2, 2), (8192, 5120, 2, 4), (64, 256, 4, 4), (3, 7, 2, 2)])
+def test_algorithmic_bytes(N, H, e, ew):
+    row = N * H * e   # one pass over a row tensor
+    want = {
+        "ln_fwd": 2 * row + 2 * H * ew + 8 * N,          # x in, y out, gamma+beta, mean+rstd
+        "rms_fwd": 2 * row + H * ew + 4 * N,             # x in, y out, gamma, rstd
+        "fused_fwd": 4 * row + H * ew + 4 * N,           # x, res in; h, y out; gamma; rstd
+        "ln_bwd": 3 * row + 3 * H * ew + 8 * N,          # x, dy in; dx out; gamma in; dgamma, dbeta out
+        "rms_bwd": 3 * row + 2 * H * ew + 4 * N,
+        "fused_bwd": 5 * row + 2 * H * ew + 4 * N,       # dy, h, stream grad in; dx, dres out
+        "ln_bwd_y": 3 * row + 4 * H * ew + 4 * N,        # y instead of x, beta read, no mean
+        "rms_bwd_y": 3 * row + 2 * H * ew + 4 * N,
+        "fused_fwd_ip": 4 * row + H * ew + 4 * N,
+    }
+    for op, v in want.items():
+        assert bench.alg_bytes(op, N, H, e, ew) == v, op
+    assert set(bench.LAUNCHES) >= set(bench.OPS) | set(bench.EXTRA_OPS)
+
+
+REQUIRED = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+            "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"}
+
+
+def _json_line(out):
+    lines = [ln for ln in out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, out[-2000:]
+    return json.loads(lines[0])
+
+
+@pytest.mark.gpu
+@pytest.mark.slow
+def test_bench_json_line():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "3", "--warmup", "3",
+                        "--e2e-steps", "1", "--cpu-seconds", "0.5", "--cpu-rows", "16"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert p.returncode == 0, p.stderr[-3000:]
+    j = _json_line(p.stdout)
+    assert REQUIRED <= set(j), REQUIRED - set(j)
+    assert j["value"] > 0 and j["ms_per_step"] > 0 and j["n_gpus"] == 1 and j["steps"] == 3 and j["warmup"] == 3
+    assert j["higher_is_better"] is True and j["vs_baseline"] is None and j["config"]["workload"]
+    r = j["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["achieved"] > 0 and r["peak"] > 0
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-2
+    c = j["cpu_baseline"]
+    assert c["kind"] == "oracle" and c["value"] > 0 and c["cores"] >= 1 and c["sample"]
+    e = j["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert j["gpu_launches"] > 0
+    assert "sm_mhz" in j["clocks"] and "reasons" in j["clocks"]
+
+
+@pytest.mark.gpu
+@pytest.mark.slow
+def test_reference_arm_json_line():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3", "--ref-rows", "8"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert p.returncode == 0, p.stderr[-3000:]
+    j = _json_line(p.stdout)
+    assert j["impl"] == "reference" and j["value"] > 0
+    assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["e2e"]["d2h_bytes_per_step"] == 0
+    assert j["cpu_baseline"]["kind"] == "oracle"
