@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
   // threads: dbeta stays in registers (they fit there without spilling;
   // measured, the shared-memory pipe is what bounds this kernel: 8192x5120
   // bf16 66.4 -> 60.1 us).
-  constexpr bool DB_REG = ACC_SMEM && KIND == KIND_LN && MAXT <= 640 && VEC == 8;
+  constexpr bool DB_REG = ACC_SMEM && KIND == KIND_LN && MAXT == 640 && VEC == 8;
   float2 acc_db[DB_REG ? VPT : 1][VP];
 #pragma unroll
   for (int v = 0; v < (DB_REG ? VPT : 1); ++v)
@@ -750,6 +750,16 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   } else {
     tpr = ((Hv + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32;
   }
+  // Half-precision rows needing more than 640 threads at 16 elements each
+  // (10240 < H <= 16384) take 32 elements a thread instead: up to 512
+  // threads and 128 registers rather than 1024 threads at 64, which spill
+  // (measured: 2048x16384 bf16 LN 101.9 -> 89.1 us, RMS 62.4 -> 49.2 us).
+  const int tpr4 = ((Hv + 3) / 4 + 31) / 32 * 32;
+  const bool wide4 = VEC == 8 && tpr > 640 && tpr4 <= 512;
+  if (wide4) {
+    vpt = 4;
+    tpr = tpr4;
+  }
   const int rpc_rows = tpr <= 256 ? 256 / tpr : 1;
   // group scratch | fp32 gamma (| 1/gamma | beta) | shared accumulators (one
   // row slot) or the fold buffer of several row slots
@@ -820,6 +830,8 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
           if constexpr (VPT_MAX >= 4) err = run_rows<KIND, D, 4, 256, 2>(a, threads, &P, p_cap, smem, dev, s);
           break;
       }
+    } else if (wide4) {
+      if constexpr (VEC == 8) err = run_rows<KIND, D, 4, 512, 1, true>(a, threads, &P, p_cap, smem, dev, s);
     } else if (threads <= 640) {
       err = run_rows<KIND, D, VPT_MAX, 640, 1, true>(a, threads, &P, p_cap, smem, dev, s);
     } else {
