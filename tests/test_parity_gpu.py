@@ -176,6 +176,44 @@ def test_stability_offset_rows_fp32():
     rms_case(8192, 1024, F32, x_offset=1000.0, x_scale=1e-2, seed=22)
 
 
+@pytest.mark.parametrize("where", ["random", "fixed"])
+@pytest.mark.parametrize("H", [1024, 5120, 16384])
+@pytest.mark.parametrize("dt", [BF, F16], ids=["bf16", "f16"])
+def test_ln_offset_outlier_rows(H, dt, where):
+    """Rows constant at 1000 but for one outlier of a few storage spacings
+    (|mean| * rstd above 1e3): the worst case for the saved fp32 mean's
+    rounding inside x_hat.  Half an fp32 ulp of the mean shifts every x_hat by
+    about 2e-4 here; through c2 = mean(g * x_hat) the shift reaches the
+    outlier's dx multiplied by its x_hat (about 70), beyond one bf16 ulp at
+    H = 5120 unless the backward removes it (the recentring).  dx elementwise
+    and dgamma/dbeta in relative RMS must meet the stated bounds."""
+    N, eps = 64, 1e-5
+    t = _inputs(N, H, dt, seed=41)
+    gen = torch.Generator().manual_seed(41)
+    spacing = 4.0 if dt == BF else 0.5  # storage spacing at 1000
+    x = torch.full((N, H), 1000.0)
+    cols = torch.randint(0, H, (N,), generator=gen) if where == "random" else torch.full((N,), H // 3)
+    k = torch.randint(1, 4, (N,), generator=gen).float()
+    sign = torch.where(torch.rand(N, generator=gen) < 0.5, -1.0, 1.0)
+    x[torch.arange(N), cols] = 1000.0 + 2.0 * spacing * k * sign
+    x = x.to(dt)
+    assert torch.equal(x.float()[torch.arange(N), cols], 1000.0 + 2.0 * spacing * k * sign), "values not exact"
+    x = x.to(DEV)
+    y, mean, rstd = nl.ln_forward(x, t["gamma"], t["beta"], eps)
+    dx, dg, db = nl.ln_backward(t["dy"], x, mean, rstd, t["gamma"])
+    torch.cuda.synchronize()
+    xn, gn, bn, dyn = np64(x), np64(t["gamma"]), np64(t["beta"]), np64(t["dy"])
+    yr, mr, rr = O.layer_norm_forward(xn, gn, bn, eps)
+    dxr, dgr, dbr = O.layer_norm_backward(dyn, xn, gn, eps)
+    assert np.all(np.abs(mr) * rr > 1e3), "rows are not offset enough to be a test"
+    check_out(np64(y), yr, ln_y_scale(xn, mr, rr, gn, bn), dt, "outlier y")
+    check_mean(np64(mean), mr, xn, "outlier mean")
+    check_rstd(np64(rstd), rr, "outlier rstd")
+    check_out(np64(dx), dxr, ln_dx_scale(dyn, xn, gn, eps), dt, "outlier dx")
+    check_param(np64(dg), dgr, dt, "outlier dgamma")
+    check_param(np64(db), dbr, dt, "outlier dbeta")
+
+
 @pytest.mark.parametrize("H", [1024, 5120, 1000])
 def test_f16_small_activations(H):
     """|x| ~ 1e-3 in fp16: x*x would underflow in fp16; the statistics are fp32."""
