@@ -742,13 +742,22 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   // thread with more warps (H <= 16384).
   const bool vec_ok = aligned && a.H % VEC == 0;
   const int Hv = a.H / VEC;
-  int vpt = VPT_MAX, tpr = 0;
-  if (Hv <= 32 * VPT_MAX) {
+  // fp32 rows take twice the registers an element: at 16 elements a thread
+  // the 640-thread kernels spill (fused 128 bytes, LayerNorm from the output
+  // 72).  Where the row fits 640 threads at 8 elements a thread (H <= 5120),
+  // fp32 rows take 8, except the plain RMSNorm backward, which barely spills
+  // and is faster at 16 (measured at 8192x5120: fused 188 -> 127 us, LN from
+  // the output 135 -> 92, LN 104 -> 90; RMS 4096x4096 32.8 -> 36.9 at 8).
+  constexpr int VPT_F32 = 2;
+  const bool f32_narrow = VEC == 4 && KIND != KIND_RMS && (Hv + VPT_F32 - 1) / VPT_F32 <= 640;
+  const int vmax = f32_narrow ? VPT_F32 : VPT_MAX;
+  int vpt = vmax, tpr = 0;
+  if (Hv <= 32 * vmax) {
     tpr = 32;
     vpt = 1;
     while (vpt * 32 < Hv) vpt *= 2;
   } else {
-    tpr = ((Hv + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32;
+    tpr = ((Hv + vmax - 1) / vmax + 31) / 32 * 32;
   }
   // Half-precision rows needing more than 640 threads at 16 elements each
   // (10240 < H <= 16384) take 32 elements a thread instead: up to 512
@@ -833,7 +842,11 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
     } else if (wide4) {
       if constexpr (VEC == 8) err = run_rows<KIND, D, 4, 512, 1, true>(a, threads, &P, p_cap, smem, dev, s);
     } else if (threads <= 640) {
-      err = run_rows<KIND, D, VPT_MAX, 640, 1, true>(a, threads, &P, p_cap, smem, dev, s);
+      if (vpt == VPT_F32 && VPT_MAX != VPT_F32) {
+        if constexpr (VEC == 4) err = run_rows<KIND, D, VPT_F32, 640, 1, true>(a, threads, &P, p_cap, smem, dev, s);
+      } else {
+        err = run_rows<KIND, D, VPT_MAX, 640, 1, true>(a, threads, &P, p_cap, smem, dev, s);
+      }
     } else {
       err = run_rows<KIND, D, VPT_MAX, 1024, 1, true>(a, threads, &P, p_cap, smem, dev, s);
     }
