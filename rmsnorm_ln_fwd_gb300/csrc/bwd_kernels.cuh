@@ -44,8 +44,35 @@ namespace normk {
 // false), or, when one CTA covers a whole row (so every column has exactly one
 // owner thread), in shared memory, updated by plain read-modify-write, which
 // frees the registers for wide rows.  Elementwise math uses f32x2.
-template <int KIND, typename D, int VPT, int MAXT, int MINB, bool ACC_SMEM>
-__global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
+//
+// CLUSTER: a thread-block cluster of two CTAs shares each row, CTA rank r
+// taking columns [r*H/2, (r+1)*H/2) with its accumulators in registers; the
+// two CTAs' row sums meet through distributed shared memory (one cluster
+// barrier a row), and cluster c writes partial row c.  Used for rows too wide
+// for one CTA's registers (10240 < H <= 16384).
+template <typename D>
+__device__ __forceinline__ BwdArgs half_row_view(BwdArgs a, int rank) {
+  using T = typename D::T;
+  const int64_t c0 = (int64_t)rank * (a.H / 2);
+  const size_t wes = a.w_f32 ? 4 : sizeof(T);
+  a.x = reinterpret_cast<const T*>(a.x) + c0;
+  a.dy = reinterpret_cast<const T*>(a.dy) + c0;
+  a.dx = reinterpret_cast<T*>(a.dx) + c0;
+  if (a.dh_in) a.dh_in = reinterpret_cast<const T*>(a.dh_in) + c0;
+  if (a.dres) a.dres = reinterpret_cast<T*>(a.dres) + c0;
+  if (a.gamma) a.gamma = reinterpret_cast<const unsigned char*>(a.gamma) + c0 * wes;
+  if (a.beta) a.beta = reinterpret_cast<const unsigned char*>(a.beta) + c0 * wes;
+  if (a.ws) a.ws += c0;
+  a.H /= 2;
+  return a;
+}
+
+// The body of bwd_rows_kernel: `a` describes this CTA's columns, `h_full`
+// is the row length the statistics divide by, `crank` the CTA's rank in its
+// cluster (0 without clusters).
+template <int KIND, typename D, int VPT, int MAXT, bool ACC_SMEM, bool CLUSTER>
+__device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int crank) {
+  static_assert(!(CLUSTER && ACC_SMEM), "cluster rows keep their accumulators in registers");
   using T = typename D::T;
   constexpr int VEC = D::VEC;
   constexpr int VP = VEC / 2;
@@ -61,13 +88,17 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
   const int nw = tpr >> 5;
   const int wig = t >> 5;
   const int lane = threadIdx.x & 31;
-  const int H = a.H;
+  const int H = a.H;  // this CTA's columns (half the row in a cluster)
   const int hv = H / VEC;
-  const float inv_h = 1.f / (float)H;
+  const float inv_h = 1.f / (float)h_full;
   const bool w_f32 = a.w_f32 != 0;
   float* sh = sh_dyn + slot * (2 * nw * NS);
   const int bar_id = 1 + slot;
-  const int64_t stride = (int64_t)gridDim.x * rpc;
+  // Partial rows: one a CTA, or one a cluster.
+  const int prow = CLUSTER ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+  const int nprow = CLUSTER ? (int)gridDim.x / 2 : (int)gridDim.x;
+  const int64_t stride = (int64_t)nprow * rpc;
+  __shared__ float xch[2][4];  // cluster exchange of the row sums, by parity
   int nvec = 0;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
@@ -106,7 +137,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
   };
 
   int parity = 0;
-  int64_t row = (int64_t)blockIdx.x * rpc + slot;
+  int64_t row = (int64_t)prow * rpc + slot;
   if (row < a.N) fetch(row);  // first row in flight while gamma is staged
 
   const int Hp = a.Hp;
@@ -210,6 +241,18 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
       S[0] = sgx.x + sgx.y;
     }
     group_sum<NS>(S, sh, nw, wig, lane, bar_id, parity);
+    if constexpr (CLUSTER) {
+      // The partner CTA's sums land in xch[parity] of this CTA and ours in
+      // its; both add the two in the same order, so both halves of the row
+      // use bit-identical statistics.
+      if (threadIdx.x == 0) {
+#pragma unroll
+        for (int k = 0; k < NS; ++k) st_cluster_f32(&xch[parity][k], crank ^ 1, S[k]);
+      }
+      cluster_sync_all();
+#pragma unroll
+      for (int k = 0; k < NS; ++k) S[k] = crank == 0 ? S[k] + xch[parity][k] : xch[parity][k] + S[k];
+    }
     // LayerNorm: mean(x_hat) is 0 exactly; its computed value s0 is the shift
     // left by the saved mean's rounding, removed from x_hat here.  (From the
     // output there is no saved mean: x_hat is taken as recovered.)
@@ -289,10 +332,11 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
     parity ^= 1;
   }
 
+  if constexpr (CLUSTER) cluster_sync_all();  // no CTA leaves while its partner may still write to it
   if (a.ws == nullptr) return;
-  // Fold the CTA's row groups into partial row blockIdx.x.
-  float* pg = a.ws + (size_t)blockIdx.x * Hp;
-  float* pb = a.ws + ((size_t)gridDim.x + blockIdx.x) * Hp;
+  // Fold the CTA's row groups into partial row prow.
+  float* pg = a.ws + (size_t)prow * Hp;
+  float* pb = a.ws + ((size_t)nprow + prow) * Hp;
   if constexpr (ACC_SMEM) {
     // Each thread owns its accumulator slots: copy them straight out.
 #pragma unroll
@@ -353,6 +397,17 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
   for (int k = threadIdx.x * 4; k < H; k += blockDim.x * 4) {
     *reinterpret_cast<float4*>(pg + k) = *reinterpret_cast<const float4*>(red_g + k);
     if (LN) *reinterpret_cast<float4*>(pb + k) = *reinterpret_cast<const float4*>(red_b + k);
+  }
+}
+
+template <int KIND, typename D, int VPT, int MAXT, int MINB, bool ACC_SMEM, bool CLUSTER = false>
+__global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
+  if constexpr (CLUSTER) {
+    const int crank = (int)cluster_ctarank();
+    const BwdArgs half = half_row_view<D>(a, crank);
+    bwd_rows_body<KIND, D, VPT, MAXT, ACC_SMEM, CLUSTER>(half, a.H, crank);
+  } else {
+    bwd_rows_body<KIND, D, VPT, MAXT, ACC_SMEM, CLUSTER>(a, a.H, 0);
   }
 }
 
@@ -681,6 +736,37 @@ __global__ void __launch_bounds__(256) bwd_param_reduce_kernel(const float* ws, 
 
 static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Two-CTA clusters a row: as many clusters as can be resident at once, at
+// most p_cap (one partial row each).
+template <int KIND, typename D, int VPT>
+static cudaError_t run_rows_cluster(const BwdArgs& a, int threads, int* P, int p_cap, size_t smem,
+                                    cudaStream_t s) {
+  auto kern = bwd_rows_kernel<KIND, D, VPT, 512, 1, false, true>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (unsigned)p_cap);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int resident = 0;
+  if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) resident = 1;
+  *P = std::max(1, std::min(p_cap, resident));
+  cfg.gridDim = dim3(2 * (unsigned)*P);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <int KIND, typename D, int VPT, int MAXT, int MINB, bool ACC_SMEM = false>
 static cudaError_t run_rows(const BwdArgs& a, int threads, int* P, int p_cap, size_t smem, const DeviceInfo& dev,
                             cudaStream_t s) {
@@ -764,8 +850,26 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   // threads and 128 registers rather than 1024 threads at 64, which spill
   // (measured: 2048x16384 bf16 LN 101.9 -> 89.1 us, RMS 62.4 -> 49.2 us).
   const int tpr4 = ((Hv + 3) / 4 + 31) / 32 * 32;
-  const bool wide4 = VEC == 8 && tpr > 640 && tpr4 <= 512;
-  if (wide4) {
+  // Rows past 640 threads at 16 elements a thread and up to 16384 wide: a
+  // cluster of two CTAs a row, each with half the columns at 16 elements a
+  // thread and its accumulators in registers, or, for half precision, one CTA
+  // at 32 elements a thread.  Measured (µs): fp32 takes the cluster (2048x16384
+  // LN 167.9 -> 108.5, RMS 145.4 -> 84.0; its single-CTA kernels spill); half
+  // precision takes it for the fused backward (4096x12288 141.8 -> 120.8) and
+  // the LayerNorm backward from the output (whose single-CTA shape does not fit
+  // shared memory: 4096x12288 fp16 926.7 on the loop -> 108.5), and for the
+  // LayerNorm backward past 14336 columns (2048x16384 71.7 -> 65.5, but
+  // 4096x12288 92.2 -> 101.9); the RMSNorm kinds stay on one CTA (2048x16384
+  // 46.1 vs 54.3).
+  const int tprc = ((Hv / 2 + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32;
+  const bool cluster_pref =
+      VEC == 4 || KIND == KIND_FUSED || KIND == KIND_LN_Y || (KIND == KIND_LN && a.H > 14336);
+  const bool cluster = cluster_pref && tpr > 640 && a.H % (2 * VEC) == 0 && tprc <= 512;
+  const bool wide4 = !cluster && VEC == 8 && tpr > 640 && tpr4 <= 512;
+  if (cluster) {
+    vpt = VPT_MAX;
+    tpr = tprc;
+  } else if (wide4) {
     vpt = 4;
     tpr = tpr4;
   }
@@ -839,6 +943,9 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
           if constexpr (VPT_MAX >= 4) err = run_rows<KIND, D, 4, 256, 2>(a, threads, &P, p_cap, smem, dev, s);
           break;
       }
+    } else if (cluster) {
+      const int cl_cap = (int)std::min<int64_t>(a.N, p_max);
+      err = run_rows_cluster<KIND, D, VPT_MAX>(a, threads, &P, cl_cap, smem, s);
     } else if (wide4) {
       if constexpr (VEC == 8) err = run_rows<KIND, D, 4, 512, 1, true>(a, threads, &P, p_cap, smem, dev, s);
     } else if (threads <= 640) {

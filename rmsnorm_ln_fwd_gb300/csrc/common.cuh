@@ -407,6 +407,26 @@ __device__ __forceinline__ void cta_rows(int64_t N, int c, int grid, int64_t& lo
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Thread-block clusters (sm_90+ PTX): this CTA's rank in its cluster, a
+// 32-bit store into the same shared-memory offset of another CTA of the
+// cluster, and the cluster-wide barrier (every thread of every CTA of the
+// cluster arrives; release/acquire order the distributed shared-memory stores
+// before it with the loads after it).
+__device__ __forceinline__ unsigned cluster_ctarank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f32(const float* local, unsigned rank, float v) {
+  unsigned remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // 16-byte shared memory access.
 __device__ __forceinline__ uint4 lds16(const void* p) {
   uint4 r;

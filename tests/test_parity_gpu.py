@@ -147,6 +147,35 @@ def test_row_counts(N, H, dt):
 
 
 # ---------------------------------------------------------------------------
+# two-CTA cluster rows of the backward (10240 < H <= 16384): row counts from
+# one to beyond the resident cluster count, fp32 rows at 12288 columns, fp32
+# parameters with half-precision rows (the parameter halves are offset by the
+# parameter element size), and 16376 columns: in bf16 the halves are not whole
+# 16-byte vectors (one CTA a row instead), in fp32 they are, with threads past
+# the end of each half
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N", [1, 3, 77, 500])
+@pytest.mark.parametrize("H,dt", [(16384, BF), (16384, F16), (16384, F32), (12288, F32)],
+                         ids=["16384bf16", "16384f16", "16384f32", "12288f32"])
+def test_cluster_rows(N, H, dt):
+    ln_case(N, H, dt, seed=N + H)
+    rms_case(N, H, dt, seed=N + H + 1)
+
+
+@pytest.mark.parametrize("dt", [BF, F16], ids=["bf16", "f16"])
+def test_cluster_rows_fp32_params(dt):
+    ln_case(40, 16384, dt, wdt=F32, seed=9)
+    rms_case(40, 16384, dt, wdt=F32, seed=10)
+
+
+@pytest.mark.parametrize("H,dt", [(16376, BF), (16376, F32)], ids=["bf16", "f32"])
+def test_wide_rows_without_whole_halves(H, dt):
+    ln_case(37, H, dt, seed=11)
+    rms_case(37, H, dt, seed=12)
+
+
+# ---------------------------------------------------------------------------
 # parameter variants
 # ---------------------------------------------------------------------------
 
