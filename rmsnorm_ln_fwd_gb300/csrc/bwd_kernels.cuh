@@ -241,18 +241,7 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
       S[0] = sgx.x + sgx.y;
     }
     group_sum<NS>(S, sh, nw, wig, lane, bar_id, parity);
-    if constexpr (CLUSTER) {
-      // The partner CTA's sums land in xch[parity] of this CTA and ours in
-      // its; both add the two in the same order, so both halves of the row
-      // use bit-identical statistics.
-      if (threadIdx.x == 0) {
-#pragma unroll
-        for (int k = 0; k < NS; ++k) st_cluster_f32(&xch[parity][k], crank ^ 1, S[k]);
-      }
-      cluster_sync_all();
-#pragma unroll
-      for (int k = 0; k < NS; ++k) S[k] = crank == 0 ? S[k] + xch[parity][k] : xch[parity][k] + S[k];
-    }
+    if constexpr (CLUSTER) cluster_pair_sum<NS>(S, xch[parity], crank);  // both halves: identical sums
     // LayerNorm: mean(x_hat) is 0 exactly; its computed value s0 is the shift
     // left by the saved mean's rounding, removed from x_hat here.  (From the
     // output there is no saved mean: x_hat is taken as recovered.)

@@ -427,6 +427,23 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Sum K row totals over the two CTAs of a cluster pair: thread 0 stores this
+// CTA's totals (held by every thread) into `slot` of the partner CTA, a
+// cluster barrier orders them, and every thread adds the partner's totals in
+// rank order, so both CTAs end with bit-identical sums.  `slot` is this CTA's
+// own buffer at the same shared-memory offset; callers alternate two slots by
+// row parity, which makes one barrier a row enough.
+template <int K>
+__device__ __forceinline__ void cluster_pair_sum(float (&v)[K], float* slot, int crank) {
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) st_cluster_f32(slot + k, crank ^ 1, v[k]);
+  }
+  cluster_sync_all();
+#pragma unroll
+  for (int k = 0; k < K; ++k) v[k] = crank == 0 ? v[k] + slot[k] : slot[k] + v[k];
+}
+
 // 16-byte shared memory access.
 __device__ __forceinline__ uint4 lds16(const void* p) {
   uint4 r;
