@@ -45,15 +45,15 @@ namespace normk {
 // owner thread), in shared memory, updated by plain read-modify-write, which
 // frees the registers for wide rows.  Elementwise math uses f32x2.
 //
-// CLUSTER: a thread-block cluster of two CTAs shares each row, CTA rank r
-// taking columns [r*H/2, (r+1)*H/2) with its accumulators in registers; the
-// two CTAs' row sums meet through distributed shared memory (one cluster
-// barrier a row), and cluster c writes partial row c.  Used for rows too wide
-// for one CTA's registers (10240 < H <= 16384).
+// CL > 1: a thread-block cluster of CL CTAs shares each row, CTA rank r
+// taking columns [r*H/CL, (r+1)*H/CL) with its accumulators in registers; the
+// CTAs' row sums meet through distributed shared memory (one cluster barrier
+// a row), and cluster c writes partial row c.  Used for rows too wide for one
+// CTA's registers (H > 10240).
 template <typename D>
-__device__ __forceinline__ BwdArgs half_row_view(BwdArgs a, int rank) {
+__device__ __forceinline__ BwdArgs part_row_view(BwdArgs a, int rank, int parts) {
   using T = typename D::T;
-  const int64_t c0 = (int64_t)rank * (a.H / 2);
+  const int64_t c0 = (int64_t)rank * (a.H / parts);
   const size_t wes = a.w_f32 ? 4 : sizeof(T);
   a.x = reinterpret_cast<const T*>(a.x) + c0;
   a.dy = reinterpret_cast<const T*>(a.dy) + c0;
@@ -63,16 +63,17 @@ __device__ __forceinline__ BwdArgs half_row_view(BwdArgs a, int rank) {
   if (a.gamma) a.gamma = reinterpret_cast<const unsigned char*>(a.gamma) + c0 * wes;
   if (a.beta) a.beta = reinterpret_cast<const unsigned char*>(a.beta) + c0 * wes;
   if (a.ws) a.ws += c0;
-  a.H /= 2;
+  a.H /= parts;
   return a;
 }
 
 // The body of bwd_rows_kernel: `a` describes this CTA's columns, `h_full`
 // is the row length the statistics divide by, `crank` the CTA's rank in its
 // cluster (0 without clusters).
-template <int KIND, typename D, int VPT, int MAXT, bool ACC_SMEM, bool CLUSTER>
+template <int KIND, typename D, int VPT, int MAXT, bool ACC_SMEM, int CL>
 __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int crank) {
-  static_assert(!(CLUSTER && ACC_SMEM), "cluster rows keep their accumulators in registers");
+  static_assert(!(CL > 1 && ACC_SMEM), "cluster rows keep their accumulators in registers");
+  constexpr bool CLUSTER = CL > 1;
   using T = typename D::T;
   constexpr int VEC = D::VEC;
   constexpr int VP = VEC / 2;
@@ -95,10 +96,10 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
   float* sh = sh_dyn + slot * (2 * nw * NS);
   const int bar_id = 1 + slot;
   // Partial rows: one a CTA, or one a cluster.
-  const int prow = CLUSTER ? (int)blockIdx.x / 2 : (int)blockIdx.x;
-  const int nprow = CLUSTER ? (int)gridDim.x / 2 : (int)gridDim.x;
+  const int prow = (int)blockIdx.x / CL;
+  const int nprow = (int)gridDim.x / CL;
   const int64_t stride = (int64_t)nprow * rpc;
-  __shared__ float xch[2][4];  // cluster exchange of the row sums, by parity
+  __shared__ float xch[2][CL * 4];  // cluster exchange of the row sums ([rank][value]), by parity
   int nvec = 0;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
@@ -241,7 +242,7 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
       S[0] = sgx.x + sgx.y;
     }
     group_sum<NS>(S, sh, nw, wig, lane, bar_id, parity);
-    if constexpr (CLUSTER) cluster_pair_sum<NS>(S, xch[parity], crank);  // both halves: identical sums
+    if constexpr (CLUSTER) cluster_group_sum<NS, CL>(S, xch[parity], crank);  // identical sums in every part
     // LayerNorm: mean(x_hat) is 0 exactly; its computed value s0 is the shift
     // left by the saved mean's rounding, removed from x_hat here.  (From the
     // output there is no saved mean: x_hat is taken as recovered.)
@@ -389,14 +390,14 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
   }
 }
 
-template <int KIND, typename D, int VPT, int MAXT, int MINB, bool ACC_SMEM, bool CLUSTER = false>
+template <int KIND, typename D, int VPT, int MAXT, int MINB, bool ACC_SMEM, int CL = 1>
 __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
-  if constexpr (CLUSTER) {
+  if constexpr (CL > 1) {
     const int crank = (int)cluster_ctarank();
-    const BwdArgs half = half_row_view<D>(a, crank);
-    bwd_rows_body<KIND, D, VPT, MAXT, ACC_SMEM, CLUSTER>(half, a.H, crank);
+    const BwdArgs part = part_row_view<D>(a, crank, CL);
+    bwd_rows_body<KIND, D, VPT, MAXT, ACC_SMEM, CL>(part, a.H, crank);
   } else {
-    bwd_rows_body<KIND, D, VPT, MAXT, ACC_SMEM, CLUSTER>(a, a.H, 0);
+    bwd_rows_body<KIND, D, VPT, MAXT, ACC_SMEM, CL>(a, a.H, 0);
   }
 }
 
@@ -725,24 +726,24 @@ __global__ void __launch_bounds__(256) bwd_param_reduce_kernel(const float* ws, 
 
 static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Two-CTA clusters a row: as many clusters as can be resident at once, at
+// Clusters of CL CTAs a row: as many clusters as can be resident at once, at
 // most p_cap (one partial row each).
-template <int KIND, typename D, int VPT>
+template <int KIND, typename D, int VPT, int CL>
 static cudaError_t run_rows_cluster(const BwdArgs& a, int threads, int* P, int p_cap, size_t smem,
                                     cudaStream_t s) {
-  auto kern = bwd_rows_kernel<KIND, D, VPT, 512, 1, false, true>;
+  auto kern = bwd_rows_kernel<KIND, D, VPT, 512, 1, false, CL>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (unsigned)p_cap);
+  cfg.gridDim = dim3(CL * (unsigned)p_cap);
   cfg.blockDim = dim3((unsigned)threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -750,7 +751,7 @@ static cudaError_t run_rows_cluster(const BwdArgs& a, int threads, int* P, int p
   int resident = 0;
   if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) resident = 1;
   *P = std::max(1, std::min(p_cap, resident));
-  cfg.gridDim = dim3(2 * (unsigned)*P);
+  cfg.gridDim = dim3(CL * (unsigned)*P);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -850,10 +851,22 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   // LayerNorm backward past 14336 columns (2048x16384 71.7 -> 65.5, but
   // 4096x12288 92.2 -> 101.9); the RMSNorm kinds stay on one CTA (2048x16384
   // 46.1 vs 54.3).
-  const int tprc = ((Hv / 2 + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32;
+  // Past 1024 threads a row (H > 16384 in half precision and fp32) every kind
+  // takes clusters of 4 or 8 CTAs, 512 threads a CTA at most: one CTA's
+  // registers and shared memory cannot hold such rows (the staged ring's
+  // stages no longer fit either, and the loop reads every row twice).
+  auto part_tpr = [&](int parts) { return ((Hv / parts + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32; };
   const bool cluster_pref =
       VEC == 4 || KIND == KIND_FUSED || KIND == KIND_LN_Y || (KIND == KIND_LN && a.H > 14336);
-  const bool cluster = cluster_pref && tpr > 640 && a.H % (2 * VEC) == 0 && tprc <= 512;
+  int cl = 1;
+  if (tpr > 640 && tpr <= 1024) {
+    if (cluster_pref && a.H % (2 * VEC) == 0 && part_tpr(2) <= 512) cl = 2;
+  } else if (tpr > 1024) {
+    for (int parts = 2; parts <= 8 && cl == 1; parts *= 2)
+      if (a.H % (parts * VEC) == 0 && part_tpr(parts) <= 512) cl = parts;
+  }
+  const bool cluster = cl > 1;
+  const int tprc = cluster ? part_tpr(cl) : 0;
   const bool wide4 = !cluster && VEC == 8 && tpr > 640 && tpr4 <= 512;
   if (cluster) {
     vpt = VPT_MAX;
@@ -934,7 +947,9 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
       }
     } else if (cluster) {
       const int cl_cap = (int)std::min<int64_t>(a.N, p_max);
-      err = run_rows_cluster<KIND, D, VPT_MAX>(a, threads, &P, cl_cap, smem, s);
+      if (cl == 2) err = run_rows_cluster<KIND, D, VPT_MAX, 2>(a, threads, &P, cl_cap, smem, s);
+      else if (cl == 4) err = run_rows_cluster<KIND, D, VPT_MAX, 4>(a, threads, &P, cl_cap, smem, s);
+      else err = run_rows_cluster<KIND, D, VPT_MAX, 8>(a, threads, &P, cl_cap, smem, s);
     } else if (wide4) {
       if constexpr (VEC == 8) err = run_rows<KIND, D, 4, 512, 1, true>(a, threads, &P, p_cap, smem, dev, s);
     } else if (threads <= 640) {

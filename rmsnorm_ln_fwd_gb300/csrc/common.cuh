@@ -427,21 +427,30 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Sum K row totals over the two CTAs of a cluster pair: thread 0 stores this
-// CTA's totals (held by every thread) into `slot` of the partner CTA, a
-// cluster barrier orders them, and every thread adds the partner's totals in
-// rank order, so both CTAs end with bit-identical sums.  `slot` is this CTA's
-// own buffer at the same shared-memory offset; callers alternate two slots by
-// row parity, which makes one barrier a row enough.
-template <int K>
-__device__ __forceinline__ void cluster_pair_sum(float (&v)[K], float* slot, int crank) {
+// Sum K row totals over the CL CTAs of a cluster: thread 0 of each CTA stores
+// its CTA's totals (held by every thread) into row `crank` of `slots` in every
+// CTA of the cluster, a cluster barrier orders the stores, and every thread
+// adds the CL rows in rank order, so all CTAs end with bit-identical sums.
+// `slots` is this CTA's [CL][4] buffer, at the same shared-memory offset in
+// every CTA; callers alternate two such buffers by row parity, which makes one
+// barrier a row enough.
+template <int K, int CL>
+__device__ __forceinline__ void cluster_group_sum(float (&v)[K], float* slots, int crank) {
+  static_assert(K <= 4, "four values a rank at most");
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int k = 0; k < K; ++k) st_cluster_f32(slot + k, crank ^ 1, v[k]);
+    for (int r = 0; r < CL; ++r)
+#pragma unroll
+      for (int k = 0; k < K; ++k) st_cluster_f32(slots + crank * 4 + k, (unsigned)r, v[k]);
   }
   cluster_sync_all();
 #pragma unroll
-  for (int k = 0; k < K; ++k) v[k] = crank == 0 ? v[k] + slot[k] : slot[k] + v[k];
+  for (int k = 0; k < K; ++k) {
+    float t = slots[k];
+#pragma unroll
+    for (int r = 1; r < CL; ++r) t += slots[r * 4 + k];
+    v[k] = t;
+  }
 }
 
 // 16-byte shared memory access.

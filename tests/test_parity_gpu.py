@@ -163,6 +163,15 @@ def test_cluster_rows(N, H, dt):
     rms_case(N, H, dt, seed=N + H + 1)
 
 
+@pytest.mark.parametrize("N", [1, 5, 40])
+@pytest.mark.parametrize("H,dt", [(24576, BF), (32768, BF), (65536, BF), (32768, F32)],
+                         ids=["24576bf16", "32768bf16", "65536bf16", "32768f32"])
+def test_cluster_rows_4_and_8(N, H, dt):
+    """Rows past 16384 columns: clusters of four or eight CTAs a row."""
+    ln_case(N, H, dt, seed=N + H)
+    rms_case(N, H, dt, seed=N + H + 1)
+
+
 @pytest.mark.parametrize("dt", [BF, F16], ids=["bf16", "f16"])
 def test_cluster_rows_fp32_params(dt):
     ln_case(40, 16384, dt, wdt=F32, seed=9)
