@@ -57,12 +57,38 @@ namespace normk {
 // of its next row are already in flight (software pipelining), so each warp
 // keeps two rows' worth of HBM reads outstanding.  Each row is unpacked once
 // into fp32 pairs and every elementwise step uses packed f32x2 instructions.
-template <int KIND, typename D, int VPT, int MAXT, int MINB>
-__global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
+//
+// CL > 1: a thread-block cluster of CL CTAs shares each row, CTA rank r taking
+// columns [r*H/CL, (r+1)*H/CL); the row sums meet through distributed shared
+// memory (one cluster barrier a row, two when the exact second pass runs).
+// Used only for rows that neither one CTA's registers nor the bulk-copy ring
+// can hold (measured: where one CTA still fits, it is faster).
+template <typename D>
+__device__ __forceinline__ FwdArgs part_row_view(FwdArgs a, int rank, int parts) {
+  using T = typename D::T;
+  const int64_t c0 = (int64_t)rank * (a.H / parts);
+  const size_t wes = a.w_f32 ? 4 : sizeof(T);
+  a.x = reinterpret_cast<const T*>(a.x) + c0;
+  a.y = reinterpret_cast<T*>(a.y) + c0;
+  if (a.res) a.res = reinterpret_cast<const T*>(a.res) + c0;
+  if (a.h) a.h = reinterpret_cast<T*>(a.h) + c0;
+  if (a.gamma) a.gamma = reinterpret_cast<const unsigned char*>(a.gamma) + c0 * wes;
+  if (a.beta) a.beta = reinterpret_cast<const unsigned char*>(a.beta) + c0 * wes;
+  a.H /= parts;
+  return a;
+}
+
+// The body of fwd_rows_kernel: `a` describes this CTA's columns, `af` the
+// whole row (its first vector sets the LayerNorm shift; its length is what
+// the statistics divide by), `crank` the CTA's rank in its cluster.
+template <int KIND, typename D, int VPT, int CL>
+__device__ __forceinline__ void fwd_rows_body(const FwdArgs& a, const FwdArgs& af, int crank) {
   using T = typename D::T;
   constexpr int VEC = D::VEC;
   constexpr int VP = VEC / 2;
+  constexpr bool CLUSTER = CL > 1;
   extern __shared__ __align__(16) float sh_dyn[];
+  __shared__ float xch[2][CL * 4];  // cluster exchange of the row sums ([rank][value]), by parity
   const int tpr = a.tpr;
   const int rpc = blockDim.x / tpr;
   const int slot = threadIdx.x / tpr;
@@ -70,13 +96,14 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
   const int nw = tpr >> 5;
   const int wig = t >> 5;
   const int lane = threadIdx.x & 31;
-  const int H = a.H;
+  const int H = a.H;  // this CTA's columns (a part of the row in a cluster)
   const int hv = H / VEC;
-  const float inv_h = 1.f / (float)H;
+  const float inv_h = 1.f / (float)af.H;
   const bool w_f32 = a.w_f32 != 0;
   float* sh = sh_dyn + slot * (2 * nw * 3);
   const int bar_id = 1 + slot;
-  const int64_t stride = (int64_t)gridDim.x * rpc;
+  const int prow = (int)blockIdx.x / CL;
+  const int64_t stride = (int64_t)(gridDim.x / CL) * rpc;
   int nvec = 0;  // vectors of each row this thread owns
 #pragma unroll
   for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
@@ -95,7 +122,7 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
       // The shift: the mean of the row's first 16-byte vector (one broadcast
       // load), so that one outlying first element does not set it.
       float f0[VEC];
-      unpack<D>(ld_cached(xrow), f0);
+      unpack<D>(ld_cached(reinterpret_cast<const T*>(af.x) + r * af.ldx), f0);
       float sum0 = 0.f;
 #pragma unroll
       for (int i = 0; i < VEC; ++i) sum0 += f0[i];
@@ -104,7 +131,7 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
   };
 
   int parity = 0;
-  int64_t row = (int64_t)blockIdx.x * rpc + slot;
+  int64_t row = (int64_t)prow * rpc + slot;
   if (row < a.N) fetch(row);  // first row in flight while the parameters are staged
 
   // gamma (and beta) as fp32, thread-interleaved, shared by the row slots.
@@ -173,9 +200,10 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
       }
       float sq[2] = {s2.x + s2.y, q2.x + q2.y};
       group_sum<2>(sq, sh, nw, wig, lane, bar_id, parity);
+      if constexpr (CLUSTER) cluster_group_sum<2, CL>(sq, xch[parity], crank);
       mean_d = sq[0] * inv_h;
       float m2 = fmaf(-mean_d, sq[0], sq[1]);
-      if (mean_d * mean_d * (float)H > 4.f * m2) {
+      if (mean_d * mean_d * (float)af.H > 4.f * m2) {
         const float2 ml = splat2(mean_d);
         float2 e2 = splat2(0.f);
 #pragma unroll
@@ -190,6 +218,7 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
         }
         float mm[1] = {e2.x + e2.y};
         group_sum<1>(mm, sh + 4 * nw, nw, wig, lane, bar_id, parity);
+        if constexpr (CLUSTER) cluster_group_sum<1, CL>(mm, xch[parity] + 2, crank);
         m2 = mm[0];
       }
       rstd = rsqrtf(fmaxf(m2, 0.f) * inv_h + a.eps);
@@ -206,9 +235,10 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
       }
       float ss[1] = {s2.x + s2.y};
       group_sum<1>(ss, sh, nw, wig, lane, bar_id, parity);
+      if constexpr (CLUSTER) cluster_group_sum<1, CL>(ss, xch[parity], crank);
       rstd = rsqrtf(ss[0] * inv_h + a.eps);
     }
-    if (t == 0) {
+    if (t == 0 && crank == 0) {
       if constexpr (KIND == KIND_LN) {
         if (a.mean) a.mean[row] = pivot + mean_d;
       }
@@ -237,6 +267,18 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
       }
     }
     parity ^= 1;
+  }
+  if constexpr (CLUSTER) cluster_sync_all();  // no CTA leaves while a partner may still write to it
+}
+
+template <int KIND, typename D, int VPT, int MAXT, int MINB, int CL = 1>
+__global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
+  if constexpr (CL > 1) {
+    const int crank = (int)cluster_ctarank();
+    const FwdArgs part = part_row_view<D>(a, crank, CL);
+    fwd_rows_body<KIND, D, VPT, CL>(part, a, crank);
+  } else {
+    fwd_rows_body<KIND, D, VPT, CL>(a, a, 0);
   }
 }
 
@@ -542,6 +584,36 @@ static cudaError_t run_rows(const FwdArgs& a, int threads, int rpc, size_t smem,
   return launch_rows(fwd_rows_kernel<KIND, D, VPT, 1024, 1>, a, threads, smem, dev, groups, s);
 }
 
+// Clusters of CL CTAs a row: as many clusters as can be resident at once, at
+// most one a row.
+template <int KIND, typename D, int VPT, int CL>
+static cudaError_t run_rows_cluster(const FwdArgs& a, int threads, size_t smem, cudaStream_t s) {
+  auto kern = fwd_rows_kernel<KIND, D, VPT, 512, 1, CL>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t want = std::max<int64_t>(1, std::min<int64_t>(a.N, 1 << 20));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL * (unsigned)want);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int resident = 0;
+  if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) resident = 1;
+  cfg.gridDim = dim3(CL * (unsigned)std::min<int64_t>(want, resident));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <int KIND, typename D, int VPT>
 static cudaError_t run_staged(const FwdArgs& a, const StageCfg& c, int64_t blocks, size_t smem, cudaStream_t s) {
   auto kern = fwd_staged_kernel<KIND, D, VPT>;
@@ -632,6 +704,22 @@ cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream_t s) {
       default:
         if constexpr (VPT_MAX >= 4) return run_rows<KIND, D, 4>(a, threads, rpc, smem, dev, s);
         break;
+    }
+  }
+  // Rows neither one CTA's registers and shared memory nor the bulk-copy ring
+  // can hold (H past about 16384): clusters of 2, 4 or 8 CTAs a row, at most
+  // 512 threads a part, before the loop, which reads each row twice.
+  if (vec_ok && dev.path != PATH_LOOP) {
+    for (int parts = 2; parts <= 8; parts *= 2) {
+      if (a.H % (parts * VEC) != 0) continue;
+      const int ptpr = ((Hv / parts + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32;
+      const size_t psmem = (((size_t)2 * (ptpr / 32) * 3 + 3) & ~(size_t)3) * sizeof(float) +
+                           (KIND == KIND_LN ? 2 : 1) * (size_t)VPT_MAX * VEC * ptpr * sizeof(float);
+      if (ptpr > 512 || psmem > (size_t)dev.max_smem_optin) continue;
+      a.tpr = ptpr;
+      if (parts == 2) return run_rows_cluster<KIND, D, VPT_MAX, 2>(a, ptpr, psmem, s);
+      if (parts == 4) return run_rows_cluster<KIND, D, VPT_MAX, 4>(a, ptpr, psmem, s);
+      return run_rows_cluster<KIND, D, VPT_MAX, 8>(a, ptpr, psmem, s);
     }
   }
   const int64_t blocks = std::min<int64_t>(a.N, (int64_t)dev.sm_count * 8);
