@@ -23,9 +23,11 @@
 // Summary items 1-2): a fixed grid of at most P = 2 x SM-count CTAs
 // grid-strides the rows.  Each thread owns fixed columns, so its dgamma/dbeta
 // accumulators stay in fp32 (registers or shared memory) across all rows it
-// visits; at the end each CTA folds its row groups into ONE partial row.  The partial buffer is therefore P x H,
-// independent of N, and a second small kernel sums it column-wise, casting to
-// the parameter dtype once at the store.
+// visits; at the end each CTA folds its row groups into ONE partial row (a
+// cluster of CTAs sharing wide rows writes one partial row between them).  The
+// partial buffer is therefore at most P x H, independent of N, and a second
+// small kernel sums it column-wise, casting to the parameter dtype once at the
+// store.
 
 #pragma once
 

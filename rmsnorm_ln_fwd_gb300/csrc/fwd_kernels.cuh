@@ -5,7 +5,8 @@
 //
 // Three kernel families (launch_fwd_typed picks one per call: register rows
 // while a row needs at most 640 threads, then the bulk-copy pipeline, then
-// register rows up to 1024 threads, then the loop):
+// register rows up to 1024 threads, then register rows shared by a cluster of
+// 2, 4 or 8 CTAs, then the loop):
 //
 // * fwd_rows_kernel -- the row lives in registers.  A "row group" of `tpr`
 //   threads (one warp for narrow rows, up to 1024 threads for wide rows) owns
