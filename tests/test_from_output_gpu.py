@@ -125,7 +125,7 @@ def test_from_output_without_affine(H, dt):
     rms_y_case(29, H, dt, seed=6, gamma=False)
 
 
-@pytest.mark.parametrize("H,dt", [(1024, BF), (1000, F16), (5120, BF)])
+@pytest.mark.parametrize("H,dt", [(1024, BF), (1000, F16), (5120, BF), (16384, BF), (32768, F16)])
 def test_from_output_fp32_params(H, dt):
     ln_y_case(29, H, dt, seed=7, wdt=F32)
     rms_y_case(29, H, dt, seed=8, wdt=F32)
@@ -157,7 +157,7 @@ def _strided(src, ld, offset=0):
 
 
 @pytest.mark.parametrize("H,ld,off,dt", [(1024, 1032, 0, BF), (1024, 1027, 0, BF), (1024, 1024, 1, BF),
-                                         (5120, 5123, 3, F16), (2048, 2049, 0, F32)])
+                                         (5120, 5123, 3, F16), (2048, 2049, 0, F32), (16384, 16392, 0, BF)])
 def test_from_output_strides_and_alignment(H, ld, off, dt):
     N = 29
     t = _inputs(N, H, dt, 13)

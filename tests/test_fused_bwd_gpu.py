@@ -117,7 +117,8 @@ def test_fused_bwd_without_stream_gradient(H, dt):
 
 
 @pytest.mark.parametrize("mode", ["separate", "none", "same"])
-@pytest.mark.parametrize("H,dt", [(1024, BF), (4096, BF), (1000, BF), (2048, F32), (7, F32)])
+@pytest.mark.parametrize("H,dt", [(1024, BF), (4096, BF), (1000, BF), (2048, F32), (7, F32), (16384, BF),
+                                  (32768, BF)])
 def test_fused_bwd_residual_grad_modes(mode, H, dt):
     fused_bwd_case(67, H, dt, residual_grad=mode)
 
@@ -167,7 +168,7 @@ def _strided(src, ld, offset=0):
 
 
 @pytest.mark.parametrize("H,ld,off,dt", [(1024, 1032, 0, BF), (1024, 1027, 0, BF), (1024, 1024, 1, BF),
-                                         (5120, 5123, 3, BF), (2048, 2049, 0, F32)])
+                                         (5120, 5123, 3, BF), (2048, 2049, 0, F32), (16384, 16392, 0, BF)])
 def test_fused_bwd_strides_and_alignment(H, ld, off, dt):
     N, eps = 67, 1e-6
     t = _inputs(N, H, dt, 3)

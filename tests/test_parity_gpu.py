@@ -350,7 +350,7 @@ def _strided(src, ld, offset=0):
 
 @pytest.mark.parametrize("dt", DTS, ids=DT_IDS)
 @pytest.mark.parametrize("H,ld,off", [(1024, 1032, 0), (1024, 1027, 0), (1024, 1024, 1), (5120, 5123, 3),
-                                      (96, 100, 2)])
+                                      (96, 100, 2), (16384, 16392, 0), (32768, 32776, 0)])
 def test_strides_and_alignment(H, ld, off, dt):
     N, eps = 29, 1e-5
     t = _inputs(N, H, dt, seed=41)
