@@ -877,7 +877,7 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
     vpt = 4;
     tpr = tpr4;
   }
-  const int rpc_rows = tpr <= 256 ? 256 / tpr : 1;
+  const int rpc_rows = tpr <= 256 && !cluster ? 256 / tpr : 1;  // a cluster part: one row at a time
   // group scratch | fp32 gamma (| 1/gamma | beta) | shared accumulators (one
   // row slot) or the fold buffer of several row slots
   const size_t rows_slots = (size_t)vpt * VEC * tpr;
@@ -939,7 +939,12 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
     const int threads = rpc * tpr;
     const int p_cap = (int)std::min<int64_t>((a.N + rpc - 1) / rpc, p_max);
     const size_t smem = rows_smem;
-    if (threads <= 256) {
+    if (cluster) {  // first: a cluster part may have 256 threads or fewer
+      const int cl_cap = (int)std::min<int64_t>(a.N, p_max);
+      if (cl == 2) err = run_rows_cluster<KIND, D, VPT_MAX, 2>(a, threads, &P, cl_cap, smem, s);
+      else if (cl == 4) err = run_rows_cluster<KIND, D, VPT_MAX, 4>(a, threads, &P, cl_cap, smem, s);
+      else err = run_rows_cluster<KIND, D, VPT_MAX, 8>(a, threads, &P, cl_cap, smem, s);
+    } else if (threads <= 256) {
       switch (vpt) {
         case 1: err = run_rows<KIND, D, 1, 256, 2>(a, threads, &P, p_cap, smem, dev, s); break;
         case 2: err = run_rows<KIND, D, 2, 256, 2>(a, threads, &P, p_cap, smem, dev, s); break;
@@ -947,11 +952,6 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
           if constexpr (VPT_MAX >= 4) err = run_rows<KIND, D, 4, 256, 2>(a, threads, &P, p_cap, smem, dev, s);
           break;
       }
-    } else if (cluster) {
-      const int cl_cap = (int)std::min<int64_t>(a.N, p_max);
-      if (cl == 2) err = run_rows_cluster<KIND, D, VPT_MAX, 2>(a, threads, &P, cl_cap, smem, s);
-      else if (cl == 4) err = run_rows_cluster<KIND, D, VPT_MAX, 4>(a, threads, &P, cl_cap, smem, s);
-      else err = run_rows_cluster<KIND, D, VPT_MAX, 8>(a, threads, &P, cl_cap, smem, s);
     } else if (wide4) {
       if constexpr (VEC == 8) err = run_rows<KIND, D, 4, 512, 1, true>(a, threads, &P, p_cap, smem, dev, s);
     } else if (threads <= 640) {
