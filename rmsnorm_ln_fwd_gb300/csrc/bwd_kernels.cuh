@@ -817,7 +817,7 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   cudaError_t err = cudaSuccess;
   bool done = false;
   // Register-row shape: narrow rows one warp each, wider rows 16 elements a
-  // thread with more warps (H <= 16384).
+  // thread with more warps, the widest rows shared by a cluster (below).
   const bool vec_ok = aligned && a.H % VEC == 0;
   const int Hv = a.H / VEC;
   // fp32 rows take twice the registers an element: at 16 elements a thread
