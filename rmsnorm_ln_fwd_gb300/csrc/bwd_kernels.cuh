@@ -860,8 +860,15 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   auto part_tpr = [&](int parts) { return ((Hv / parts + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32; };
   const bool cluster_pref =
       VEC == 4 || KIND == KIND_FUSED || KIND == KIND_LN_Y || (KIND == KIND_LN && a.H > 14336);
+  // fp32 rows of 5120 < H <= 10240 for the fused and from-the-output kinds,
+  // whose single-CTA kernels spill there: clusters with parts of 256 threads or
+  // fewer (measured, fp32 fused 2560x8192 109.6 -> 71.7 us, LN from the output
+  // 2048x10240 84.0 -> 65.5; LN and RMS from x gain nothing).
   int cl = 1;
-  if (tpr > 640 && tpr <= 1024) {
+  if (VEC == 4 && (KIND == KIND_FUSED || FROM_Y) && part_tpr(1) > 320 && part_tpr(1) <= 640) {
+    for (int parts = 2; parts <= 8 && cl == 1; parts *= 2)
+      if (a.H % (parts * VEC) == 0 && part_tpr(parts) <= 256) cl = parts;
+  } else if (tpr > 640 && tpr <= 1024) {
     if (cluster_pref && a.H % (2 * VEC) == 0 && part_tpr(2) <= 512) cl = 2;
   } else if (tpr > 1024) {
     for (int parts = 2; parts <= 8 && cl == 1; parts *= 2)
