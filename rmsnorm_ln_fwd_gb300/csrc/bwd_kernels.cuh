@@ -102,6 +102,8 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
   const int nprow = (int)gridDim.x / CL;
   const int64_t stride = (int64_t)nprow * rpc;
   __shared__ float xch[2][CL * 4];  // cluster exchange of the row sums ([rank][value]), by parity
+  __shared__ uint64_t xbar[2];      // their mbarriers, by parity
+  __shared__ int xabort;            // a bounded wait ran out: later waits give up at once
   int nvec = 0;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
@@ -175,6 +177,16 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
     }
   }
   __syncthreads();
+  unsigned it = 0;  // rows this CTA has exchanged (cluster rows)
+  if constexpr (CLUSTER) {
+    if (threadIdx.x == 0) {
+      mbar_init(&xbar[0], 1);
+      mbar_init(&xbar[1], 1);
+      xabort = 0;
+      fence_barrier_init();
+    }
+    cluster_sync_all();  // every CTA's mbarriers exist before any CTA sends to them
+  }
 
 
   for (; row < a.N; row += stride) {
@@ -244,7 +256,10 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
       S[0] = sgx.x + sgx.y;
     }
     group_sum<NS>(S, sh, nw, wig, lane, bar_id, parity);
-    if constexpr (CLUSTER) cluster_group_sum<NS, CL>(S, xch[parity], crank);  // identical sums in every part
+    if constexpr (CLUSTER) {  // identical sums in every part
+      cluster_group_sum_async<NS, CL>(S, xch[parity], &xbar[parity], (it >> 1) & 1u, crank, a.err, &xabort);
+      ++it;
+    }
     // LayerNorm: mean(x_hat) is 0 exactly; its computed value s0 is the shift
     // left by the saved mean's rounding, removed from x_hat here.  (From the
     // output there is no saved mean: x_hat is taken as recovered.)
@@ -805,6 +820,7 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
     return cudaSuccess;
   }
   if (!want) a.ws = nullptr;
+  a.err = dev.err;
   a.Hp = bwd_partial_stride(a.H);
   const int p_max = bwd_max_partials(dev);
   bool aligned = aligned16(a.x) && aligned16(a.dy) && aligned16(a.dx) && (a.ldx * es) % 16 == 0 &&

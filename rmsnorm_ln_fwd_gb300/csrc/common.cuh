@@ -453,6 +453,53 @@ __device__ __forceinline__ void cluster_group_sum(float (&v)[K], float* slots, i
   }
 }
 
+// Asynchronous 16-byte store into another CTA of the cluster: `local_dst` and
+// `local_bar` are this CTA's addresses of a buffer and an mbarrier at the same
+// offsets as the target's; the store counts 16 bytes on the target's
+// mbarrier when it lands.  No fence: the target's mbarrier wait orders it.
+__device__ __forceinline__ void st_async_cluster_v4(const float* local_dst, const uint64_t* local_bar,
+                                                    unsigned rank, float4 v) {
+  unsigned dst, bar;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst) : "r"(smem_u32(local_dst)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(bar) : "r"(smem_u32(local_bar)), "r"(rank));
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
+}
+
+// The row-sum exchange of cluster rows without a cluster barrier: thread 0
+// arms this CTA's mbarrier for the other CL-1 CTAs' 16-byte messages and sends
+// this CTA's totals (held by every thread) into row `crank` of `slots` in each
+// of them; every thread then waits (bounded) on its own mbarrier and adds the
+// CL rows in rank order, its own totals in place of row `crank`, so all CTAs
+// end with bit-identical sums.  `slots` ([CL][4] floats) and `bar` alternate
+// by row parity; `phase` is the use count of this `bar` modulo 2.  A CTA can
+// send its next row's totals only after receiving every CTA's totals of this
+// row, so a buffer is never rewritten before it has been read.
+template <int K, int CL>
+__device__ __forceinline__ bool cluster_group_sum_async(float (&v)[K], float* slots, uint64_t* bar, unsigned phase,
+                                                        int crank, unsigned* err, volatile int* abort) {
+  static_assert(K <= 4, "four values a rank at most");
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(bar, (uint32_t)((CL - 1) * 16));
+    const float4 m = make_float4(v[0], K > 1 ? v[K > 1 ? 1 : 0] : 0.f, K > 2 ? v[K > 2 ? 2 : 0] : 0.f,
+                                 K > 3 ? v[K > 3 ? 3 : 0] : 0.f);
+#pragma unroll
+    for (int r = 0; r < CL; ++r)
+      if (r != crank) st_async_cluster_v4(slots + crank * 4, bar, (unsigned)r, m);
+  }
+  const bool ok = mbar_wait(bar, phase, err, abort);
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    float t = 0.f;
+#pragma unroll
+    for (int r = 0; r < CL; ++r) t += r == crank ? v[k] : slots[r * 4 + k];
+    v[k] = t;
+  }
+  return ok;
+}
+
 // 16-byte shared memory access.
 __device__ __forceinline__ uint4 lds16(const void* p) {
   uint4 r;

@@ -77,7 +77,8 @@ struct BwdArgs {
   int64_t N;
   int H;
   int w_f32;
-  int tpr;  // threads per row (filled in by the launcher)
+  int tpr;        // threads per row (filled in by the launcher)
+  unsigned* err;  // device error flags (bounded waits of cluster rows; filled in by the launcher)
 };
 
 // Shape of a staged (bulk-copy pipelined) launch, chosen on the host.  The CTA
