@@ -861,21 +861,18 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   // Rows past 640 threads at 16 elements a thread and up to 16384 wide: a
   // cluster of two CTAs a row, each with half the columns at 16 elements a
   // thread and its accumulators in registers, or, for half precision, one CTA
-  // at 32 elements a thread.  Measured (µs): fp32 takes the cluster (2048x16384
-  // LN 167.9 -> 108.5, RMS 145.4 -> 84.0; its single-CTA kernels spill); half
-  // precision takes it for the fused backward (4096x12288 141.8 -> 120.8) and
-  // the LayerNorm backward from the output (whose single-CTA shape does not fit
-  // shared memory: 4096x12288 fp16 926.7 on the loop -> 108.5), and for the
-  // LayerNorm backward past 14336 columns (2048x16384 71.7 -> 65.5, but
-  // 4096x12288 92.2 -> 101.9); the RMSNorm kinds stay on one CTA (2048x16384
-  // 46.1 vs 54.3).
+  // at 32 elements a thread.  Measured (µs) with the asynchronous row-sum
+  // exchange: the cluster for every kind (bf16 LN 3413x12288 81.9 -> 69.6,
+  // 2048x16384 RMS 47.1 -> 43.0, RMS from the output 53.3 -> 45.1; fp32 2048x16384
+  // LN 167.9 -> 108.5 against a spilling single CTA; the LN backward from the
+  // output has no single-CTA shape that fits), except the half-precision RMSNorm
+  // backward up to 14336 columns (4096x10752 57.3 vs 63.5 with the cluster).
   // Past 1024 threads a row (H > 16384 in half precision and fp32) every kind
   // takes clusters of 4 or 8 CTAs, 512 threads a CTA at most: one CTA's
   // registers and shared memory cannot hold such rows (the staged ring's
   // stages no longer fit either, and the loop reads every row twice).
   auto part_tpr = [&](int parts) { return ((Hv / parts + VPT_MAX - 1) / VPT_MAX + 31) / 32 * 32; };
-  const bool cluster_pref =
-      VEC == 4 || KIND == KIND_FUSED || KIND == KIND_LN_Y || (KIND == KIND_LN && a.H > 14336);
+  const bool cluster_pref = !(KIND == KIND_RMS && VEC == 8 && a.H <= 14336);
   // fp32 rows of 5120 < H <= 10240 for the fused and from-the-output kinds,
   // whose single-CTA kernels spill there: clusters with parts of 256 threads or
   // fewer (measured, fp32 fused 2560x8192 109.6 -> 71.7 us, LN from the output
