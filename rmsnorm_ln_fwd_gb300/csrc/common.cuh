@@ -407,50 +407,17 @@ __device__ __forceinline__ void cta_rows(int64_t N, int c, int grid, int64_t& lo
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Thread-block clusters (sm_90+ PTX): this CTA's rank in its cluster, a
-// 32-bit store into the same shared-memory offset of another CTA of the
-// cluster, and the cluster-wide barrier (every thread of every CTA of the
-// cluster arrives; release/acquire order the distributed shared-memory stores
-// before it with the loads after it).
+// Thread-block clusters (sm_90+ PTX): this CTA's rank in its cluster, and the
+// cluster-wide barrier (every thread of every CTA of the cluster arrives;
+// release/acquire order memory operations before it with those after it).
 __device__ __forceinline__ unsigned cluster_ctarank() {
   unsigned r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void st_cluster_f32(const float* local, unsigned rank, float v) {
-  unsigned remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
-}
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Sum K row totals over the CL CTAs of a cluster: thread 0 of each CTA stores
-// its CTA's totals (held by every thread) into row `crank` of `slots` in every
-// CTA of the cluster, a cluster barrier orders the stores, and every thread
-// adds the CL rows in rank order, so all CTAs end with bit-identical sums.
-// `slots` is this CTA's [CL][4] buffer, at the same shared-memory offset in
-// every CTA; callers alternate two such buffers by row parity, which makes one
-// barrier a row enough.
-template <int K, int CL>
-__device__ __forceinline__ void cluster_group_sum(float (&v)[K], float* slots, int crank) {
-  static_assert(K <= 4, "four values a rank at most");
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int r = 0; r < CL; ++r)
-#pragma unroll
-      for (int k = 0; k < K; ++k) st_cluster_f32(slots + crank * 4 + k, (unsigned)r, v[k]);
-  }
-  cluster_sync_all();
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    float t = slots[k];
-#pragma unroll
-    for (int r = 1; r < CL; ++r) t += slots[r * 4 + k];
-    v[k] = t;
-  }
 }
 
 // Asynchronous 16-byte store into another CTA of the cluster: `local_dst` and

@@ -89,7 +89,10 @@ __device__ __forceinline__ void fwd_rows_body(const FwdArgs& a, const FwdArgs& a
   constexpr int VP = VEC / 2;
   constexpr bool CLUSTER = CL > 1;
   extern __shared__ __align__(16) float sh_dyn[];
-  __shared__ float xch[2][CL * 4];  // cluster exchange of the row sums ([rank][value]), by parity
+  __shared__ float xch[2][CL * 4];   // cluster exchange of the row sums ([rank][value]), by parity
+  __shared__ float xch2[2][CL * 4];  // the exact second pass's exchange, by its own parity
+  __shared__ uint64_t xbar[2], xbar2[2];
+  __shared__ int xabort;
   const int tpr = a.tpr;
   const int rpc = blockDim.x / tpr;
   const int slot = threadIdx.x / tpr;
@@ -143,6 +146,18 @@ __device__ __forceinline__ void fwd_rows_body(const FwdArgs& a, const FwdArgs& a
     if constexpr (KIND == KIND_LN) stage_params<D, VPT>(bs, a.beta, w_f32, 0.f, t, tpr, hv);
   }
   __syncthreads();
+  unsigned it = 0, it2 = 0;  // exchanges this CTA has made (cluster rows)
+  if constexpr (CLUSTER) {
+    if (threadIdx.x == 0) {
+      mbar_init(&xbar[0], 1);
+      mbar_init(&xbar[1], 1);
+      mbar_init(&xbar2[0], 1);
+      mbar_init(&xbar2[1], 1);
+      xabort = 0;
+      fence_barrier_init();
+    }
+    cluster_sync_all();  // every CTA's mbarriers exist before any CTA sends to them
+  }
 
   for (; row < a.N; row += stride) {
     // Unpack the current row (it arrived while the previous row computed).
@@ -201,7 +216,10 @@ __device__ __forceinline__ void fwd_rows_body(const FwdArgs& a, const FwdArgs& a
       }
       float sq[2] = {s2.x + s2.y, q2.x + q2.y};
       group_sum<2>(sq, sh, nw, wig, lane, bar_id, parity);
-      if constexpr (CLUSTER) cluster_group_sum<2, CL>(sq, xch[parity], crank);
+      if constexpr (CLUSTER) {
+        cluster_group_sum_async<2, CL>(sq, xch[it & 1], &xbar[it & 1], (it >> 1) & 1u, crank, a.err, &xabort);
+        ++it;
+      }
       mean_d = sq[0] * inv_h;
       float m2 = fmaf(-mean_d, sq[0], sq[1]);
       if (mean_d * mean_d * (float)af.H > 4.f * m2) {
@@ -219,7 +237,11 @@ __device__ __forceinline__ void fwd_rows_body(const FwdArgs& a, const FwdArgs& a
         }
         float mm[1] = {e2.x + e2.y};
         group_sum<1>(mm, sh + 4 * nw, nw, wig, lane, bar_id, parity);
-        if constexpr (CLUSTER) cluster_group_sum<1, CL>(mm, xch[parity] + 2, crank);
+        if constexpr (CLUSTER) {  // uniform across the cluster: every part holds the same sums
+          cluster_group_sum_async<1, CL>(mm, xch2[it2 & 1], &xbar2[it2 & 1], (it2 >> 1) & 1u, crank, a.err,
+                                         &xabort);
+          ++it2;
+        }
         m2 = mm[0];
       }
       rstd = rsqrtf(fmaxf(m2, 0.f) * inv_h + a.eps);
@@ -236,7 +258,10 @@ __device__ __forceinline__ void fwd_rows_body(const FwdArgs& a, const FwdArgs& a
       }
       float ss[1] = {s2.x + s2.y};
       group_sum<1>(ss, sh, nw, wig, lane, bar_id, parity);
-      if constexpr (CLUSTER) cluster_group_sum<1, CL>(ss, xch[parity], crank);
+      if constexpr (CLUSTER) {
+        cluster_group_sum_async<1, CL>(ss, xch[it & 1], &xbar[it & 1], (it >> 1) & 1u, crank, a.err, &xabort);
+        ++it;
+      }
       rstd = rsqrtf(ss[0] * inv_h + a.eps);
     }
     if (t == 0 && crank == 0) {
@@ -633,6 +658,7 @@ cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream_t s) {
   // flight; fp32 takes twice the registers per element).
   constexpr int VPT_MAX = (KIND != KIND_FUSED && VEC == 8) ? 4 : 16 / VEC;
   const size_t es = sizeof(T);
+  a.err = dev.err;
   bool aligned = aligned16(a.x) && aligned16(a.y) && (a.ldx * es) % 16 == 0 && (a.ldy * es) % 16 == 0;
   if (a.gamma) aligned = aligned && aligned16(a.gamma);
   if (a.beta) aligned = aligned && aligned16(a.beta);

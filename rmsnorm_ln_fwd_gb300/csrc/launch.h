@@ -49,6 +49,7 @@ struct FwdArgs {
   float eps;
   int w_f32;    // parameters are fp32 (else the row dtype)
   int tpr;      // threads per row (filled in by the launcher)
+  unsigned* err;  // device error flags (bounded waits of cluster rows; filled in by the launcher)
 };
 
 // Backward: LayerNorm (KIND_LN) or RMSNorm (KIND_RMS) from x and the saved
