@@ -120,6 +120,61 @@ def _rms_from_y_times_gamma():
     return f
 
 
+def _fused_normalises_rounded_h():
+    def f(x, residual, gamma=None, eps=1e-6, h_dtype="float32"):
+        h = np.asarray(x, dtype=np.float64) + np.asarray(residual, dtype=np.float64)
+        h_st = R.round_to_dtype(R.round_to_float32(h), h_dtype)
+        y, rstd = R.rms_norm_forward(h_st, gamma, eps)
+        return y, h_st, rstd
+    return f
+
+
+def _fused_truncates_h():
+    def f(x, residual, gamma=None, eps=1e-6, h_dtype="float32"):
+        h = np.asarray(x, dtype=np.float64) + np.asarray(residual, dtype=np.float64)
+        y, rstd = R.rms_norm_forward(h, gamma, eps)
+        h32 = R.round_to_float32(h)
+        return y, (_bf16_truncate(h32) if h_dtype == "bfloat16" else R.round_to_dtype(h32, h_dtype)), rstd
+    return f
+
+
+def _fused_bwd_dgamma_of_x():
+    def f(dy, x, residual, gamma=None, eps=1e-6):
+        dh, _ = R.rms_norm_backward(dy, np.asarray(x) + np.asarray(residual), gamma, eps)
+        _, dg = R.rms_norm_backward(dy, x, gamma, eps)
+        return dh, dh.copy(), dg
+    return f
+
+
+def _fused_from_h_subtracts_stream():
+    def f(dy, h, gamma=None, eps=1e-6, dh_stream=None):
+        dh, dg = R.rms_norm_backward(dy, h, gamma, eps)
+        return (dh if dh_stream is None else dh - np.asarray(dh_stream)), dg
+    return f
+
+
+def _ln_from_y(xhat_times_gamma=False, drop_rstd=False):
+    def f(dy, y, rstd, gamma=None, beta=None):
+        dy = np.asarray(dy, dtype=np.float64)
+        y = np.asarray(y, dtype=np.float64)
+        H = y.shape[1]
+        gm = np.ones(H) if gamma is None else np.asarray(gamma, dtype=np.float64)
+        bt = np.zeros(H) if beta is None else np.asarray(beta, dtype=np.float64)
+        r = np.ones(y.shape[0]) if drop_rstd else np.asarray(rstd, dtype=np.float64).reshape(-1)
+        xh = (y - bt) * gm if xhat_times_gamma else (y - bt) / gm
+        g = dy * gm
+        dx = r[:, None] / H * (H * g - g.sum(axis=1)[:, None] - xh * (g * xh).sum(axis=1)[:, None])
+        return dx, (dy * xh).sum(axis=0), dy.sum(axis=0)
+    return f
+
+
+def _rms_from_y_dgamma_of_y():
+    def f(dy, y, rstd, gamma=None):
+        dx, _ = R.rms_norm_backward_from_output(dy, y, rstd, gamma)
+        return dx, (np.asarray(dy, dtype=np.float64) * np.asarray(y, dtype=np.float64)).sum(axis=0)
+    return f
+
+
 def _merge_wrong(a, b):
     na, ma, m2a = a
     nb, mb, m2b = b
@@ -176,6 +231,13 @@ MUTANTS = {
     "ln_from_output_forgets_beta": dict(layer_norm_backward_from_output=_ln_from_y_forgets_beta()),
     "rms_from_output_multiplies_gamma": dict(rms_norm_backward_from_output=_rms_from_y_times_gamma()),
     "fused_bwd_from_h_forgets_stream": dict(fused_add_rms_norm_backward_from_h=_fused_from_h_forgets_stream()),
+    "fused_normalises_rounded_h": dict(fused_add_rms_norm_forward=_fused_normalises_rounded_h()),
+    "fused_truncates_h": dict(fused_add_rms_norm_forward=_fused_truncates_h()),
+    "fused_bwd_dgamma_of_x": dict(fused_add_rms_norm_backward=_fused_bwd_dgamma_of_x()),
+    "fused_bwd_from_h_subtracts_stream": dict(fused_add_rms_norm_backward_from_h=_fused_from_h_subtracts_stream()),
+    "ln_from_output_xhat_times_gamma": dict(layer_norm_backward_from_output=_ln_from_y(xhat_times_gamma=True)),
+    "ln_from_output_drops_rstd": dict(layer_norm_backward_from_output=_ln_from_y(drop_rstd=True)),
+    "rms_from_output_dgamma_of_y": dict(rms_norm_backward_from_output=_rms_from_y_dgamma_of_y()),
     "welford_merge_wrong_weight": dict(welford_merge=_merge_wrong),
     "welford_recurrence_old_mean_twice": dict(welford_sequential=_welford_seq_wrong),
     "bf16_truncates": dict(round_to_bfloat16=_bf16_truncate),
