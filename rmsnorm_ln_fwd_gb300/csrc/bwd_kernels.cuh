@@ -49,9 +49,10 @@ namespace normk {
 //
 // CL > 1: a thread-block cluster of CL CTAs shares each row, CTA rank r
 // taking columns [r*H/CL, (r+1)*H/CL) with its accumulators in registers; the
-// CTAs' row sums meet through distributed shared memory (one cluster barrier
-// a row), and cluster c writes partial row c.  Used for rows too wide for one
-// CTA's registers (H > 10240).
+// CTAs' row sums meet through distributed shared memory
+// (cluster_group_sum_async, one exchange a row), and cluster c writes partial
+// row c.  Used for rows too wide for one CTA's registers, and for fp32 rows
+// whose one-CTA kernels spill (the host policy in launch_bwd_typed).
 template <typename D>
 __device__ __forceinline__ BwdArgs part_row_view(BwdArgs a, int rank, int parts) {
   using T = typename D::T;
@@ -91,7 +92,7 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
   const int nw = tpr >> 5;
   const int wig = t >> 5;
   const int lane = threadIdx.x & 31;
-  const int H = a.H;  // this CTA's columns (half the row in a cluster)
+  const int H = a.H;  // this CTA's columns (H/CL of the row in a cluster)
   const int hv = H / VEC;
   const float inv_h = 1.f / (float)h_full;
   const bool w_f32 = a.w_f32 != 0;
@@ -919,8 +920,10 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
     case PATH_AUTO:
       // LayerNorm keeps two accumulators a column, which the bulk-copy
       // consumers hold in registers: measured, the register rows win for it up
-      // to 1024 threads a row (2048x16384 bf16: 98 vs 113 us); RMSNorm gains
-      // from the pipeline past 640.
+      // to 1024 threads a row (2048x16384 bf16: 98 vs 113 us); RMSNorm gained
+      // from the pipeline past 640 before cluster rows.  Now every row the
+      // pipeline could hold fits a one-CTA shape of at most 640 threads or a
+      // cluster, so AUTO no longer reaches it; PATH_STAGED still forces it.
       use_rows = rows_ok && tpr <= (KIND == KIND_LN ? 1024 : kRowsAutoMaxThreads);
       use_staged = !use_rows && staged_ok;
       use_rows = use_rows || (!use_staged && rows_ok);

@@ -61,7 +61,8 @@ namespace normk {
 //
 // CL > 1: a thread-block cluster of CL CTAs shares each row, CTA rank r taking
 // columns [r*H/CL, (r+1)*H/CL); the row sums meet through distributed shared
-// memory (one cluster barrier a row, two when the exact second pass runs).
+// memory (cluster_group_sum_async: one exchange a row, two when the exact
+// second pass runs).
 // Used only for rows that neither one CTA's registers nor the bulk-copy ring
 // can hold (measured: where one CTA still fits, it is faster).
 template <typename D>
