@@ -162,8 +162,9 @@ class ClockSampler:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-        except OSError:
+        except OSError:  # no nvidia-smi: no clock record
             self.proc = None
+            os.unlink(self.path)
             return
         t0 = time.time()
         while time.time() - t0 < 5.0 and os.path.getsize(self.path) == 0:
