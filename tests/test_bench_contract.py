@@ -82,3 +82,14 @@ def test_reference_arm_json_line():
     assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["e2e"]["d2h_bytes_per_step"] == 0
     c = j["cpu_baseline"]
     assert c["kind"] == "oracle" and c["value"] == j["value"] and c["cores"] >= 1 and c["sample"]
+
+
+def test_cpu_baseline_on_host_cores(monkeypatch):
+    # the CUDA arm's cpu_baseline leg: the oracle on one core, then one spawned
+    # process per core (two here, to keep the test short)
+    from types import SimpleNamespace
+    monkeypatch.setattr(os, "cpu_count", lambda: 2)
+    c = bench.cpu_baseline(SimpleNamespace(cpu_seconds=0.2, cpu_rows=8))
+    assert c["kind"] == "oracle" and c["unit"] == "GB/s" and c["cores"] == 2 and c["sample"]
+    assert c["value"] > 0 and c["single_core"]["value"] > 0 and c["single_core"]["cores"] == 1
+    assert c["value"] > 0.5 * c["single_core"]["value"]
