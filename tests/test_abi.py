@@ -30,7 +30,8 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return re.findall(r"^\s*(?:norm_status|size_t|const char\*|int)\s+([a-z_0-9]+)\s*\(", text, flags=re.M)
 

@@ -34,7 +34,7 @@ def _rank_main(rank, world, port, out):
 def test_two_gloo_ranks_agree_on_max_and_job_throughput():
     world = 2
     port = _port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of a threaded test process
         out = m.dict()
         mp.start_processes(_rank_main, args=(world, port, out), nprocs=world, start_method="spawn")
         res = dict(out)
