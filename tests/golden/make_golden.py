@@ -30,6 +30,8 @@ CASES = [
     ("rms_f32_2x9", "rms", 2, 9, "float32", 1e-6, 0.0, 1.0),
     ("fused_bf16_2x48", "fused", 2, 48, "bfloat16", 1e-6, 0.0, 1.0),
     ("fused_f32_3x13", "fused", 3, 13, "float32", 1e-6, 0.0, 1.0),
+    ("ln_y_bf16_3x40", "ln_y", 3, 40, "bfloat16", 1e-5, 0.0, 1.0),
+    ("rms_y_f32_2x24", "rms_y", 2, 24, "float32", 1e-5, 0.0, 1.0),
 ]
 
 
@@ -44,6 +46,7 @@ def make(name, op, N, H, dt, eps, off, scale, seed):
     beta = _r(0.1 * rng.standard_normal(H), dt)
     dy = _r(rng.standard_normal((N, H)), dt)
     res = _r(rng.standard_normal((N, H)), dt)
+    stream = _r(rng.standard_normal((N, H)), dt)  # drawn last: the earlier draws keep their values
     case = {"name": name, "op": op, "N": N, "H": H, "dtype": dt, "eps": eps,
             "source": "oracle/norm_oracle.py via tests/golden/make_golden.py",
             "inputs": {"x": x.tolist(), "gamma": gamma.tolist()}}
@@ -59,10 +62,27 @@ def make(name, op, N, H, dt, eps, off, scale, seed):
         y, rstd = O.rms_norm_forward(x, gamma, eps)
         dx, dg = O.rms_norm_backward(dy, x, gamma, eps)
         exp.update(y=y, rstd=rstd, dx=dx, dgamma=dg)
-    else:
+    elif op == "fused":
         case["inputs"]["residual"] = res.tolist()
+        case["inputs"]["dy"] = dy.tolist()
+        case["inputs"]["dh_stream"] = stream.tolist()
         y, h, rstd = O.fused_add_rms_norm_forward(x, res, gamma, eps, dt)
-        exp.update(y=y, h=h, rstd=rstd)
+        # the backward reads the stored h, and the residual stream's gradient
+        dh, dg = O.fused_add_rms_norm_backward_from_h(dy, h, gamma, eps, stream)
+        exp.update(y=y, h=h, rstd=rstd, dh=dh, dgamma=dg)
+    elif op == "ln_y":
+        # the backward from the forward's stored output y and saved fp32 rstd
+        y, _, rstd = O.layer_norm_forward(x, gamma, beta, eps)
+        y, rstd = _r(y, dt), O.round_to_float32(rstd)
+        case["inputs"].update(beta=beta.tolist(), dy=dy.tolist(), y=y.tolist(), rstd=rstd.tolist())
+        dx, dg, db = O.layer_norm_backward_from_output(dy, y, rstd, gamma, beta)
+        exp.update(dx=dx, dgamma=dg, dbeta=db)
+    else:
+        y, rstd = O.rms_norm_forward(x, gamma, eps)
+        y, rstd = _r(y, dt), O.round_to_float32(rstd)
+        case["inputs"].update(dy=dy.tolist(), y=y.tolist(), rstd=rstd.tolist())
+        dx, dg = O.rms_norm_backward_from_output(dy, y, rstd, gamma)
+        exp.update(dx=dx, dgamma=dg)
     case["expected"] = {k: np.asarray(v).tolist() for k, v in exp.items()}
     return case
 
