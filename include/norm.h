@@ -12,7 +12,9 @@
  *   rstd have shape (N,), fp32.
  * Memory.  Every pointer is CUDA device memory owned by the caller (any
  *   allocator, e.g. PyTorch's).  The library never allocates, frees or keeps a
- *   pointer after the call returns.
+ *   pointer after the call returns.  Its only device memory is module-scope:
+ *   one error word per device (norm_device_errors) and the fixed workspace of
+ *   ln_backward_static_workspace.
  * Streams.  Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
  *   default stream) and runs asynchronously; the call returns once the work is
  *   enqueued.  Outputs are valid after the stream reaches that point.
@@ -28,8 +30,10 @@
  * Errors.  Arguments are validated on the host before anything is enqueued;
  *   an invalid call returns an error and enqueues nothing.  A failed launch
  *   returns NORM_ERR_CUDA.  No entry point aborts, throws or prints.
- * Threads.  Every entry point is thread-safe; the only library state is a
- *   per-device cache of device attributes.
+ * Threads.  Every entry point is thread-safe.  The host-side library state
+ *   is a per-device cache of device attributes (filled once, under a lock)
+ *   and the kernel-family override of norm_set_kernel_path (one atomic value
+ *   for the whole process).
  *
  * Sources: "Skill: Write a Triton LayerNorm Kernel", "Skill: Write CUDA
  * LayerNorm Kernel", "Skill: Write a Triton Fused Add+RMSNorm Kernel" and the
