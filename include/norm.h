@@ -31,9 +31,10 @@
  *   an invalid call returns an error and enqueues nothing.  A failed launch
  *   returns NORM_ERR_CUDA.  No entry point aborts, throws or prints.
  * Threads.  Every entry point is thread-safe.  The host-side library state
- *   is a per-device cache of device attributes (filled once, under a lock)
- *   and the kernel-family override of norm_set_kernel_path (one atomic value
- *   for the whole process).
+ *   is a per-device cache of device attributes (filled once, under a lock),
+ *   the kernel-family override of norm_set_kernel_path and the timing event
+ *   of norm_set_bwd_split_event (one atomic value each for the whole
+ *   process).
  *
  * Sources: "Skill: Write a Triton LayerNorm Kernel", "Skill: Write CUDA
  * LayerNorm Kernel", "Skill: Write a Triton Fused Add+RMSNorm Kernel" and the
@@ -292,6 +293,21 @@ norm_status norm_selftest_bounded_wait(unsigned long long limit_ns, norm_stream_
  * every family computes the same results within rounding.
  */
 norm_status norm_set_kernel_path(int path);
+
+/*
+ * Timing: split every later backward call in the process into its two
+ * kernels.  The bounded partial reduction of "Rewrite Triton normalization
+ * backward kernel_1 (#499)" runs the backward as a main kernel (dx and the
+ * per-CTA dgamma/dbeta partial rows) and a second kernel that sums the
+ * partials; its Benchmark harness asks for the device time of each.  When
+ * `event` (a cudaEvent_t, or NULL to turn the split off) is set, each backward
+ * records it on its stream after the main kernel and launches the reduction
+ * as an ordinary dependent launch instead of a programmatic one, so events
+ * recorded before and after the call bracket the two kernels.  Results are
+ * unchanged.  One value for the whole process; for benchmarks, not for
+ * concurrent production calls.
+ */
+norm_status norm_set_bwd_split_event(void* event);
 
 #ifdef __cplusplus
 }

@@ -49,6 +49,7 @@ SIGNATURES = {
     "norm_device_errors": (_I, [_I, ctypes.POINTER(ctypes.c_uint), _I]),
     "norm_selftest_bounded_wait": (_I, [ctypes.c_ulonglong, _P]),
     "norm_set_kernel_path": (_I, [_I]),
+    "norm_set_bwd_split_event": (_I, [_P]),
 }
 
 _lock = threading.Lock()
@@ -98,6 +99,12 @@ def device_errors(device: int = 0, clear: bool = True) -> int:
 def set_kernel_path(path: int) -> None:
     """0: automatic (default), 1: register rows, 2: strided loop, 3: bulk-copy pipeline first."""
     check("norm_set_kernel_path", load().norm_set_kernel_path(int(path)))
+
+
+def set_bwd_split_event(event_handle) -> None:
+    """Record the raw cudaEvent_t `event_handle` (an int, or None to stop)
+    between every later backward's main kernel and its partial reduction."""
+    check("norm_set_bwd_split_event", load().norm_set_bwd_split_event(event_handle or None))
 
 
 def check(fn: str, status: int) -> None:

@@ -145,6 +145,18 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
   int parity = 0;
   int64_t row = (int64_t)prow * rpc + slot;
   if (row < a.N) fetch(row);  // first row in flight while gamma is staged
+  constexpr bool PF = kBwdL2PrefetchRows > 1;
+  auto l2_prefetch_row = [&](int64_t pr) {
+    l2_prefetch_bulk(reinterpret_cast<const T*>(a.x) + pr * a.ldx, (uint32_t)(H * sizeof(T)));
+    l2_prefetch_bulk(reinterpret_cast<const T*>(a.dy) + pr * a.lddy, (uint32_t)(H * sizeof(T)));
+  };
+  if constexpr (PF) {
+    if (t == 0) {
+#pragma unroll 1
+      for (int k = 2; k < kBwdL2PrefetchRows; ++k)
+        if (row + k * stride < a.N) l2_prefetch_row(row + k * stride);
+    }
+  }
 
   const int Hp = a.Hp;
   // Shared memory: group scratch | fp32 gamma (thread-interleaved, shared by
@@ -221,6 +233,10 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
       }
     }
     if (row + stride < a.N) fetch(row + stride);
+    if constexpr (PF) {
+      const int64_t pr = row + kBwdL2PrefetchRows * stride;
+      if (t == 0 && pr < a.N) l2_prefetch_row(pr);
+    }
     if constexpr (FUSED) {
       // The gradient through h is only added in pass 2: load it for this row
       // now, in flight over the row reduction, rather than a row ahead.
@@ -738,6 +754,75 @@ __global__ void __launch_bounds__(256) bwd_param_reduce_kernel(const float* ws, 
   }
 }
 
+// The same sum with more CTAs: a CTA covers kRedColVecs column vectors (4
+// columns each) with kRedWarpsPerCol warps apiece; lane l of warp w of a
+// column vector sums partial rows l + 32w, l + 32w + 32*kRedWarpsPerCol, ...
+// (all loads issued before the adds), then a warp butterfly and a fixed-order
+// sum over the warps.  Same result up to fp32 summation order.
+#ifndef NORM_REDUCE_V2
+#define NORM_REDUCE_V2 0
+#endif
+constexpr int kRedColVecs = 2;
+constexpr int kRedWarpsPerCol = 4;
+constexpr int kRedRows = 4;  // partial rows a lane loads per batch
+
+template <typename D>
+__global__ void __launch_bounds__(256) bwd_param_reduce2_kernel(const float* ws, int P, int Hp, int H,
+                                                                void* dg, void* db, int w_f32) {
+  pdl_wait_primary();
+  const int which = blockIdx.y;
+  void* out = which ? db : dg;
+  if (out == nullptr) return;
+  const float* src = ws + (size_t)which * P * Hp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cv = warp / kRedWarpsPerCol;            // column vector of this warp in the CTA
+  const int wr = warp - cv * kRedWarpsPerCol;       // warp rank within the column vector
+  const int col = (blockIdx.x * kRedColVecs + cv) * 4;
+  constexpr int RS = 32 * kRedWarpsPerCol;          // row stride of one lane
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (col < Hp) {
+    for (int p0 = lane + 32 * wr; p0 < P; p0 += RS * kRedRows) {
+      float4 v[kRedRows];
+#pragma unroll
+      for (int k = 0; k < kRedRows; ++k) {
+        const int p = p0 + RS * k;
+        v[k] = p < P ? *reinterpret_cast<const float4*>(src + (size_t)p * Hp + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < kRedRows; ++k) {
+        acc.x += v[k].x;
+        acc.y += v[k].y;
+        acc.z += v[k].z;
+        acc.w += v[k].w;
+      }
+    }
+  }
+  float r[4] = {acc.x, acc.y, acc.z, acc.w};
+  warp_sum<4>(r);
+  __shared__ float4 sm[kRedColVecs * kRedWarpsPerCol];
+  if (lane == 0) sm[warp] = make_float4(r[0], r[1], r[2], r[3]);
+  __syncthreads();
+  if (threadIdx.x < kRedColVecs) {
+    const int c = (blockIdx.x * kRedColVecs + threadIdx.x) * 4;
+    float4 s4 = sm[threadIdx.x * kRedWarpsPerCol];
+    for (int k = 1; k < kRedWarpsPerCol; ++k) {
+      const float4 v = sm[threadIdx.x * kRedWarpsPerCol + k];
+      s4.x += v.x;
+      s4.y += v.y;
+      s4.z += v.z;
+      s4.w += v.w;
+    }
+    const float vals[4] = {s4.x, s4.y, s4.z, s4.w};
+    for (int i = 0; i < 4 && c + i < H; ++i) {
+      if (w_f32) {
+        reinterpret_cast<float*>(out)[c + i] = vals[i];
+      } else {
+        store_elem<D>(out, c + i, vals[i]);
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host-side configuration.
 // ---------------------------------------------------------------------------
@@ -996,8 +1081,16 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   if (err != cudaSuccess || !want) return err;
   // The column reduction is a programmatic dependent of the main kernel: it
   // is scheduled while the main kernel drains and waits for it on the device.
+  // With a split event set (timing the two kernels apart), the event is
+  // recorded between them and the reduction is an ordinary launch.
+  const bool split = dev.split_event != nullptr;
+  if (split) {
+    err = cudaEventRecord(static_cast<cudaEvent_t>(dev.split_event), s);
+    if (err != cudaSuccess) return err;
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.Hp + 31) / 32, LN ? 2 : 1);
+  cfg.gridDim = NORM_REDUCE_V2 ? dim3((a.Hp + 4 * kRedColVecs - 1) / (4 * kRedColVecs), LN ? 2 : 1)
+                               : dim3((a.Hp + 31) / 32, LN ? 2 : 1);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
@@ -1005,10 +1098,11 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = split ? 0 : 1;
   const float* ws = a.ws;
   void* dbeta = LN ? db : nullptr;
-  err = cudaLaunchKernelEx(&cfg, bwd_param_reduce_kernel<D>, ws, P, a.Hp, a.H, dg, dbeta, a.w_f32);
+  err = NORM_REDUCE_V2 ? cudaLaunchKernelEx(&cfg, bwd_param_reduce2_kernel<D>, ws, P, a.Hp, a.H, dg, dbeta, a.w_f32)
+                       : cudaLaunchKernelEx(&cfg, bwd_param_reduce_kernel<D>, ws, P, a.Hp, a.H, dg, dbeta, a.w_f32);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

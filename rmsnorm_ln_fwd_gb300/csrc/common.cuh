@@ -314,6 +314,15 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 #define NORM_L2_PREFETCH_ROWS 2
 #endif
 constexpr int kL2PrefetchRows = NORM_L2_PREFETCH_ROWS;
+#ifndef NORM_L2_PREFETCH_FUSED
+#define NORM_L2_PREFETCH_FUSED 0
+#endif
+constexpr bool kL2PrefetchFused = NORM_L2_PREFETCH_FUSED != 0;
+// The same for the register-row backward (x and dy rows; 0: off).
+#ifndef NORM_BWD_L2_PREFETCH_ROWS
+#define NORM_BWD_L2_PREFETCH_ROWS 0
+#endif
+constexpr int kBwdL2PrefetchRows = NORM_BWD_L2_PREFETCH_ROWS;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -138,6 +138,20 @@ __device__ __forceinline__ void fwd_rows_body(const FwdArgs& a, const FwdArgs& a
   int parity = 0;
   int64_t row = (int64_t)prow * rpc + slot;
   if (row < a.N) fetch(row);  // first row in flight while the parameters are staged
+  constexpr bool PF = kL2PrefetchRows > 1 && (KIND != KIND_FUSED || kL2PrefetchFused);
+  auto l2_prefetch_row = [&](int64_t pr) {
+    l2_prefetch_bulk(reinterpret_cast<const T*>(a.x) + pr * a.ldx, (uint32_t)(H * sizeof(T)));
+    if constexpr (KIND == KIND_FUSED)
+      l2_prefetch_bulk(reinterpret_cast<const T*>(a.res) + pr * a.ldr, (uint32_t)(H * sizeof(T)));
+  };
+  if constexpr (PF) {
+    // rows 2 .. depth-1 strides ahead now; the loop asks for `depth` ahead
+    if (t == 0) {
+#pragma unroll 1
+      for (int k = 2; k < kL2PrefetchRows; ++k)
+        if (row + k * stride < a.N) l2_prefetch_row(row + k * stride);
+    }
+  }
 
   // gamma (and beta) as fp32, thread-interleaved, shared by the row slots.
   float4* gs = reinterpret_cast<float4*>(sh_dyn + ((rpc * 2 * nw * 3 + 3) & ~3));
@@ -182,10 +196,9 @@ __device__ __forceinline__ void fwd_rows_body(const FwdArgs& a, const FwdArgs& a
     // wide-row forward; the fused add, already near the HBM roof, and the
     // backward, bound by the shared-memory pipe, lose with it).
     if (row + stride < a.N) fetch(row + stride);
-    if constexpr (kL2PrefetchRows > 1 && KIND != KIND_FUSED) {
+    if constexpr (PF) {
       const int64_t pr = row + kL2PrefetchRows * stride;
-      if (t == 0 && pr < a.N)
-        l2_prefetch_bulk(reinterpret_cast<const T*>(a.x) + pr * a.ldx, (uint32_t)(H * sizeof(T)));
+      if (t == 0 && pr < a.N) l2_prefetch_row(pr);
     }
 
     float rstd, mean_d = 0.f;

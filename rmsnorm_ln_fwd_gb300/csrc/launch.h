@@ -28,6 +28,8 @@ struct DeviceInfo {
   int max_smem_optin;  // bytes of shared memory one CTA may opt into
   unsigned* err;       // this device's error-flag word (see norm_device_errors)
   int path;            // first kernel family to try (norm_set_kernel_path)
+  void* split_event;   // cudaEvent_t recorded between the backward's two kernels, or null
+                       // (norm_set_bwd_split_event; the reduction then runs without PDL)
 };
 
 // Forward: LayerNorm (KIND_LN), RMSNorm (KIND_RMS), fused add + RMSNorm (KIND_FUSED).

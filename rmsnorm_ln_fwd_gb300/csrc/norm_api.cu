@@ -29,6 +29,7 @@ std::mutex g_mu;
 DeviceInfo g_info[kMaxDevices];
 bool g_have[kMaxDevices];
 std::atomic<int> g_path{normk::PATH_AUTO};
+std::atomic<void*> g_split_event{nullptr};
 
 }  // namespace
 
@@ -100,6 +101,7 @@ bool current_device_info(DeviceInfo* out) {
     out->err = g_info[dev].err;
   }
   out->path = g_path.load(std::memory_order_relaxed);
+  out->split_event = g_split_event.load(std::memory_order_relaxed);
   return true;
 }
 
@@ -142,6 +144,17 @@ Span vec_span(const void* p, int64_t n, size_t es) {
 }
 
 bool overlap(const Span& a, const Span& b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo; }
+
+// Whether any span of `a` overlaps any span of `b` (empty spans never do).
+template <size_t NA, size_t NB>
+bool any_overlap(const Span (&a)[NA], const Span (&b)[NB]) {
+  for (const Span& p : a)
+    for (const Span& q : b)
+      if (overlap(p, q)) return true;
+  return false;
+}
+
+constexpr Span kNoSpan{0, 0};
 
 // Two row tensors may be the same buffer (same pointer and stride) or
 // disjoint; anything in between is a partial overlap.
@@ -191,6 +204,18 @@ norm_status forward_common(int kind, const void* x, int64_t ldx, const void* res
     if (!same_or_disjoint(y, ldy, x, ldx, N, H, es)) return NORM_ERR_INVALID_VALUE;
   }
   if (mean && rstd && overlap(vec_span(mean, N, 4), vec_span(rstd, N, 4))) return NORM_ERR_INVALID_VALUE;
+  {
+    // The statistics and parameters stay clear of every output, and the saved
+    // statistics clear of the input rows.
+    const size_t wes = elem_size(wd);
+    const Span stats[] = {mean ? vec_span(mean, N, 4) : kNoSpan, rstd ? vec_span(rstd, N, 4) : kNoSpan};
+    const Span params[] = {gamma ? vec_span(gamma, H, wes) : kNoSpan, beta ? vec_span(beta, H, wes) : kNoSpan};
+    const Span out_rows[] = {rows_span(y, N, ldy, H, es), fused ? rows_span(h, N, ldh, H, es) : kNoSpan};
+    const Span in_rows[] = {rows_span(x, N, ldx, H, es), fused ? rows_span(res, N, ldr, H, es) : kNoSpan};
+    if (any_overlap(params, out_rows) || any_overlap(params, stats) || any_overlap(stats, out_rows) ||
+        any_overlap(stats, in_rows))
+      return NORM_ERR_INVALID_VALUE;
+  }
   DeviceInfo dev;
   if (!current_device_info(&dev)) return NORM_ERR_CUDA;
   FwdArgs a{};
@@ -262,17 +287,40 @@ norm_status backward_common(int kind, const void* dy, int64_t lddy, const void* 
   const Span sdx = rows_span(dx, N, lddx, H, es);
   if (dgamma && overlap(vec_span(dgamma, H, wes), sdx)) return NORM_ERR_INVALID_VALUE;
   if (dbeta && overlap(vec_span(dbeta, H, wes), sdx)) return NORM_ERR_INVALID_VALUE;
-  DeviceInfo dev;
-  if (!current_device_info(&dev)) return NORM_ERR_CUDA;
+  {
+    // The saved statistics and parameters (inputs) stay clear of every
+    // output, and the parameter gradients clear of every input.
+    const Span small_in[] = {mean ? vec_span(mean, N, 4) : kNoSpan, vec_span(rstd, N, 4),
+                             gamma ? vec_span(gamma, H, wes) : kNoSpan, beta ? vec_span(beta, H, wes) : kNoSpan};
+    const Span pgrads[] = {dgamma ? vec_span(dgamma, H, wes) : kNoSpan, dbeta ? vec_span(dbeta, H, wes) : kNoSpan};
+    const Span out_rows[] = {sdx, (dres && !dx_twice) ? rows_span(dres, N, lddres, H, es) : kNoSpan};
+    const Span in_rows[] = {rows_span(dy, N, lddy, H, es), rows_span(x, N, ldx, H, es),
+                            dh_in ? rows_span(dh_in, N, lddh, H, es) : kNoSpan};
+    if (any_overlap(small_in, out_rows) || any_overlap(small_in, pgrads) || any_overlap(pgrads, in_rows) ||
+        any_overlap(pgrads, out_rows))
+      return NORM_ERR_INVALID_VALUE;
+  }
   const bool want = dgamma != nullptr || dbeta != nullptr;
   if (want) {
     if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 15u) != 0) return NORM_ERR_WORKSPACE;
-    if (ws_bytes < workspace_bytes_for(H, dev)) return NORM_ERR_WORKSPACE;
-    const Span sws = Span{reinterpret_cast<uintptr_t>(ws), reinterpret_cast<uintptr_t>(ws) + ws_bytes};
-    if (overlap(sws, sdx) || (dgamma && overlap(sws, vec_span(dgamma, H, wes))) ||
-        (dbeta && overlap(sws, vec_span(dbeta, H, wes))))
-      return NORM_ERR_WORKSPACE;
+    const Span sws[] = {Span{reinterpret_cast<uintptr_t>(ws), reinterpret_cast<uintptr_t>(ws) + ws_bytes}};
+    // The workspace is scratch: clear of every input and output.
+    const Span others[] = {sdx,
+                           (dres && !dx_twice) ? rows_span(dres, N, lddres, H, es) : kNoSpan,
+                           dgamma ? vec_span(dgamma, H, wes) : kNoSpan,
+                           dbeta ? vec_span(dbeta, H, wes) : kNoSpan,
+                           rows_span(dy, N, lddy, H, es),
+                           rows_span(x, N, ldx, H, es),
+                           dh_in ? rows_span(dh_in, N, lddh, H, es) : kNoSpan,
+                           mean ? vec_span(mean, N, 4) : kNoSpan,
+                           vec_span(rstd, N, 4),
+                           gamma ? vec_span(gamma, H, wes) : kNoSpan,
+                           beta ? vec_span(beta, H, wes) : kNoSpan};
+    if (any_overlap(sws, others)) return NORM_ERR_WORKSPACE;
   }
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return NORM_ERR_CUDA;
+  if (want && ws_bytes < workspace_bytes_for(H, dev)) return NORM_ERR_WORKSPACE;
   BwdArgs a{};
   a.dy = dy;
   a.lddy = lddy;
@@ -407,6 +455,11 @@ const char* norm_last_error(void) { return t_last_error; }
 norm_status norm_set_kernel_path(int path) {
   if (path < normk::PATH_AUTO || path > normk::PATH_STAGED) return NORM_ERR_INVALID_VALUE;
   g_path.store(path, std::memory_order_relaxed);
+  return NORM_OK;
+}
+
+norm_status norm_set_bwd_split_event(void* event) {
+  g_split_event.store(event, std::memory_order_relaxed);
   return NORM_OK;
 }
 

@@ -44,12 +44,39 @@ def _rows(t: torch.Tensor, what: str):
     return v, N, H, ld
 
 
-def _vec(t, H, what):
+def _vec(t, H, what, device=None):
     if t is None:
         return None
-    if not t.is_cuda or t.dim() != 1 or t.shape[0] != H or (H > 1 and t.stride(0) != 1):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 1 or t.shape[0] != H or \
+            (H > 1 and t.stride(0) != 1):
         raise ValueError(f"{what} must be a contiguous CUDA tensor of shape ({H},)")
+    if device is not None and t.device != device:
+        raise ValueError(f"{what} is on {t.device}, the rows on {device}")
     return t
+
+
+def _stats(t, N, what, device):
+    """A saved statistic: a contiguous fp32 CUDA tensor of N elements (any
+    shape, e.g. (B, T) for (B, T, H) rows) on the rows' device."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if t.dtype != torch.float32:
+        raise ValueError(f"{what} must be float32, not {t.dtype}")
+    if t.numel() != N or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous tensor of {N} elements (one per row)")
+    if t.device != device:
+        raise ValueError(f"{what} is on {t.device}, the rows on {device}")
+    return t
+
+
+def _grad_out(out, ref, N, H, what):
+    """The 2-D view of a caller's output tensor, which must match the rows
+    (N, H), dtype and device of `ref`."""
+    ov, No, Ho, ld = _rows(out, what)
+    if (No, Ho) != (N, H) or out.dtype != ref.dtype or out.device != ref.device:
+        raise ValueError(f"{what} must match {tuple(ref.shape)} {ref.dtype} on {ref.device} in rows, width, "
+                         f"dtype and device")
+    return ov, ld
 
 
 def _ptr(t):
@@ -72,12 +99,10 @@ def ln_forward(x, gamma=None, beta=None, eps: float = 1e-5, *, out=None, save_st
     fp32 of shape (N,) (None when save_stats is False)."""
     xv, N, H, ldx = _rows(x, "x")
     xc = _dtype_code(x, "x")
-    gamma, beta = _vec(gamma, H, "gamma"), _vec(beta, H, "beta")
+    gamma, beta = _vec(gamma, H, "gamma", x.device), _vec(beta, H, "beta", x.device)
     wc = _w_code(xc, gamma, beta)
     y = torch.empty_like(x, memory_format=torch.contiguous_format) if out is None else out
-    yv, Ny, Hy, ldy = _rows(y, "out")
-    if (Ny, Hy) != (N, H) or y.dtype != x.dtype:
-        raise ValueError("out must match x in rows, width and dtype")
+    yv, ldy = _grad_out(y, x, N, H, "out")
     mean = torch.empty(N, device=x.device, dtype=torch.float32) if save_stats else None
     rstd = torch.empty(N, device=x.device, dtype=torch.float32) if save_stats else None
     lib = _lib.load()
@@ -92,12 +117,10 @@ def rms_forward(x, gamma=None, eps: float = 1e-5, *, out=None, save_stats: bool 
     """RMSNorm over the last dim.  Returns (y, rstd)."""
     xv, N, H, ldx = _rows(x, "x")
     xc = _dtype_code(x, "x")
-    gamma = _vec(gamma, H, "gamma")
+    gamma = _vec(gamma, H, "gamma", x.device)
     wc = _w_code(xc, gamma)
     y = torch.empty_like(x, memory_format=torch.contiguous_format) if out is None else out
-    yv, Ny, Hy, ldy = _rows(y, "out")
-    if (Ny, Hy) != (N, H) or y.dtype != x.dtype:
-        raise ValueError("out must match x in rows, width and dtype")
+    yv, ldy = _grad_out(y, x, N, H, "out")
     rstd = torch.empty(N, device=x.device, dtype=torch.float32) if save_stats else None
     lib = _lib.load()
     with torch.cuda.device(x.device):
@@ -114,18 +137,14 @@ def fused_add_rms_forward(x, residual, gamma=None, eps: float = 1e-6, *, h_out=N
     ``h_out`` may be a fresh tensor (default), ``x`` or ``residual`` itself
     (in-place update of the residual stream).  Returns (y, h, rstd)."""
     xv, N, H, ldx = _rows(x, "x")
-    rv, Nr, Hr, ldr = _rows(residual, "residual")
-    if (Nr, Hr) != (N, H) or residual.dtype != x.dtype:
-        raise ValueError("residual must match x in rows, width and dtype")
     xc = _dtype_code(x, "x")
-    gamma = _vec(gamma, H, "gamma")
+    rv, ldr = _grad_out(residual, x, N, H, "residual")
+    gamma = _vec(gamma, H, "gamma", x.device)
     wc = _w_code(xc, gamma)
     h = torch.empty_like(x, memory_format=torch.contiguous_format) if h_out is None else h_out
-    hv, Nh, Hh, ldh = _rows(h, "h_out")
+    hv, ldh = _grad_out(h, x, N, H, "h_out")
     y = torch.empty_like(x, memory_format=torch.contiguous_format) if out is None else out
-    yv, Ny, Hy, ldy = _rows(y, "out")
-    if (Nh, Hh) != (N, H) or (Ny, Hy) != (N, H) or h.dtype != x.dtype or y.dtype != x.dtype:
-        raise ValueError("h_out and out must match x in rows, width and dtype")
+    yv, ldy = _grad_out(y, x, N, H, "out")
     rstd = torch.empty(N, device=x.device, dtype=torch.float32) if save_stats else None
     lib = _lib.load()
     with torch.cuda.device(x.device):
@@ -148,6 +167,8 @@ def _workspace(ws, H, device):
         raise RuntimeError("could not size the backward workspace (no CUDA device?)")
     if ws is None:
         return torch.empty((need + 3) // 4, device=device, dtype=torch.float32), need
+    if not isinstance(ws, torch.Tensor) or not ws.is_cuda or ws.device != device or not ws.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous CUDA tensor on {device}")
     nbytes = ws.numel() * ws.element_size()
     return ws, nbytes
 
@@ -157,16 +178,15 @@ def ln_backward(dy, x, mean, rstd, gamma=None, *, need_param_grads: bool = True,
     """LayerNorm backward.  Returns (dx, dgamma, dbeta) (dgamma/dbeta None when
     need_param_grads is False).  dgamma/dbeta take gamma's dtype (or
     ``param_dtype``, else x's dtype)."""
-    dyv, N, H, lddy = _rows(dy, "dy")
-    xv, Nx, Hx, ldx = _rows(x, "x")
-    if (Nx, Hx) != (N, H) or dy.dtype != x.dtype:
-        raise ValueError("dy must match x")
+    xv, N, H, ldx = _rows(x, "x")
+    dyv, lddy = _grad_out(dy, x, N, H, "dy")
     xc = _dtype_code(x, "x")
-    gamma = _vec(gamma, H, "gamma")
+    mean, rstd = _stats(mean, N, "mean", x.device), _stats(rstd, N, "rstd", x.device)
+    gamma = _vec(gamma, H, "gamma", x.device)
     wdt = gamma.dtype if gamma is not None else (param_dtype or x.dtype)
     wc = _DT[wdt]
     out = torch.empty_like(x, memory_format=torch.contiguous_format) if dx is None else dx
-    ov, No, Ho, lddx = _rows(out, "dx")
+    ov, lddx = _grad_out(out, x, N, H, "dx")
     dgamma = torch.empty(H, device=x.device, dtype=wdt) if need_param_grads else None
     dbeta = torch.empty(H, device=x.device, dtype=wdt) if (need_param_grads and beta_grad) else None
     ws, wsb = (None, 0)
@@ -184,16 +204,15 @@ def ln_backward(dy, x, mean, rstd, gamma=None, *, need_param_grads: bool = True,
 def rms_backward(dy, x, rstd, gamma=None, *, need_param_grads: bool = True, workspace=None, dx=None,
                  param_dtype=None):
     """RMSNorm backward.  Returns (dx, dgamma)."""
-    dyv, N, H, lddy = _rows(dy, "dy")
-    xv, Nx, Hx, ldx = _rows(x, "x")
-    if (Nx, Hx) != (N, H) or dy.dtype != x.dtype:
-        raise ValueError("dy must match x")
+    xv, N, H, ldx = _rows(x, "x")
+    dyv, lddy = _grad_out(dy, x, N, H, "dy")
     xc = _dtype_code(x, "x")
-    gamma = _vec(gamma, H, "gamma")
+    rstd = _stats(rstd, N, "rstd", x.device)
+    gamma = _vec(gamma, H, "gamma", x.device)
     wdt = gamma.dtype if gamma is not None else (param_dtype or x.dtype)
     wc = _DT[wdt]
     out = torch.empty_like(x, memory_format=torch.contiguous_format) if dx is None else dx
-    ov, No, Ho, lddx = _rows(out, "dx")
+    ov, lddx = _grad_out(out, x, N, H, "dx")
     dgamma = torch.empty(H, device=x.device, dtype=wdt) if need_param_grads else None
     ws, wsb = (None, 0)
     if need_param_grads:
@@ -215,22 +234,19 @@ def fused_add_rms_backward(dy, h, rstd, gamma=None, dh_in=None, *, need_param_gr
     None).  ``residual_grad``: "separate" writes a second buffer, "none"
     returns dres = None (the caller reuses dx), "same" treats x and residual
     as one tensor and returns 2 * dL/dh in dx (dres is dx)."""
-    dyv, N, H, lddy = _rows(dy, "dy")
-    hv, Nh, Hh, ldh = _rows(h, "h")
-    if (Nh, Hh) != (N, H) or dy.dtype != h.dtype:
-        raise ValueError("dy must match h")
+    hv, N, H, ldh = _rows(h, "h")
+    dyv, lddy = _grad_out(dy, h, N, H, "dy")
     xc = _dtype_code(h, "h")
-    gamma = _vec(gamma, H, "gamma")
+    rstd = _stats(rstd, N, "rstd", h.device)
+    gamma = _vec(gamma, H, "gamma", h.device)
     wdt = gamma.dtype if gamma is not None else (param_dtype or h.dtype)
     wc = _DT[wdt]
     if dh_in is not None:
-        dv, Nd, Hd, lddh = _rows(dh_in, "dh_in")
-        if (Nd, Hd) != (N, H) or dh_in.dtype != h.dtype:
-            raise ValueError("dh_in must match h")
+        dv, lddh = _grad_out(dh_in, h, N, H, "dh_in")
     else:
         dv, lddh = None, 0
     out = torch.empty_like(h, memory_format=torch.contiguous_format) if dx is None else dx
-    ov, No, Ho, lddx = _rows(out, "dx")
+    ov, lddx = _grad_out(out, h, N, H, "dx")
     if residual_grad == "separate":
         dres = torch.empty_like(h, memory_format=torch.contiguous_format)
         rv, _, _, lddres = _rows(dres, "dres")
@@ -258,16 +274,15 @@ def ln_backward_from_output(dy, y, rstd, gamma=None, beta=None, *, need_param_gr
                             beta_grad: bool = True, workspace=None, dx=None, param_dtype=None):
     """LayerNorm backward from the forward's output y (x_hat = (y - beta)/gamma)
     and saved rstd.  Returns (dx, dgamma, dbeta)."""
-    dyv, N, H, lddy = _rows(dy, "dy")
-    yv, Ny, Hy, ldy = _rows(y, "y")
-    if (Ny, Hy) != (N, H) or dy.dtype != y.dtype:
-        raise ValueError("dy must match y")
+    yv, N, H, ldy = _rows(y, "y")
+    dyv, lddy = _grad_out(dy, y, N, H, "dy")
     xc = _dtype_code(y, "y")
-    gamma, beta = _vec(gamma, H, "gamma"), _vec(beta, H, "beta")
+    rstd = _stats(rstd, N, "rstd", y.device)
+    gamma, beta = _vec(gamma, H, "gamma", y.device), _vec(beta, H, "beta", y.device)
     wdt = gamma.dtype if gamma is not None else (beta.dtype if beta is not None else (param_dtype or y.dtype))
     wc = _w_code(_DT[wdt], gamma, beta)
     out = torch.empty_like(y, memory_format=torch.contiguous_format) if dx is None else dx
-    ov, _, _, lddx = _rows(out, "dx")
+    ov, lddx = _grad_out(out, y, N, H, "dx")
     dgamma = torch.empty(H, device=y.device, dtype=wdt) if need_param_grads else None
     dbeta = torch.empty(H, device=y.device, dtype=wdt) if (need_param_grads and beta_grad) else None
     ws, wsb = (None, 0)
@@ -286,16 +301,15 @@ def rms_backward_from_output(dy, y, rstd, gamma=None, *, need_param_grads: bool 
                              param_dtype=None):
     """RMSNorm backward from the forward's output y (x_hat = y/gamma) and saved
     rstd.  Returns (dx, dgamma)."""
-    dyv, N, H, lddy = _rows(dy, "dy")
-    yv, Ny, Hy, ldy = _rows(y, "y")
-    if (Ny, Hy) != (N, H) or dy.dtype != y.dtype:
-        raise ValueError("dy must match y")
+    yv, N, H, ldy = _rows(y, "y")
+    dyv, lddy = _grad_out(dy, y, N, H, "dy")
     xc = _dtype_code(y, "y")
-    gamma = _vec(gamma, H, "gamma")
+    rstd = _stats(rstd, N, "rstd", y.device)
+    gamma = _vec(gamma, H, "gamma", y.device)
     wdt = gamma.dtype if gamma is not None else (param_dtype or y.dtype)
     wc = _DT[wdt]
     out = torch.empty_like(y, memory_format=torch.contiguous_format) if dx is None else dx
-    ov, _, _, lddx = _rows(out, "dx")
+    ov, lddx = _grad_out(out, y, N, H, "dx")
     dgamma = torch.empty(H, device=y.device, dtype=wdt) if need_param_grads else None
     ws, wsb = (None, 0)
     if need_param_grads:

@@ -112,6 +112,39 @@ def test_fused_validation(lib):
     assert f(N=0, x=None, r=None, y=None, h=None) == OK
 
 
+def test_forward_stats_and_params_clear_of_outputs(lib):
+    # mean/rstd (outputs) and gamma/beta (inputs) may not overlap each other,
+    # the output rows or (for the statistics) the input rows
+    E = 0x600000
+    assert _ln(lib, g=B) == INVALID                          # gamma under y
+    assert _ln(lib, b=B + 64) == INVALID                     # beta under y
+    assert _ln(lib, mean=A + 8) == INVALID                   # mean over x
+    assert _ln(lib, rstd=B + 8) == INVALID                   # rstd over y
+    assert _ln(lib, g=E, mean=E + 8) == INVALID              # mean over gamma
+    assert _ln(lib, b=E, rstd=E) == INVALID                  # rstd over beta
+    assert lib.fused_add_rms_forward(A, 64, B, 64, D + 8, C, 64, D, 64, None, 4, 64, 1e-6, BF16, BF16,
+                                     None) == INVALID      # gamma under h
+    assert lib.fused_add_rms_forward(A, 64, B, 64, None, C, 64, D, 64, B + 4, 4, 64, 1e-6, BF16, BF16,
+                                     None) == INVALID      # rstd over the residual
+    assert lib.rms_forward(A, 64, B + 2, B, 64, None, 4, 64, 1e-5, BF16, BF16, None) == INVALID  # gamma under y
+
+
+def test_backward_stats_and_params_clear_of_outputs(lib):
+    E, F = 0x600000, 0x700000
+    assert _bwd(lib, mean=D + 16) == INVALID                 # mean under dx
+    assert _bwd(lib, rstd=D) == INVALID                      # rstd under dx
+    assert _bwd(lib, g=D + 32) == INVALID                    # gamma under dx
+    assert _bwd(lib, g=E, dg=E + 2, ws=F, wsb=1 << 20) == INVALID  # dgamma over gamma
+    assert _bwd(lib, dg=B + 2, ws=F, wsb=1 << 20) == INVALID  # dgamma over x
+    assert _bwd(lib, db=A, ws=F, wsb=1 << 20) == INVALID     # dbeta over dy
+    assert _bwd(lib, dg=C + 4, ws=F, wsb=1 << 20) == INVALID  # dgamma over mean
+    assert _bwd(lib, dg=E, ws=B - 16, wsb=64) == WORKSPACE   # workspace over x
+    assert _bwd(lib, dg=E, ws=C, wsb=64) == WORKSPACE        # workspace over mean
+    assert _bwd(lib, dg=E, ws=D + 64, wsb=64) == WORKSPACE   # workspace over dx
+    assert _bwd(lib, dg=E, ws=None) == WORKSPACE
+    assert _bwd(lib, dg=E, ws=F + 4, wsb=64) == WORKSPACE    # misaligned workspace
+
+
 def _bwd(lib, **kw):
     a = dict(dy=A, ldy=64, x=B, ldx=64, mean=C, rstd=C + 4096, g=None, dx=D, lddx=64, dg=None, db=None, ws=None,
              wsb=0, N=4, H=64, xd=BF16, wd=BF16)
@@ -157,6 +190,14 @@ def test_fused_backward_validation(lib):
     assert _fbwd(lib, dh=0x500000, lddh=64, dres=0x500000 + 2, lddres=64) == INVALID  # dres partly over dh
 
 
+def test_fused_backward_clear_of_outputs(lib):
+    E = 0x600000
+    assert _fbwd(lib, rstd=0x500000, dres=0x500000 - 64, lddres=64) == INVALID       # rstd under dres
+    assert _fbwd(lib, dg=0x500000 + 8, dres=0x500000, lddres=64, ws=E, wsb=1 << 20) == INVALID  # dgamma under dres
+    assert _fbwd(lib, dg=0x500000 + 8, dh=0x500000, lddh=64, ws=E, wsb=1 << 20) == INVALID  # dgamma over dh_in
+    assert _fbwd(lib, g=D + 8) == INVALID                                              # gamma under dx
+
+
 def test_from_output_validation(lib):
     def ln(**kw):
         a = dict(dy=A, lddy=64, y=B, ldy=64, rstd=C, g=None, b=None, dx=D, lddx=64, dg=None, db=None, ws=None,
@@ -174,6 +215,7 @@ def test_from_output_validation(lib):
     assert ln(ldy=10) == INVALID
     assert ln(H=0) == INVALID
     assert ln(dg=0x500000, db=0x500000 + 4) == INVALID
+    assert ln(b=D + 4) == INVALID       # beta under dx
     assert lib.rms_backward_from_output(A, 64, B, 64, None, None, D, 64, None, None, 0, 4, 64, BF16, BF16,
                                         None) == INVALID
     assert lib.rms_backward_from_output(A, 64, B, 64, C, None, B + 8, 64, None, None, 0, 4, 64, BF16, BF16,
