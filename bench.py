@@ -202,11 +202,12 @@ class ClockSampler:
 class Shape:
     """Device tensors of one (N, H) shape and argument tuples for the C ABI."""
 
-    def __init__(self, N, H, dev, seed, lib, extra=False, dtype="bf16"):
+    def __init__(self, N, H, dev, seed, lib, extra=False, dtype="bf16", x_offset=0.0, x_scale=1.0):
         import torch
         from rmsnorm_ln_fwd_gb300 import synth, ops
         self.N, self.H, self.lib, self.dev = N, H, lib, dev
-        host = synth.norm_inputs(N, H, dtype, seed=seed, with_residual=True, with_dh_stream=extra)
+        host = synth.norm_inputs(N, H, dtype, seed=seed, with_residual=True, with_dh_stream=extra,
+                                 x_offset=x_offset, x_scale=x_scale)
         self.code = {"f32": 0, "bf16": 1, "f16": 2}[dtype]
         self.esize = 4 if dtype == "f32" else 2
         self.host = host
@@ -277,6 +278,106 @@ class Shape:
                                          EPS_FUSED, BF, BF, stream)
         if st != 0:
             raise RuntimeError(f"{op} {N}x{H}: status {st}")
+
+
+# Every configuration of the workload's specification, timed call by call
+# after the step (the step itself is the C2 workload): (config, op, N, H,
+# row dtype, x offset, x scale).  C2's backwards are listed again so that
+# their main-kernel / partial-reduction split is reported too.
+CONFIGS = [
+    ("C1", "ln_fwd", 64, 256, "f32", 0.0, 1.0),
+    ("C1", "ln_bwd", 64, 256, "f32", 0.0, 1.0),
+    ("C2", "ln_bwd", 8192, 1024, "bf16", 0.0, 1.0),
+    ("C2", "rms_bwd", 8192, 1024, "bf16", 0.0, 1.0),
+    ("C2", "ln_bwd", 8192, 5120, "bf16", 0.0, 1.0),
+    ("C2", "rms_bwd", 8192, 5120, "bf16", 0.0, 1.0),
+    ("C2s", "ln_fwd", 8192, 1024, "f32", 1000.0, 1e-2),
+    ("C2s", "ln_bwd", 8192, 1024, "f32", 1000.0, 1e-2),
+    ("C2s", "rms_fwd", 8192, 1024, "f32", 1000.0, 1e-2),
+    ("C2s", "rms_bwd", 8192, 1024, "f32", 1000.0, 1e-2),
+    ("C3", "fused_fwd", 16384, 4096, "bf16", 0.0, 1.0),
+    ("C4", "ln_bwd", 32768, 1024, "bf16", 0.0, 1.0),
+    ("C4", "rms_bwd", 32768, 1024, "bf16", 0.0, 1.0),
+    ("C4", "ln_bwd", 16384, 2048, "bf16", 0.0, 1.0),
+    ("C4", "rms_bwd", 16384, 2048, "bf16", 0.0, 1.0),
+    ("C5", "ln_fwd", 2048, 16384, "bf16", 0.0, 1.0),
+    ("C5", "rms_fwd", 2048, 16384, "bf16", 0.0, 1.0),
+    ("C5", "ln_bwd", 2048, 16384, "bf16", 0.0, 1.0),
+    ("C5", "rms_bwd", 2048, 16384, "bf16", 0.0, 1.0),
+    ("C5", "ln_fwd", 512, 16384, "bf16", 0.0, 1.0),
+    ("C5", "rms_fwd", 512, 16384, "bf16", 0.0, 1.0),
+    ("C5", "ln_bwd", 512, 16384, "bf16", 0.0, 1.0),
+    ("C5", "rms_bwd", 512, 16384, "bf16", 0.0, 1.0),
+]
+
+
+def time_call(s, op, stream, flush, iters, split=False):
+    """Per-call device µs of `op` on shape `s`: L2 flushed before each call,
+    CUDA events on the launching stream.  With split, the backward's main
+    kernel and its partial reduction are timed apart (an event recorded
+    between them by the library; the reduction then runs as an ordinary
+    launch instead of a programmatic dependent one)."""
+    import ctypes
+    import torch
+    sh = stream.cuda_stream
+    if op in FORWARD_OF:
+        s.call(FORWARD_OF[op], sh)
+    for _ in range(3):
+        flush()
+        s.call(op, sh)
+    ev = []
+    for _ in range(iters):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        s.call(op, sh)
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    out = {"us_mean": round(statistics.fmean(us), 2), "us_median": round(statistics.median(us), 2),
+           "us_min": round(min(us), 2)}
+    if split:
+        sp = []
+        for _ in range(iters):
+            flush()
+            a, m, b = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            m.record(stream)  # creates the event's handle; the library records it again
+            a.record(stream)
+            s.lib.norm_set_bwd_split_event(ctypes.c_void_p(m.cuda_event))
+            s.call(op, sh)
+            b.record(stream)
+            sp.append((a, m, b))
+        s.lib.norm_set_bwd_split_event(None)
+        torch.cuda.synchronize()
+        out["main_us_mean"] = round(statistics.fmean(a.elapsed_time(m) * 1e3 for a, m, _ in sp), 2)
+        out["reduce_us_mean"] = round(statistics.fmean(m.elapsed_time(b) * 1e3 for _, m, b in sp), 2)
+        out["split_note"] = "main + reduce timed apart, the reduction launched without PDL"
+    return out
+
+
+def run_configs(lib, dev, stream, flush, peak, iters):
+    import torch
+    out = {}
+    cache = {}
+    for cfg, op, N, H, dt, off, scale in CONFIGS:
+        key = (N, H, dt, off, scale)
+        if key not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            cache[key] = Shape(N, H, dev, seed=11, lib=lib, dtype=dt, x_offset=off, x_scale=scale)
+        s = cache[key]
+        r = time_call(s, op, stream, flush, iters, split="bwd" in op)
+        byts = alg_bytes(op, N, H, s.esize, s.esize)
+        gbs = byts / (r["us_mean"] * 1e-6) / 1e9
+        r.update({"config": cfg, "op": op, "N": N, "H": H, "dtype": dt, "bytes": byts, "gbs": round(gbs, 1),
+                  "frac": round(gbs / peak, 3), "launches": LAUNCHES[op]})
+        if off:
+            r["x"] = f"{off:g} + {scale:g}*N(0,1)"
+        out[f"{cfg}_{op}_{dt}_{N}x{H}"] = r
+    cache.clear()
+    torch.cuda.empty_cache()
+    return out
 
 
 def step_calls(shapes):
@@ -365,6 +466,7 @@ def run_ours(args):
     traffic = recorded_traffic(dkey)
 
     e2e = run_e2e(args, shapes, stream, dev, world, dist)
+    configs = run_configs(lib, dev, stream, flush, peak, args.config_iters) if args.config_iters > 0 else None
     out = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -385,12 +487,13 @@ def run_ours(args):
         "frac_of_peak": round(value / world / peak, 3),
         "peak_gbs": peak,
         "peak_kind": peak_kind,
-        "bwd_us": {k.replace("_bwd", ""): v["us_mean"] for k, v in breakdown.items() if "_bwd_" in k},
+        "bwd_us": bwd_us(breakdown, configs),
         "breakdown": breakdown,
         "roofline": {"bound": "hbm", "kernel": dkey + (" (main + partial-reduce kernels)" if "bwd" in dop else ""),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3), "traffic": traffic,
                      "algorithmic_bytes": ds.bytes[dop], "peak_kind": f"{peak_kind} (hbm_gbs copy)"},
+        "configs": configs,
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": args.steps * sum(LAUNCHES[op] for _, op in calls),
@@ -401,6 +504,17 @@ def run_ours(args):
         print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def bwd_us(breakdown, configs):
+    """Backward µs (mean) per bf16 shape: the step's calls, then every bf16
+    backward of the configurations, with the main/reduce split where timed."""
+    out = {k.replace("_bwd", ""): {"us": v["us_mean"]} for k, v in breakdown.items() if "_bwd_" in k}
+    for k, v in (configs or {}).items():
+        if v["dtype"] == "bf16" and "_bwd" in v["op"]:
+            e = out.setdefault(f"{v['op'].replace('_bwd', '')}_{v['N']}x{v['H']}", {"us": v["us_mean"]})
+            e["main_us"], e["reduce_us"] = v["main_us_mean"], v["reduce_us_mean"]
+    return out
 
 
 OUT_NAMES = ("y", "mean", "rstd", "dx", "dg", "db", "yr", "rstd_r", "dxr", "dgr", "yf", "h", "rstd_f")
@@ -650,6 +764,102 @@ def run_profile_loop(args):
     print(json.dumps({"profiled": op, "N": N, "H": H, "iters": args.iters}))
 
 
+def run_calibrate(args):
+    """Reference points for the per-call numbers, under the same flush and
+    events: an almost empty kernel (the floor of an event-timed call), plain
+    device copies moving the bytes of the step's calls, back-to-back copies
+    over rotating buffers, and the host link (pinned host memory)."""
+    import torch
+    from rmsnorm_ln_fwd_gb300 import _build
+    _build.build()
+    import rmsnorm_ln_fwd_gb300 as nl
+    lib = nl.load_library()
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.current_stream(dev)
+    flush = L2Flush(dev)
+    peak, kind = measured_peak()
+
+    def timed(fn, iters=60, do_flush=True):
+        for _ in range(5):
+            if do_flush:
+                flush()
+            fn()
+        ev = []
+        for _ in range(iters):
+            if do_flush:
+                flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            fn()
+            b.record(st)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+        return round(statistics.fmean(us), 2), round(min(us), 2)
+
+    def emit(**kw):
+        print(json.dumps(kw), flush=True)
+
+    tiny = torch.zeros(1, device=dev)
+    m, mn = timed(lambda: tiny.add_(1))
+    emit(what="torch add on one element (the floor of an event-timed call)", us_mean=m, us_min=mn)
+    one = Shape(1, 256, dev, seed=0, lib=lib)
+    m, mn = timed(lambda: one.call("rms_fwd", st.cuda_stream))
+    emit(what="rms_forward on one row of 256 (one CTA)", us_mean=m, us_min=mn)
+    del one
+    for mib in (8, 16, 32, 40, 64, 80, 128, 256):
+        n = mib * (1 << 20) // 2
+        src = torch.ones(n, dtype=torch.bfloat16, device=dev)
+        dst = torch.empty_like(src)
+        m, mn = timed(lambda: dst.copy_(src))
+        byts = 4 * n
+        emit(what=f"device copy {mib} MiB -> {mib} MiB", bytes=byts, us_mean=m, us_min=mn,
+             gbs=round(byts / (m * 1e-6) / 1e9, 1), frac=round(byts / (m * 1e-6) / 1e9 / peak, 3))
+        del src, dst
+    n = 16 * (1 << 20) // 2
+    bufs = [(torch.ones(n, dtype=torch.bfloat16, device=dev), torch.empty(n, dtype=torch.bfloat16, device=dev))
+            for _ in range(16)]  # 512 MiB in all: every copy reads buffers L2 no longer holds
+    reps = 4
+    for _ in range(2):
+        for a_, b_ in bufs:
+            b_.copy_(a_)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush()
+    a.record(st)
+    for _ in range(reps):
+        for a_, b_ in bufs:
+            b_.copy_(a_)
+    b.record(st)
+    torch.cuda.synchronize()
+    per = a.elapsed_time(b) * 1e3 / (reps * len(bufs))
+    emit(what="device copy 16 MiB -> 16 MiB, 64 copies back to back over 16 buffer pairs", us_per_copy=round(per, 2),
+         frac=round(4 * n / (per * 1e-6) / 1e9 / peak, 3))
+    del bufs
+    n = 1 << 30
+    h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    h2 = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    d2 = torch.empty(n, dtype=torch.uint8, device=dev)
+    m, _ = timed(lambda: d.copy_(h, non_blocking=True), iters=5, do_flush=False)
+    emit(what="host -> device, 1 GiB from pinned memory", gbs=round(n / (m * 1e-6) / 1e9, 1), us_mean=m)
+    m, _ = timed(lambda: h.copy_(d, non_blocking=True), iters=5, do_flush=False)
+    emit(what="device -> host, 1 GiB to pinned memory", gbs=round(n / (m * 1e-6) / 1e9, 1), us_mean=m)
+    s2 = torch.cuda.Stream(dev)
+
+    def both():
+        ev0 = torch.cuda.Event()
+        ev0.record(st)
+        s2.wait_event(ev0)
+        d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+        st.wait_stream(s2)
+    m, _ = timed(both, iters=5, do_flush=False)
+    emit(what="both directions at once, 1 GiB each", gbs_each=round(n / (m * 1e-6) / 1e9, 1), us_mean=m)
+    emit(what="peak", hbm_gbs=peak, kind=kind)
+
+
 def main():
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
@@ -657,10 +867,14 @@ def main():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--config-iters", type=int, default=50,
+                   help="timed calls per configuration call after the step (0: skip the configs object)")
     p.add_argument("--cpu-rows", type=int, default=512)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--ref-rows", type=int, default=64)
     p.add_argument("--sweep", action="store_true", help="per-call timings over every configured shape")
+    p.add_argument("--calibrate", action="store_true",
+                   help="reference points: event floor, plain device copies, host link")
     p.add_argument("--sweep-iters", type=int, default=50)
     p.add_argument("--dtype", choices=["bf16", "f16", "f32"], default="bf16",
                    help="row dtype of --sweep / --profile-op (the step itself is bf16)")
@@ -675,6 +889,8 @@ def main():
         run_reference(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.calibrate:
+        run_calibrate(args)
     elif args.profile_op:
         run_profile_loop(args)
     else:

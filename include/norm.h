@@ -182,10 +182,15 @@ norm_status rms_backward(const void* dy, int64_t lddy, const void* x, int64_t ld
  * GPU that loads it, held until the process exits.  Nothing is allocated.
  * - Widths whose partial rows need more than that (when dgamma or dbeta is
  *   requested: norm_bwd_workspace_bytes(H, device) > the limit; H up to about
- *   27000 on a 152-SM GPU) are refused with NORM_ERR_WORKSPACE.
- * - The first call on each device looks up that device's copy of the array
- *   (cudaGetSymbolAddress, with the device current); make that first call
- *   before any stream capture.
+ *   27000 on a 152-SM GPU), or that the device cannot be asked to size, are
+ *   refused with NORM_ERR_WORKSPACE.
+ * - Every call looks up the current device's copy of the array
+ *   (cudaGetSymbolAddress, a host-side lookup).  Under lazy module loading
+ *   (CUDA's default) the 64 MiB are reserved when the library's device code
+ *   is first used on a device, which may be this call: make one set-up call
+ *   (N == 0 is enough) before any stream capture and before a framework takes
+ *   the device's memory.  If that reservation fails the call returns
+ *   NORM_ERR_CUDA and norm_last_error() names the failed step.
  * - Every call on a device shares the one array, which keeps the last call's
  *   contents; no part of it needs clearing, as each call writes every partial
  *   value before reading it.  Calls whose GPU work overlaps (other streams,

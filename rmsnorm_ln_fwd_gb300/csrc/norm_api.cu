@@ -60,6 +60,16 @@ void note_error(const char* where, cudaError_t e) {
   snprintf(t_last_error, sizeof(t_last_error), "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
 }
 
+}  // namespace
+
+namespace normk {
+// For the other translation units of the library (not part of the C ABI).
+void note_cuda_error(const char* where, cudaError_t e) { note_error(where, e); }
+void note_error_text(const char* text) { snprintf(t_last_error, sizeof(t_last_error), "%s", text); }
+}  // namespace normk
+
+namespace {
+
 bool device_info(int dev, DeviceInfo* out) {
   if (dev < 0 || dev >= kMaxDevices) return false;
   std::lock_guard<std::mutex> lock(g_mu);

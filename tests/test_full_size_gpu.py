@@ -1,10 +1,11 @@
 """The measured configurations at their full sizes, in the launch configuration
 the benchmark times (the auto kernel choice), against the fp64 oracle.
 
-Row-local outputs (y, mean, rstd, dx) are checked on a sample of rows -- the
-first, the last and 30 drawn at random -- by running the oracle on those rows
-alone.  The parameter gradients sum over every row, so the oracle computes
-them at full size; the fused add's stored h is checked bit for bit everywhere.
+Every row is checked: the oracle runs over the whole input in blocks of rows
+on the host, each block's row-local outputs (y, mean, rstd, dx) are compared
+element by element with the kernel's, and the blocks' parameter-gradient sums
+add up to the full-size dgamma/dbeta.  The fused add's stored h is checked
+bit for bit everywhere.
 """
 
 import numpy as np
@@ -31,20 +32,10 @@ def _gpu():
     nl.load_library()
 
 
-def _rows(N, seed):
-    r = np.random.default_rng(seed)
-    return np.unique(np.concatenate([[0, N - 1], r.choice(N, size=min(30, N), replace=False)]))
-
-
-def _col_sums(dy, xhat):
-    """Full-size dgamma/dbeta in fp64, streamed over row blocks."""
-    dg = np.zeros(dy.shape[1])
-    db = np.zeros(dy.shape[1])
-    for i in range(0, dy.shape[0], 2048):
-        d = dy[i:i + 2048].astype(np.float64)
-        dg += (d * xhat(i, i + 2048)).sum(axis=0)
-        db += d.sum(axis=0)
-    return dg, db
+def _blocks(N, rows=2048):
+    """[i, j) row blocks covering all N rows."""
+    for i in range(0, N, rows):
+        yield i, min(N, i + rows)
 
 
 CONFIGS = [(8192, 1024, BF), (8192, 5120, BF), (32768, 1024, BF), (16384, 2048, BF), (2048, 16384, BF),
@@ -59,22 +50,23 @@ def test_ln_full_size(N, H, dt):
     y, mean, rstd = nl.ln_forward(t["x"], t["gamma"], t["beta"], eps)
     dx, dg, db = nl.ln_backward(t["dy"], t["x"], mean, rstd, t["gamma"])
     torch.cuda.synchronize()
-    rows = _rows(N, N + H)
     x, dy = c["x"].double().numpy(), c["dy"].double().numpy()
     g, b = c["gamma"].double().numpy(), c["beta"].double().numpy()
-    xs, dys = x[rows], dy[rows]
-    yr, mr, rr = O.layer_norm_forward(xs, g, b, eps)
-    dxr, _, _ = O.layer_norm_backward(dys, xs, g, eps)
-    what = f"ln {N}x{H}"
-    check_out(np64(y[rows]), yr, ln_y_scale(xs, mr, rr, g, b), dt, what + " y rows")
-    check_mean(np64(mean[rows]), mr, xs, what + " mean rows")
-    check_rstd(np64(rstd[rows]), rr, what + " rstd rows")
-    check_out(np64(dx[rows]), dxr, ln_dx_scale(dys, xs, g, eps), dt, what + " dx rows")
-    mean_all, var_all = O.two_pass_stats(x)
-    r_all = 1.0 / np.sqrt(var_all + eps)
-    dgr, dbr = _col_sums(dy, lambda i, j: (x[i:j] - mean_all[i:j, None]) * r_all[i:j, None])
-    check_param(np64(dg), dgr, dt, what + " dgamma")
-    check_param(np64(db), dbr, dt, what + " dbeta")
+    yk, mk, rk, dxk = np64(y), np64(mean), np64(rstd), np64(dx)
+    dgr, dbr = np.zeros(H), np.zeros(H)
+    for i, j in _blocks(N):
+        xs, dys = x[i:j], dy[i:j]
+        yr, mr, rr = O.layer_norm_forward(xs, g, b, eps)
+        dxr, dgb, dbb = O.layer_norm_backward(dys, xs, g, eps)
+        dgr += dgb
+        dbr += dbb
+        what = f"ln {N}x{H} rows {i}..{j - 1}"
+        check_out(yk[i:j], yr, ln_y_scale(xs, mr, rr, g, b), dt, what + " y")
+        check_mean(mk[i:j], mr, xs, what + " mean")
+        check_rstd(rk[i:j], rr, what + " rstd")
+        check_out(dxk[i:j], dxr, ln_dx_scale(dys, xs, g, eps), dt, what + " dx")
+    check_param(np64(dg), dgr, dt, f"ln {N}x{H} dgamma")
+    check_param(np64(db), dbr, dt, f"ln {N}x{H} dbeta")
 
 
 @pytest.mark.parametrize("N,H,dt", CONFIGS, ids=[f"{n}x{h}{DT_NAME[d]}" for n, h, d in CONFIGS])
@@ -85,18 +77,19 @@ def test_rms_full_size(N, H, dt):
     y, rstd = nl.rms_forward(t["x"], t["gamma"], eps)
     dx, dg = nl.rms_backward(t["dy"], t["x"], rstd, t["gamma"])
     torch.cuda.synchronize()
-    rows = _rows(N, N + H + 1)
     x, dy, g = c["x"].double().numpy(), c["dy"].double().numpy(), c["gamma"].double().numpy()
-    xs, dys = x[rows], dy[rows]
-    yr, rr = O.rms_norm_forward(xs, g, eps)
-    dxr, _ = O.rms_norm_backward(dys, xs, g, eps)
-    what = f"rms {N}x{H}"
-    check_out(np64(y[rows]), yr, rms_y_scale(xs, rr, g), dt, what + " y rows")
-    check_rstd(np64(rstd[rows]), rr, what + " rstd rows")
-    check_out(np64(dx[rows]), dxr, rms_dx_scale(dys, xs, g, eps), dt, what + " dx rows")
-    r_all = 1.0 / np.sqrt((x * x).mean(axis=1) + eps)
-    dgr, _ = _col_sums(dy, lambda i, j: x[i:j] * r_all[i:j, None])
-    check_param(np64(dg), dgr, dt, what + " dgamma")
+    yk, rk, dxk = np64(y), np64(rstd), np64(dx)
+    dgr = np.zeros(H)
+    for i, j in _blocks(N):
+        xs, dys = x[i:j], dy[i:j]
+        yr, rr = O.rms_norm_forward(xs, g, eps)
+        dxr, dgb = O.rms_norm_backward(dys, xs, g, eps)
+        dgr += dgb
+        what = f"rms {N}x{H} rows {i}..{j - 1}"
+        check_out(yk[i:j], yr, rms_y_scale(xs, rr, g), dt, what + " y")
+        check_rstd(rk[i:j], rr, what + " rstd")
+        check_out(dxk[i:j], dxr, rms_dx_scale(dys, xs, g, eps), dt, what + " dx")
+    check_param(np64(dg), dgr, dt, f"rms {N}x{H} dgamma")
 
 
 def test_fused_full_size_16384x4096():
@@ -106,14 +99,12 @@ def test_fused_full_size_16384x4096():
     y, h, rstd = nl.fused_add_rms_forward(t["x"], t["residual"], t["gamma"], eps)
     torch.cuda.synchronize()
     x, res, g = c["x"].double().numpy(), c["residual"].double().numpy(), c["gamma"].double().numpy()
-    hn = np64(h)
-    for i in range(0, N, 2048):   # every element of the stored sum, bit for bit
-        want = O.round_to_dtype(O.round_to_float32(x[i:i + 2048] + res[i:i + 2048]), "bfloat16")
-        assert np.array_equal(hn[i:i + 2048], want), f"h rows {i}..: not bit-exact"
-    rows = _rows(N, 7)
-    yr, hr, rr = O.fused_add_rms_norm_forward(x[rows], res[rows], g, eps, DT_ORACLE[BF])
-    check_out(np64(y[rows]), yr, rms_y_scale(x[rows] + res[rows], rr, g), BF, "fused y rows")
-    check_rstd(np64(rstd[rows]), rr, "fused rstd rows")
+    hn, yk, rk = np64(h), np64(y), np64(rstd)
+    for i, j in _blocks(N):
+        yr, hr, rr = O.fused_add_rms_norm_forward(x[i:j], res[i:j], g, eps, DT_ORACLE[BF])
+        assert np.array_equal(hn[i:j], hr), f"h rows {i}..{j - 1}: not bit-exact"
+        check_out(yk[i:j], yr, rms_y_scale(x[i:j] + res[i:j], rr, g), BF, f"fused y rows {i}..{j - 1}")
+        check_rstd(rk[i:j], rr, f"fused rstd rows {i}..{j - 1}")
 
 
 def test_fused_backward_full_size_16384x4096():
@@ -127,16 +118,15 @@ def test_fused_backward_full_size_16384x4096():
     torch.cuda.synchronize()
     x, res = c["x"].double().numpy(), c["residual"].double().numpy()
     dy, dh, g = c["dy"].double().numpy(), c["dh_stream"].double().numpy(), c["gamma"].double().numpy()
-    rows = _rows(N, 9)
-    hs = O.round_to_dtype(O.round_to_float32(x[rows] + res[rows]), "bfloat16")
-    dhr, _ = O.fused_add_rms_norm_backward_from_h(dy[rows], hs, g, eps, dh[rows])
-    check_out(np64(dx[rows]), dhr, rms_dx_scale(dy[rows], hs, g, eps) + np.abs(dh[rows]), BF, "fused bwd dx rows")
+    dxk = np64(dx)
+    dgr = np.zeros(H)
+    for i, j in _blocks(N):
+        hs = O.round_to_dtype(O.round_to_float32(x[i:j] + res[i:j]), "bfloat16")
+        dhr, dgb = O.fused_add_rms_norm_backward_from_h(dy[i:j], hs, g, eps, dh[i:j])
+        dgr += dgb
+        check_out(dxk[i:j], dhr, rms_dx_scale(dy[i:j], hs, g, eps) + np.abs(dh[i:j]), BF,
+                  f"fused bwd dx rows {i}..{j - 1}")
     assert torch.equal(dx, dres)
-
-    def h_hat(i, j):
-        hb = O.round_to_dtype(O.round_to_float32(x[i:j] + res[i:j]), "bfloat16")
-        return hb / np.sqrt((hb * hb).mean(axis=1, keepdims=True) + eps)
-    dgr, _ = _col_sums(dy, h_hat)
     check_param(np64(dg), dgr, BF, "fused bwd dgamma")
 
 
@@ -152,14 +142,17 @@ def test_ln_backward_from_output_full_size_8192x5120():
     torch.cuda.synchronize()
     y, dy = c["x"].double().numpy(), c["dy"].double().numpy()
     g, b, r = c["gamma"].double().numpy(), c["beta"].double().numpy(), np64(rstd)
-    rows = _rows(N, 11)
-    dxr, _, _ = O.layer_norm_backward_from_output(dy[rows], y[rows], r[rows], g, b)
-    xh = (y[rows] - b) / g
-    gg = dy[rows] * g
-    scale = r[rows, None] * (np.abs(gg) + np.abs(gg).mean(1, keepdims=True) +
-                             np.abs(xh) * np.abs(gg * xh).mean(1, keepdims=True))
-    check_out(np64(dx[rows]), dxr, scale, BF, "from-output dx rows")
-    dgr, dbr = _col_sums(dy, lambda i, j: (y[i:j] - b) / g)
+    dxk = np64(dx)
+    dgr, dbr = np.zeros(H), np.zeros(H)
+    for i, j in _blocks(N):
+        dxr, dgb, dbb = O.layer_norm_backward_from_output(dy[i:j], y[i:j], r[i:j], g, b)
+        dgr += dgb
+        dbr += dbb
+        xh = (y[i:j] - b) / g
+        gg = dy[i:j] * g
+        scale = r[i:j, None] * (np.abs(gg) + np.abs(gg).mean(1, keepdims=True) +
+                                np.abs(xh) * np.abs(gg * xh).mean(1, keepdims=True))
+        check_out(dxk[i:j], dxr, scale, BF, f"from-output dx rows {i}..{j - 1}")
     check_param(np64(dg), dgr, BF, "from-output dgamma")
     check_param(np64(db), dbr, BF, "from-output dbeta")
 
@@ -189,6 +182,14 @@ def test_beyond_2pow31_elements():
     check_out(np64(y.index_select(0, idx)), yr, ln_y_scale(xs, mr, rr, g, b), BF, "2^31 y rows")
     check_rstd(np64(rstd.index_select(0, idx)), rr, "2^31 rstd rows")
     check_out(np64(dx.index_select(0, idx)), dxr, ln_dx_scale(dys, xs, g, eps), BF, "2^31 dx rows")
+    # Every other row: a row's outputs depend on that row alone, and the rows
+    # repeat the block, so each later block must equal the first bit for bit
+    # (the first block's last rows are among the sampled rows above).
+    for out in (y, mean, rstd, dx):
+        first = out[:B]
+        for i in range(B, N, B):
+            j = min(N, i + B)
+            assert torch.equal(out[i:j], first[:j - i]), f"2^31 rows {i}..{j - 1} differ from the first block"
     count = np.full(B, N // B, dtype=np.float64)
     count[:N % B] += 1
     _, dgb, dbb = O.layer_norm_backward(dyb * count[:, None], xb, g, eps)
