@@ -145,18 +145,6 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
   int parity = 0;
   int64_t row = (int64_t)prow * rpc + slot;
   if (row < a.N) fetch(row);  // first row in flight while gamma is staged
-  constexpr bool PF = kBwdL2PrefetchRows > 1;
-  auto l2_prefetch_row = [&](int64_t pr) {
-    l2_prefetch_bulk(reinterpret_cast<const T*>(a.x) + pr * a.ldx, (uint32_t)(H * sizeof(T)));
-    l2_prefetch_bulk(reinterpret_cast<const T*>(a.dy) + pr * a.lddy, (uint32_t)(H * sizeof(T)));
-  };
-  if constexpr (PF) {
-    if (t == 0) {
-#pragma unroll 1
-      for (int k = 2; k < kBwdL2PrefetchRows; ++k)
-        if (row + k * stride < a.N) l2_prefetch_row(row + k * stride);
-    }
-  }
 
   const int Hp = a.Hp;
   // Shared memory: group scratch | fp32 gamma (thread-interleaved, shared by
@@ -233,10 +221,6 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
       }
     }
     if (row + stride < a.N) fetch(row + stride);
-    if constexpr (PF) {
-      const int64_t pr = row + kBwdL2PrefetchRows * stride;
-      if (t == 0 && pr < a.N) l2_prefetch_row(pr);
-    }
     if constexpr (FUSED) {
       // The gradient through h is only added in pass 2: load it for this row
       // now, in flight over the row reduction, rather than a row ahead.
@@ -432,6 +416,224 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
     bwd_rows_body<KIND, D, VPT, MAXT, ACC_SMEM, CL>(part, a.H, crank);
   } else {
     bwd_rows_body<KIND, D, VPT, MAXT, ACC_SMEM, CL>(a, a.H, 0);
+  }
+}
+
+// Span backward (LayerNorm from x, rows of at most 256 threads): thread t of
+// a row group owns the contiguous columns [t*16, t*16 + 16) of every row it
+// visits, so a row's x, dy and dx each move in one 32-byte access a thread
+// (two in fp32), the next row's through incremented pointers, and every
+// shared-memory access is a constant offset from the thread's own slot.
+// gamma is staged as fp32 in shared memory, each thread's 16 values followed
+// by 4 floats of padding, so the 16-byte accesses of any eight consecutive
+// threads hit distinct banks; the dgamma/dbeta accumulators stay in registers.
+// The arithmetic and its order are those of bwd_rows_body (x_hat recentred by
+// its row mean).  It runs about a tenth fewer instructions an element than the
+// interleaved register rows; measured faster for narrow LayerNorm rows only
+// (8192x1024 bf16 main kernel 16.7 -> 14.3 us), so the launcher uses it there.
+// Requires H % 16 == 0 and 32-byte aligned rows.
+constexpr int kSpanCols = 16;
+constexpr int kSpanSlot = kSpanCols + 4;  // floats a thread's slot occupies in the shared arrays
+
+template <int KIND, typename D, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) bwd_span_kernel(const BwdArgs a) {
+  using T = typename D::T;
+  constexpr int E = kSpanCols;
+  constexpr int NP = E / 2;                    // fp32 pairs of a span
+  constexpr int NWD = E * (int)sizeof(T) / 4;  // 32-bit words of a span
+  constexpr int NL = NWD / 8;                  // 32-byte accesses of a span
+  constexpr int SW = kSpanSlot;
+  constexpr bool LN = KIND == KIND_LN;
+  constexpr int NS = LN ? 3 : 1;
+  static_assert(KIND == KIND_LN || KIND == KIND_RMS, "from x only");
+  extern __shared__ __align__(16) float sh_dyn[];
+  const int tpr = a.tpr;
+  const int rpc = blockDim.x / tpr;
+  const int slot = threadIdx.x / tpr;
+  const int t = threadIdx.x - slot * tpr;
+  const int nw = tpr >> 5;
+  const int wig = t >> 5;
+  const int lane = threadIdx.x & 31;
+  const int H = a.H;
+  const bool active = t * E < H;
+  const float inv_h = 1.f / (float)H;
+  const bool w_f32 = a.w_f32 != 0;
+  float* red = sh_dyn + slot * (2 * nw * NS);
+  float* gsh = sh_dyn + (((rpc * 2 * nw * NS) + 3) & ~3);  // [tpr][SW] fp32 gamma
+  const float* my_g = gsh + t * SW;
+
+  const int64_t stride = (int64_t)gridDim.x * rpc;
+  int64_t row = (int64_t)blockIdx.x * rpc + slot;
+  const size_t es = sizeof(T);
+  // Byte pointers to this thread's span; the fetch pointers run a row ahead.
+  const int64_t col0 = (int64_t)t * E;
+  const char* fx = reinterpret_cast<const char*>(a.x) + (row * a.ldx + col0) * es;
+  const char* fdy = reinterpret_cast<const char*>(a.dy) + (row * a.lddy + col0) * es;
+  char* dxp = reinterpret_cast<char*>(a.dx) + (row * a.lddx + col0) * es;
+  const int64_t sx_step = stride * a.ldx * (int64_t)es, sdy_step = stride * a.lddy * (int64_t)es,
+                sdx_step = stride * a.lddx * (int64_t)es;
+  uint32_t nx[NWD], nd[NWD];
+  float nrs = 0.f, nmu = 0.f;
+  auto fetch = [&](int64_t r) {
+    if (active) {
+#pragma unroll
+      for (int l = 0; l < NL; ++l) {
+        ld_stream32(fx + 32 * l, *reinterpret_cast<uint32_t(*)[8]>(nx + 8 * l));
+        ld_stream32(fdy + 32 * l, *reinterpret_cast<uint32_t(*)[8]>(nd + 8 * l));
+      }
+    }
+    nrs = a.rstd[r];
+    if (LN) nmu = a.mean[r];
+    fx += sx_step;
+    fdy += sdy_step;
+  };
+  if (row < a.N) fetch(row);  // first row in flight while gamma is staged
+
+  if (slot == 0) {  // every row slot owns the same columns
+#pragma unroll
+    for (int q = 0; q < E / 4; ++q) {
+      float4 g4 = make_float4(1.f, 1.f, 1.f, 1.f);
+      if (a.gamma != nullptr && active) {
+        const int c = (int)col0 + 4 * q;
+        if (w_f32) {
+          g4 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.gamma) + c);
+        } else {
+          const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const T*>(a.gamma) + c);
+          const uint32_t w[2] = {u.x, u.y};
+          const float2 lo = word_pair<D>(w, 0), hi = word_pair<D>(w, 1);
+          g4 = make_float4(lo.x, lo.y, hi.x, hi.y);
+        }
+      }
+      *reinterpret_cast<float4*>(gsh + t * SW + 4 * q) = g4;
+    }
+  }
+  float2 accg[NP], accb[LN ? NP : 1];
+#pragma unroll
+  for (int p = 0; p < NP; ++p) accg[p] = splat2(0.f);
+#pragma unroll
+  for (int p = 0; p < (LN ? NP : 1); ++p) accb[p] = splat2(0.f);
+  __syncthreads();
+
+  int parity = 0;
+  for (; row < a.N; row += stride) {
+    const float r = nrs;
+    const float2 r2 = splat2(r);
+    const float2 b2 = splat2(LN ? -nmu * r : 0.f);
+    float2 xh[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      const float2 xv = word_pair<D>(nx, p);
+      xh[p] = LN ? fma2(xv, r2, b2) : mul2(xv, r2);
+    }
+    uint32_t dcur[NWD];
+#pragma unroll
+    for (int w = 0; w < NWD; ++w) dcur[w] = nd[w];
+    if (row + stride < a.N) fetch(row + stride);
+
+    // Pass 1: sum(g), sum(g*x_hat) and (LayerNorm) sum(x_hat), g = dy*gamma.
+    float2 sg = splat2(0.f), sgx = splat2(0.f), sxh = splat2(0.f);
+    if (active) {
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q) {
+        const float4 g4 = *reinterpret_cast<const float4*>(my_g + 4 * q);
+        const float2 gm[2] = {make_float2(g4.x, g4.y), make_float2(g4.z, g4.w)};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int p = 2 * q + h;
+          const float2 g = mul2(word_pair<D>(dcur, p), gm[h]);
+          sgx = fma2(g, xh[p], sgx);
+          if (LN) {
+            sg = add2(sg, g);
+            sxh = add2(sxh, xh[p]);
+          }
+        }
+      }
+    }
+    float S[NS];
+    if (LN) {
+      S[0] = sg.x + sg.y;
+      S[1] = sgx.x + sgx.y;
+      S[NS - 1] = sxh.x + sxh.y;
+    } else {
+      S[0] = sgx.x + sgx.y;
+    }
+    group_sum<NS>(S, red, nw, wig, lane, 1 + slot, parity);
+    const float s0 = LN ? S[NS - 1] * inv_h : 0.f;
+    const float c1 = LN ? S[0] * inv_h : 0.f;
+    const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
+    const float2 s02 = splat2(s0), c12 = splat2(c1), nc22 = splat2(-c2);
+
+    // Pass 2: dx = rstd * (g - c1 - x_hat * c2) and the accumulators.
+    if (active) {
+      uint32_t out[NWD];
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q) {
+        const float4 g4 = *reinterpret_cast<const float4*>(my_g + 4 * q);
+        const float2 gm[2] = {make_float2(g4.x, g4.y), make_float2(g4.z, g4.w)};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int p = 2 * q + h;
+          const float2 d = word_pair<D>(dcur, p);
+          const float2 g = mul2(d, gm[h]);
+          const float2 xc = LN ? sub2(xh[p], s02) : xh[p];
+          pair_word<D>(out, p, mul2(fma2(xc, nc22, LN ? sub2(g, c12) : g), r2));
+          accg[p] = fma2(d, xc, accg[p]);
+          if (LN) accb[p] = add2(accb[p], d);
+        }
+      }
+#pragma unroll
+      for (int l = 0; l < NL; ++l) st_vec32(dxp + 32 * l, *reinterpret_cast<const uint32_t(*)[8]>(out + 8 * l));
+    }
+    dxp += sdx_step;
+    parity ^= 1;
+  }
+
+  if (a.ws == nullptr) return;
+  const int Hp = a.Hp;
+  float* pg = a.ws + (size_t)blockIdx.x * Hp;
+  float* pb = a.ws + ((size_t)gridDim.x + blockIdx.x) * Hp;
+  auto quad = [](const float2* v, int q) { return make_float4(v[2 * q].x, v[2 * q].y, v[2 * q + 1].x, v[2 * q + 1].y); };
+  if (rpc == 1) {
+    if (active) {
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q) {
+        *reinterpret_cast<float4*>(pg + col0 + 4 * q) = quad(accg, q);
+        if constexpr (LN) *reinterpret_cast<float4*>(pb + col0 + 4 * q) = quad(accb, q);
+      }
+    }
+    return;
+  }
+  // Several row slots: fold them in slot order through a [2][tpr][SW] buffer
+  // in the padded layout, then write the CTA's partial row.
+  float* fg = gsh + tpr * SW + t * SW;
+  float* fb = gsh + 2 * tpr * SW + t * SW;
+  for (int s2 = 0; s2 < rpc; ++s2) {
+    if (slot == s2 && active) {
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q) {
+        float4 g4 = quad(accg, q);
+        float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (LN) b4 = quad(accb, q);
+        if (s2 > 0) {
+          const float4 og = *reinterpret_cast<const float4*>(fg + 4 * q);
+          g4 = make_float4(og.x + g4.x, og.y + g4.y, og.z + g4.z, og.w + g4.w);
+          if constexpr (LN) {
+            const float4 ob = *reinterpret_cast<const float4*>(fb + 4 * q);
+            b4 = make_float4(ob.x + b4.x, ob.y + b4.y, ob.z + b4.z, ob.w + b4.w);
+          }
+        }
+        *reinterpret_cast<float4*>(fg + 4 * q) = g4;
+        if constexpr (LN) *reinterpret_cast<float4*>(fb + 4 * q) = b4;
+      }
+    }
+    __syncthreads();
+  }
+  if (slot == 0 && active) {
+#pragma unroll
+    for (int q = 0; q < E / 4; ++q) {
+      *reinterpret_cast<float4*>(pg + col0 + 4 * q) = *reinterpret_cast<const float4*>(fg + 4 * q);
+      if constexpr (LN) *reinterpret_cast<float4*>(pb + col0 + 4 * q) = *reinterpret_cast<const float4*>(fb + 4 * q);
+    }
   }
 }
 
@@ -754,75 +956,6 @@ __global__ void __launch_bounds__(256) bwd_param_reduce_kernel(const float* ws, 
   }
 }
 
-// The same sum with more CTAs: a CTA covers kRedColVecs column vectors (4
-// columns each) with kRedWarpsPerCol warps apiece; lane l of warp w of a
-// column vector sums partial rows l + 32w, l + 32w + 32*kRedWarpsPerCol, ...
-// (all loads issued before the adds), then a warp butterfly and a fixed-order
-// sum over the warps.  Same result up to fp32 summation order.
-#ifndef NORM_REDUCE_V2
-#define NORM_REDUCE_V2 0
-#endif
-constexpr int kRedColVecs = 2;
-constexpr int kRedWarpsPerCol = 4;
-constexpr int kRedRows = 4;  // partial rows a lane loads per batch
-
-template <typename D>
-__global__ void __launch_bounds__(256) bwd_param_reduce2_kernel(const float* ws, int P, int Hp, int H,
-                                                                void* dg, void* db, int w_f32) {
-  pdl_wait_primary();
-  const int which = blockIdx.y;
-  void* out = which ? db : dg;
-  if (out == nullptr) return;
-  const float* src = ws + (size_t)which * P * Hp;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cv = warp / kRedWarpsPerCol;            // column vector of this warp in the CTA
-  const int wr = warp - cv * kRedWarpsPerCol;       // warp rank within the column vector
-  const int col = (blockIdx.x * kRedColVecs + cv) * 4;
-  constexpr int RS = 32 * kRedWarpsPerCol;          // row stride of one lane
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (col < Hp) {
-    for (int p0 = lane + 32 * wr; p0 < P; p0 += RS * kRedRows) {
-      float4 v[kRedRows];
-#pragma unroll
-      for (int k = 0; k < kRedRows; ++k) {
-        const int p = p0 + RS * k;
-        v[k] = p < P ? *reinterpret_cast<const float4*>(src + (size_t)p * Hp + col) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int k = 0; k < kRedRows; ++k) {
-        acc.x += v[k].x;
-        acc.y += v[k].y;
-        acc.z += v[k].z;
-        acc.w += v[k].w;
-      }
-    }
-  }
-  float r[4] = {acc.x, acc.y, acc.z, acc.w};
-  warp_sum<4>(r);
-  __shared__ float4 sm[kRedColVecs * kRedWarpsPerCol];
-  if (lane == 0) sm[warp] = make_float4(r[0], r[1], r[2], r[3]);
-  __syncthreads();
-  if (threadIdx.x < kRedColVecs) {
-    const int c = (blockIdx.x * kRedColVecs + threadIdx.x) * 4;
-    float4 s4 = sm[threadIdx.x * kRedWarpsPerCol];
-    for (int k = 1; k < kRedWarpsPerCol; ++k) {
-      const float4 v = sm[threadIdx.x * kRedWarpsPerCol + k];
-      s4.x += v.x;
-      s4.y += v.y;
-      s4.z += v.z;
-      s4.w += v.w;
-    }
-    const float vals[4] = {s4.x, s4.y, s4.z, s4.w};
-    for (int i = 0; i < 4 && c + i < H; ++i) {
-      if (w_f32) {
-        reinterpret_cast<float*>(out)[c + i] = vals[i];
-      } else {
-        store_elem<D>(out, c + i, vals[i]);
-      }
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Host-side configuration.
 // ---------------------------------------------------------------------------
@@ -1039,6 +1172,33 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
     done = true;
    }
   }
+  // Span rows: half-precision LayerNorm rows of at most 256 threads at 16
+  // contiguous columns a thread (measured: LayerNorm 8192x1024 19.3 -> 17.2 us,
+  // 32768x1024 42.1 -> 40.6; RMSNorm gains nothing, wider rows lose).
+  if constexpr (KIND == KIND_LN && VEC == 8) {
+    auto al32 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
+    const bool aligned32 = al32(a.x) && al32(a.dy) && al32(a.dx) && (a.ldx * es) % 32 == 0 &&
+                           (a.lddy * es) % 32 == 0 && (a.lddx * es) % 32 == 0;
+    const int stpr = (a.H / kSpanCols + 31) / 32 * 32;
+    if (!done && dev.path == PATH_AUTO && aligned32 && a.H % kSpanCols == 0 && stpr <= 256 &&
+        (!a.gamma || (reinterpret_cast<uintptr_t>(a.gamma) & 15u) == 0)) {
+      const int srpc = 256 / stpr;
+      const int threads = srpc * stpr;
+      // group scratch | gamma [tpr][slot] | fold buffer [2][tpr][slot] (several row slots)
+      const size_t smem = ((size_t)((srpc * 2 * (stpr / 32) * NS + 3) & ~3) +
+                           (size_t)stpr * kSpanSlot * (srpc > 1 ? 3 : 1)) * sizeof(float);
+      a.tpr = stpr;
+      const int p_cap = (int)std::min<int64_t>((a.N + srpc - 1) / srpc, p_max);
+      auto kern = bwd_span_kernel<KIND, D, 256, 2>;
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+      P = std::max(1, std::min(p_cap, per_sm * dev.sm_count));
+      kern<<<P, threads, smem, s>>>(a);
+      err = cudaGetLastError();
+      done = true;
+    }
+  }
   // Register rows; the grid is persistent: as many CTAs as fit, at most
   // 2 x SM count (the partial rows the workspace holds).
   if (!done && use_rows) {
@@ -1089,8 +1249,7 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
     if (err != cudaSuccess) return err;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = NORM_REDUCE_V2 ? dim3((a.Hp + 4 * kRedColVecs - 1) / (4 * kRedColVecs), LN ? 2 : 1)
-                               : dim3((a.Hp + 31) / 32, LN ? 2 : 1);
+  cfg.gridDim = dim3((a.Hp + 31) / 32, LN ? 2 : 1);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
@@ -1101,8 +1260,7 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
   cfg.numAttrs = split ? 0 : 1;
   const float* ws = a.ws;
   void* dbeta = LN ? db : nullptr;
-  err = NORM_REDUCE_V2 ? cudaLaunchKernelEx(&cfg, bwd_param_reduce2_kernel<D>, ws, P, a.Hp, a.H, dg, dbeta, a.w_f32)
-                       : cudaLaunchKernelEx(&cfg, bwd_param_reduce_kernel<D>, ws, P, a.Hp, a.H, dg, dbeta, a.w_f32);
+  err = cudaLaunchKernelEx(&cfg, bwd_param_reduce_kernel<D>, ws, P, a.Hp, a.H, dg, dbeta, a.w_f32);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

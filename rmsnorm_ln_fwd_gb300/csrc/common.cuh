@@ -1,8 +1,9 @@
 // Device helpers shared by the forward and backward kernels of libnorm.
 //
-// Everything here is bandwidth plumbing: 128-bit global loads/stores, bf16
-// and fp16 packing, warp-shuffle reductions and the parallel Welford merge.  The
-// normalisation arithmetic itself lives in norm_fwd.cu / norm_bwd.cu.
+// Everything here is bandwidth plumbing: 128- and 256-bit global loads and
+// stores, bf16 and fp16 packing, warp-shuffle reductions, the parallel Welford
+// merge, mbarriers and bulk copies, and packed fp32 pairs.  The normalisation
+// arithmetic itself lives in fwd_kernels.cuh and bwd_kernels.cuh.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -314,15 +315,6 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 #define NORM_L2_PREFETCH_ROWS 2
 #endif
 constexpr int kL2PrefetchRows = NORM_L2_PREFETCH_ROWS;
-#ifndef NORM_L2_PREFETCH_FUSED
-#define NORM_L2_PREFETCH_FUSED 0
-#endif
-constexpr bool kL2PrefetchFused = NORM_L2_PREFETCH_FUSED != 0;
-// The same for the register-row backward (x and dy rows; 0: off).
-#ifndef NORM_BWD_L2_PREFETCH_ROWS
-#define NORM_BWD_L2_PREFETCH_ROWS 0
-#endif
-constexpr int kBwdL2PrefetchRows = NORM_BWD_L2_PREFETCH_ROWS;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -567,6 +559,49 @@ template <>
 __device__ __forceinline__ uint4 pack2<F16>(const float2* p) {
   return make_uint4(pack_f16x2(p[0].x, p[0].y), pack_f16x2(p[1].x, p[1].y), pack_f16x2(p[2].x, p[2].y),
                     pack_f16x2(p[3].x, p[3].y));
+}
+
+// ---------------------------------------------------------------------------
+// 32-byte global memory access (sm_100+ 256-bit vector loads and stores): one
+// instruction moves a thread's 16 half-precision (or 8 fp32) elements.  Loads
+// of streamed rows carry the same L1 no-allocate and L2 256-byte hints as
+// ld_stream.  Addresses must be 32-byte aligned.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ld_stream32(const void* p, uint32_t (&r)[8]) {
+  asm volatile("ld.global.L1::no_allocate.L2::256B.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ void st_vec32(void* p, const uint32_t (&r)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
+// 32-bit words <-> fp32 pairs.  A half-precision word holds one pair (element
+// 2p in the low half); fp32 takes two words a pair.
+template <typename D>
+__device__ __forceinline__ float2 word_pair(const uint32_t* w, int p) {
+  if constexpr (sizeof(typename D::T) == 4) {
+    return make_float2(__uint_as_float(w[2 * p]), __uint_as_float(w[2 * p + 1]));
+  } else if constexpr (std::is_same<typename D::T, __half>::value) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w[p]));
+  } else {
+    return make_float2(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xffff0000u));
+  }
+}
+
+template <typename D>
+__device__ __forceinline__ void pair_word(uint32_t* w, int p, float2 v) {
+  if constexpr (sizeof(typename D::T) == 4) {
+    w[2 * p] = __float_as_uint(v.x);
+    w[2 * p + 1] = __float_as_uint(v.y);
+  } else if constexpr (std::is_same<typename D::T, __half>::value) {
+    w[p] = pack_f16x2(v.x, v.y);
+  } else {
+    w[p] = pack_bf16x2(v.x, v.y);
+  }
 }
 
 // gamma/beta for the full vector at column c as pairs (p == nullptr: fill).

@@ -138,7 +138,7 @@ __device__ __forceinline__ void fwd_rows_body(const FwdArgs& a, const FwdArgs& a
   int parity = 0;
   int64_t row = (int64_t)prow * rpc + slot;
   if (row < a.N) fetch(row);  // first row in flight while the parameters are staged
-  constexpr bool PF = kL2PrefetchRows > 1 && (KIND != KIND_FUSED || kL2PrefetchFused);
+  constexpr bool PF = kL2PrefetchRows > 1 && KIND != KIND_FUSED;
   auto l2_prefetch_row = [&](int64_t pr) {
     l2_prefetch_bulk(reinterpret_cast<const T*>(a.x) + pr * a.ldx, (uint32_t)(H * sizeof(T)));
     if constexpr (KIND == KIND_FUSED)
@@ -617,6 +617,11 @@ template <int KIND, typename D, int VPT>
 static cudaError_t run_rows(const FwdArgs& a, int threads, int rpc, size_t smem, const DeviceInfo& dev,
                             cudaStream_t s) {
   const int64_t groups = (a.N + rpc - 1) / rpc;
+  // One warp a row at 32 elements a lane: three CTAs an SM (80 registers, no
+  // spills) keep more rows in flight than two (measured 8192x1024 bf16 LN
+  // 12.7 -> 12.3 us, RMS 10.9 -> 10.6); wider rows keep two.
+  if (threads <= 256 && VPT * D::VEC > 16 && a.tpr == 32)
+    return launch_rows(fwd_rows_kernel<KIND, D, VPT, 256, 3>, a, threads, smem, dev, groups, s);
   if (threads <= 256)
     return launch_rows(fwd_rows_kernel<KIND, D, VPT, 256, (VPT * D::VEC > 16 ? 2 : 3)>, a, threads, smem, dev,
                        groups, s);
