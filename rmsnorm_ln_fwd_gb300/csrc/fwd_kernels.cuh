@@ -113,7 +113,7 @@ __device__ __forceinline__ void fwd_rows_body(const FwdArgs& a, const FwdArgs& a
 #pragma unroll
   for (int v = 0; v < VPT; ++v) nvec += (t + v * tpr < hv) ? 1 : 0;
   uint4 nx[VPT], nr[VPT];
-  float npivot = 0.f;
+  uint4 npv = make_uint4(0u, 0u, 0u, 0u);  // LayerNorm: the next row's first 16-byte vector (its shift)
   auto fetch = [&](int64_t r) {
     const T* xrow = reinterpret_cast<const T*>(a.x) + r * a.ldx;
 #pragma unroll
@@ -123,16 +123,19 @@ __device__ __forceinline__ void fwd_rows_body(const FwdArgs& a, const FwdArgs& a
 #pragma unroll
       for (int v = 0; v < VPT; ++v) nr[v] = load_vec_or_zero<D>(rrow, (t + v * tpr) * VEC, H);
     }
-    if constexpr (KIND == KIND_LN) {
-      // The shift: the mean of the row's first 16-byte vector (one broadcast
-      // load), so that one outlying first element does not set it.
-      float f0[VEC];
-      unpack<D>(ld_cached(reinterpret_cast<const T*>(af.x) + r * af.ldx), f0);
-      float sum0 = 0.f;
+    // LayerNorm's shift is the mean of the row's first 16-byte vector (one
+    // broadcast load), so that one outlying first element does not set it.
+    // Only the load is issued here; the mean is formed when the row is used,
+    // so the load stays in flight over the current row like the row's own.
+    if constexpr (KIND == KIND_LN) npv = ld_cached(reinterpret_cast<const T*>(af.x) + r * af.ldx);
+  };
+  auto vector_mean = [](const uint4& u) {
+    float f0[VEC];
+    unpack<D>(u, f0);
+    float sum0 = 0.f;
 #pragma unroll
-      for (int i = 0; i < VEC; ++i) sum0 += f0[i];
-      npivot = sum0 * (1.f / VEC);
-    }
+    for (int i = 0; i < VEC; ++i) sum0 += f0[i];
+    return sum0 * (1.f / VEC);
   };
 
   int parity = 0;
@@ -179,7 +182,7 @@ __device__ __forceinline__ void fwd_rows_body(const FwdArgs& a, const FwdArgs& a
     float2 f[VPT][VP];
 #pragma unroll
     for (int v = 0; v < VPT; ++v) unpack2<D>(nx[v], f[v]);
-    const float pivot = npivot;
+    const float pivot = KIND == KIND_LN ? vector_mean(npv) : 0.f;
     if constexpr (KIND == KIND_FUSED) {
       T* hrow = reinterpret_cast<T*>(a.h) + row * a.ldh;
 #pragma unroll
