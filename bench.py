@@ -117,6 +117,53 @@ def recorded_traffic(op_key: str):
     return float(v) if v else None
 
 
+def record_traffic(paths, out_path):
+    """Write the per-call DRAM traffic table that roofline.traffic reads.
+
+    Each path is an ncu raw CSV (``--csv --page raw`` with the metrics
+    dram__bytes_read.sum and dram__bytes_write.sum) of one call captured with
+    ``bench.py --profile-op OP --shape NxH``, named ``traffic_OP_NxH.csv``;
+    the call's traffic is the sum over the launches captured (a backward: its
+    main kernel and its partial reduction).  The table records the digest of
+    the kernel sources it was taken on, computed here, so bench.py stops
+    reporting it once a source changes."""
+    import csv
+    rows = {}
+    for path in paths:
+        name = os.path.basename(path)
+        if not (name.startswith("traffic_") and name.endswith(".csv")):
+            raise ValueError(f"{path}: expected traffic_<op>_<N>x<H>.csv")
+        key = name[len("traffic_"):-len(".csv")]
+        with open(path) as f:
+            lines = [r for r in csv.reader(f)]
+        head = next(i for i, r in enumerate(lines) if r and r[0] == "ID")
+        h, units = lines[head], dict(zip(lines[head], lines[head + 1]))  # the row after the header: units
+        scale = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12,
+                 "kibyte": 1024, "mibyte": 1 << 20, "gibyte": 1 << 30}
+        total, launches = 0.0, 0
+        for r in lines[head + 2:]:
+            if len(r) != len(h):
+                continue
+            d = dict(zip(h, r))
+            for m in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+                total += float(d[m].replace(",", "")) * scale[units[m].strip().lower()]
+            launches += 1
+        if launches == 0:
+            raise ValueError(f"{path}: no captured launch")
+        rows[key] = (int(total), launches)
+    with open(out_path, "w") as f:
+        f.write("# DRAM read+write bytes per call (every kernel of the call, ncu dram__bytes_read.sum +\n")
+        f.write("# dram__bytes_write.sum, cold caches), written by `python bench.py --record-traffic` from\n")
+        f.write("# captures of `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none\n")
+        f.write("# -k regex:'fwd_|bwd_' -s <forward launches> -c <kernels of one call> --csv --page raw\n")
+        f.write("# python bench.py --profile-op OP --shape NxH --iters 2`.  Writes still dirty in L2 when a\n")
+        f.write("# kernel ends are not counted.  src_digest: the kernel sources the captures ran on.\n")
+        f.write(f"src_digest={src_digest()}\n")
+        for key in sorted(rows):
+            f.write(f"{key}={rows[key][0]}\n")
+    return rows
+
+
 class L2Flush:
     """Evicts L2 between timed calls: a write of a buffer larger than twice the
     L2 size, then a read of a second one of the same size.  The read pushes the
@@ -873,6 +920,9 @@ def main():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--ref-rows", type=int, default=64)
     p.add_argument("--sweep", action="store_true", help="per-call timings over every configured shape")
+    p.add_argument("--record-traffic", nargs="+", default=None, metavar="CSV",
+                   help="write the per-call DRAM traffic table from ncu captures named traffic_<op>_<N>x<H>.csv")
+    p.add_argument("--traffic-out", default=os.path.join(ROOT, "profiles", "roofline_traffic.txt"))
     p.add_argument("--calibrate", action="store_true",
                    help="reference points: event floor, plain device copies, host link")
     p.add_argument("--sweep-iters", type=int, default=50)
@@ -885,7 +935,9 @@ def main():
     args = p.parse_args()
     if args.impl == "ours" and not (args.sweep or args.profile_op):
         args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
-    if args.impl == "reference":
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.record_traffic, args.traffic_out)))
+    elif args.impl == "reference":
         run_reference(args)
     elif args.sweep:
         run_sweep(args)

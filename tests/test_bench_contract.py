@@ -93,3 +93,28 @@ def test_cpu_baseline_on_host_cores(monkeypatch):
     assert c["kind"] == "oracle" and c["unit"] == "GB/s" and c["cores"] == 2 and c["sample"]
     assert c["value"] > 0 and c["single_core"]["value"] > 0 and c["single_core"]["cores"] == 1
     assert c["value"] > 0.5 * c["single_core"]["value"]
+
+
+def test_record_traffic_sums_launches_in_base_units(tmp_path):
+    """The traffic table is computed from ncu's raw CSV (units row honoured,
+    every captured launch of the call summed) and stamped with the digest of
+    the kernel sources, which is what makes bench.py report it."""
+    csv = tmp_path / "traffic_ln_bwd_8192x5120.csv"
+    csv.write_text('"ID","Kernel Name","dram__bytes_read.sum","dram__bytes_write.sum"\n'
+                   '"","","Mbyte","Kbyte"\n'
+                   '"0","main","167.90","36700.5"\n'
+                   '"1","reduce","12.5","0"\n')
+    csv2 = tmp_path / "traffic_ln_fwd_8192x1024.csv"
+    csv2.write_text('"ID","Kernel Name","dram__bytes_read.sum","dram__bytes_write.sum"\n'
+                    '"","","byte","byte"\n'
+                    '"0","fwd","16777216","1000"\n')
+    out = tmp_path / "roofline_traffic.txt"
+    rows = bench.record_traffic([str(csv), str(csv2)], str(out))
+    assert rows["ln_bwd_8192x5120"] == (int(167.9e6 + 36700.5e3 + 12.5e6), 2)
+    assert rows["ln_fwd_8192x1024"] == (16777216 + 1000, 1)
+    kv = dict(line.strip().split("=", 1) for line in out.read_text().splitlines() if "=" in line and
+              not line.startswith("#"))
+    assert kv["src_digest"] == bench.src_digest()
+    assert int(kv["ln_bwd_8192x5120"]) == rows["ln_bwd_8192x5120"][0]
+    with pytest.raises(ValueError):
+        bench.record_traffic([str(tmp_path / "other.csv")], str(out))
