@@ -39,10 +39,6 @@
 
 namespace normk {
 
-#ifndef NORM_PDL_TRIGGER
-#define NORM_PDL_TRIGGER 0
-#endif
-
 // Register-row backward.  Persistent row groups walk rows row, row + stride,
 // ...; the next row's x, dy and saved statistics are loaded while the current
 // row computes.  Each thread owns fixed column vectors, so its dgamma/dbeta
@@ -149,7 +145,6 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
   int parity = 0;
   int64_t row = (int64_t)prow * rpc + slot;
   if (row < a.N) fetch(row);  // first row in flight while gamma is staged
-  if (NORM_PDL_TRIGGER == 1) pdl_launch_dependents();
 
   const int Hp = a.Hp;
   // Shared memory: group scratch | fp32 gamma (thread-interleaved, shared by
@@ -345,7 +340,6 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
     parity ^= 1;
   }
 
-  if (NORM_PDL_TRIGGER == 2) pdl_launch_dependents();
   if constexpr (CLUSTER) cluster_sync_all();  // no CTA leaves while its partner may still write to it
   if (a.ws == nullptr) return;
   // Fold the CTA's row groups into partial row prow.
@@ -494,7 +488,6 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_span_kernel(const BwdArgs a) {
     fdy += sdy_step;
   };
   if (row < a.N) fetch(row);  // first row in flight while gamma is staged
-  if (NORM_PDL_TRIGGER == 1) pdl_launch_dependents();
 
   if (slot == 0) {  // every row slot owns the same columns
 #pragma unroll
@@ -594,7 +587,6 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_span_kernel(const BwdArgs a) {
     dxp += sdx_step;
     parity ^= 1;
   }
-  if (NORM_PDL_TRIGGER == 2) pdl_launch_dependents();
 
   if (a.ws == nullptr) return;
   const int Hp = a.Hp;
@@ -749,7 +741,6 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
     if (row < a.N) issue(row, 0);
     if (row + stride < a.N) issue(row + stride, 1);
   }
-  if (NORM_PDL_TRIGGER == 1) pdl_launch_dependents();
   float nrs = 0.f, nmu = 0.f;
   if (row < a.N) {
     nrs = a.rstd[row];
@@ -852,7 +843,6 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
     dxp += sdx_step;
     parity ^= 1;
   }
-  if (NORM_PDL_TRIGGER == 2) pdl_launch_dependents();
   if (t == 0) {
     for (int b = 0; b < 2; ++b)
       if (issued[b] > 0) mbar_wait(&bar[b], (uint32_t)((issued[b] - 1) & 1), a.err, nullptr);

@@ -5,8 +5,8 @@
 //
 // Three kernel families (launch_fwd_typed picks one per call: register rows
 // while a row needs at most 640 threads, then the bulk-copy pipeline, then
-// register rows up to 1024 threads, then register rows shared by a cluster of
-// 2, 4 or 8 CTAs, then the loop):
+// register rows shared by a cluster of 2, 4 or 8 CTAs, then register rows of
+// up to 1024 threads for widths no cluster split divides, then the loop):
 //
 // * fwd_rows_kernel -- the row lives in registers.  A "row group" of `tpr`
 //   threads (one warp for narrow rows, up to 1024 threads for wide rows) owns
@@ -711,12 +711,17 @@ cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream_t s) {
   // copies of gamma (and beta) in shared memory.
   const bool staged_ok = vec_ok && staged_config(a.H, (int)es, NT, dev.max_smem_optin, (8 / NT) * VEC, &c,
                                                  KIND == KIND_LN ? 2 : 1);
-  bool use_rows = false, use_staged = false;
+  bool use_rows = false, use_staged = false, wide_rows = false;
   switch (dev.path) {
     case PATH_AUTO:
+      // Rows of more than 640 threads: the bulk-copy ring where it fits, then
+      // cluster rows (below), and one CTA of up to 1024 threads only for widths
+      // no cluster split divides (its 32-element threads spill; measured: LN
+      // 2048x24576 bf16 62.5 -> 49.3 us with clusters, fp32 fused 2048x16384
+      // 98.9 -> 85.2, RMS 2048x24576 43.4 -> 38.8).
       use_rows = rows_ok && tpr <= kRowsAutoMaxThreads;
       use_staged = !use_rows && staged_ok;
-      use_rows = use_rows || (!use_staged && rows_ok);
+      wide_rows = !use_rows && !use_staged && rows_ok;
       break;
     case PATH_ROWS: use_rows = rows_ok; break;
     case PATH_STAGED:
@@ -769,6 +774,16 @@ cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream_t s) {
       if (parts == 2) return run_rows_cluster<KIND, D, VPT_MAX, 2>(a, ptpr, psmem, s);
       if (parts == 4) return run_rows_cluster<KIND, D, VPT_MAX, 4>(a, ptpr, psmem, s);
       return run_rows_cluster<KIND, D, VPT_MAX, 8>(a, ptpr, psmem, s);
+    }
+  }
+  if (wide_rows) {
+    a.tpr = tpr;
+    switch (vpt) {
+      case 1: return run_rows<KIND, D, 1>(a, tpr, 1, rows_smem, dev, s);
+      case 2: return run_rows<KIND, D, 2>(a, tpr, 1, rows_smem, dev, s);
+      default:
+        if constexpr (VPT_MAX >= 4) return run_rows<KIND, D, 4>(a, tpr, 1, rows_smem, dev, s);
+        break;
     }
   }
   const int64_t blocks = std::min<int64_t>(a.N, (int64_t)dev.sm_count * 8);
