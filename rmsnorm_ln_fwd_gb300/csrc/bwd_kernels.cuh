@@ -696,6 +696,17 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
   const float* my_g = gsh + t * SW;
   unsigned char* bufs = smem_sb + L.bufs;
   const uint32_t row_bytes = (uint32_t)H * (uint32_t)es;
+  // The two 16-byte halves of a thread's span, in the order the thread holds
+  // them: threads 4..7 of every eight take the second half first, so the eight
+  // 16-byte shared-memory reads of a quarter warp cover all 32 banks once (in
+  // span order every bank is hit twice).  gamma, the accumulators, the partial
+  // row and the two 16-byte dx stores follow the same order.  Measured:
+  // LayerNorm 8192x5120 main kernel 52.0 -> 51.1 us, RMSNorm 44.9 -> 43.3,
+  // LayerNorm 4096x10240 55.7 -> 57.3.
+  constexpr bool SWZ = true;
+  const int half_a = SWZ ? 8 * ((t >> 2) & 1) : 0;  // columns of the first held half, from the span's start
+  const int half_b = 8 - half_a;
+  auto held_col = [&](int q) { return q < 2 ? half_a + 4 * q : half_b + 4 * (q - 2); };  // float4 quad q
 
   if (t == 0) {
     mbar_init(&bar[0], 1);
@@ -707,7 +718,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
   for (int q = 0; q < E / 4; ++q) {
     float4 g4 = make_float4(1.f, 1.f, 1.f, 1.f);
     if (a.gamma != nullptr && active) {
-      const int c = t * E + 4 * q;
+      const int c = t * E + held_col(q);
       if (w_f32) {
         g4 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.gamma) + c);
       } else {
@@ -770,8 +781,9 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
     if (active) {
 #pragma unroll
       for (int l = 0; l < 2 * NL; ++l) {
-        const uint4 ux = lds16(bx + 16 * l);
-        const uint4 ud = lds16(bx + L.buf_bytes + 16 * l);
+        const int off = (l == 0 ? half_a : half_b) * (int)es;
+        const uint4 ux = lds16(bx + off);
+        const uint4 ud = lds16(bx + L.buf_bytes + off);
         xw[4 * l] = ux.x; xw[4 * l + 1] = ux.y; xw[4 * l + 2] = ux.z; xw[4 * l + 3] = ux.w;
         dw[4 * l] = ud.x; dw[4 * l + 1] = ud.y; dw[4 * l + 2] = ud.z; dw[4 * l + 3] = ud.w;
       }
@@ -836,8 +848,13 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
         }
       }
       if (ok) {
+        if constexpr (SWZ) {
+          st_vec(dxp + half_a * (int)es, make_uint4(out[0], out[1], out[2], out[3]));
+          st_vec(dxp + half_b * (int)es, make_uint4(out[4], out[5], out[6], out[7]));
+        } else {
 #pragma unroll
-        for (int l = 0; l < NL; ++l) st_vec32(dxp + 32 * l, *reinterpret_cast<const uint32_t(*)[8]>(out + 8 * l));
+          for (int l = 0; l < NL; ++l) st_vec32(dxp + 32 * l, *reinterpret_cast<const uint32_t(*)[8]>(out + 8 * l));
+        }
       }
     }
     dxp += sdx_step;
@@ -852,10 +869,10 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
   float* pb = a.ws + ((size_t)gridDim.x + blockIdx.x) * a.Hp + (size_t)t * E;
 #pragma unroll
   for (int q = 0; q < E / 4; ++q) {
-    *reinterpret_cast<float4*>(pg + 4 * q) =
+    *reinterpret_cast<float4*>(pg + held_col(q)) =
         make_float4(accg[2 * q].x, accg[2 * q].y, accg[2 * q + 1].x, accg[2 * q + 1].y);
     if constexpr (LN)
-      *reinterpret_cast<float4*>(pb + 4 * q) =
+      *reinterpret_cast<float4*>(pb + held_col(q)) =
           make_float4(accb[2 * q].x, accb[2 * q].y, accb[2 * q + 1].x, accb[2 * q + 1].y);
   }
 }
