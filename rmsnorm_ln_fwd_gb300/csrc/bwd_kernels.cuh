@@ -267,9 +267,12 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
     const float s0 = RECENTER ? S[NS - 1] * inv_h : 0.f;
     const float c1 = LN ? S[0] * inv_h : 0.f;
     const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
-    const float2 s02 = splat2(s0), c12 = splat2(c1), nc22 = splat2(-c2);
+    const float2 s02 = splat2(s0), nc22 = splat2(-c2);
+    const float2 na2 = splat2(-c2 * r), nb2 = splat2(-c1 * r);
 
-    // Pass 2: dx = rstd * (g - c1 - x_hat * c2) and the accumulators.
+    // Pass 2: dx = rstd * (g - c1 - x_hat * c2) and the accumulators
+    // (LayerNorm as (-c2*rstd)*x_hat + (g*rstd - c1*rstd): two f32x2
+    // instructions a pair).
     T* dxrow = reinterpret_cast<T*>(a.dx) + row * a.lddx;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
@@ -298,7 +301,8 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
         for (int p = 0; p < VP; ++p) {
           const float2 xc = RECENTER ? sub2(xh[v][p], s02) : xh[v][p];
           const float2 g = mul2(d[p], gm[p]);
-          out[p] = mul2(fma2(xc, nc22, LN ? sub2(g, c12) : g), r2);
+          if constexpr (LN) out[p] = fma2(xc, na2, fma2(g, r2, nb2));
+          else out[p] = mul2(fma2(xc, nc22, g), r2);
           ag[p] = fma2(d[p], xc, ag[p]);
           if (LN) ab[p] = add2(ab[p], d[p]);
         }
@@ -563,7 +567,8 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_span_kernel(const BwdArgs a) {
     const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
     const float2 s02 = splat2(s0), c12 = splat2(c1), nc22 = splat2(-c2);
 
-    // Pass 2: dx = rstd * (g - c1 - x_hat * c2) and the accumulators.
+    // Pass 2: dx = rstd * (g - c1 - x_hat * c2) and the accumulators (in
+    // this order: the shorter form of the wider kernels spills here).
     if (active) {
       uint32_t out[NWD];
 #pragma unroll
@@ -651,18 +656,24 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_span_kernel(const BwdArgs a) {
 // Every wait is bounded; a wait that runs out sets the error word and stops
 // new copies, and the issuing thread drains its copies before the CTA exits.
 
+// Row buffers (rows in flight a CTA): RMSNorm, with less arithmetic a row,
+// waits on memory more and gains from a third (measured 8192x5120 bf16 45.6 ->
+// 43.0 us); LayerNorm does not (53.3 -> 54.5).
+template <int KIND>
+__host__ __device__ constexpr int spanb_bufs() { return KIND == KIND_RMS ? 3 : 2; }
+
 struct SpanBLayout {
   int bars, abort, red, gamma, bufs, buf_bytes, total;
 };
-__host__ __device__ inline SpanBLayout spanb_layout(int tpr, int H, int es, int NS) {
+__host__ __device__ inline SpanBLayout spanb_layout(int tpr, int H, int es, int NS, int NB) {
   SpanBLayout L;
   L.bars = 0;
-  L.abort = 16;
-  L.red = 32;
+  L.abort = 8 * NB;
+  L.red = (L.abort + 4 + 15) & ~15;
   L.gamma = (L.red + 4 * 2 * (tpr / 32) * NS + 15) & ~15;
   L.bufs = (L.gamma + 4 * tpr * kSpanSlot + 127) & ~127;
   L.buf_bytes = (H * es + 127) & ~127;
-  L.total = L.bufs + 4 * L.buf_bytes;  // [2 buffers][x, dy]
+  L.total = L.bufs + 2 * NB * L.buf_bytes;  // [buffers][x, dy]
   return L;
 }
 
@@ -688,7 +699,8 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
   const float inv_h = 1.f / (float)H;
   const bool w_f32 = a.w_f32 != 0;
   const size_t es = sizeof(T);
-  const SpanBLayout L = spanb_layout(tpr, H, (int)es, NS);
+  constexpr int NB = spanb_bufs<KIND>();
+  const SpanBLayout L = spanb_layout(tpr, H, (int)es, NS, NB);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem_sb + L.bars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_sb + L.abort);
   float* red = reinterpret_cast<float*>(smem_sb + L.red);
@@ -709,8 +721,8 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
   auto held_col = [&](int q) { return q < 2 ? half_a + 4 * q : half_b + 4 * (q - 2); };  // float4 quad q
 
   if (t == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) mbar_init(&bar[b], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -734,7 +746,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
 
   const int64_t stride = gridDim.x;
   int64_t row = blockIdx.x;
-  int issued[2] = {0, 0};
+  unsigned used = 0u, fills = 0u;  // per buffer: ever filled; fills issued, mod 2
   auto issue = [&](int64_t r, int b) {
     unsigned char* dst = bufs + (size_t)b * 2 * L.buf_bytes;
     const void* sx = reinterpret_cast<const T*>(a.x) + r * a.ldx;
@@ -746,11 +758,13 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
     mbar_arrive_expect_tx(&bar[b], 2 * row_bytes);
     bulk_g2s(dst, sx, row_bytes, &bar[b]);
     bulk_g2s(dst + L.buf_bytes, sd, row_bytes, &bar[b]);
-    ++issued[b];
+    used |= 1u << b;
+    fills ^= 1u << b;
   };
   if (t == 0) {
-    if (row < a.N) issue(row, 0);
-    if (row + stride < a.N) issue(row + stride, 1);
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+      if (row + b * stride < a.N) issue(row + b * stride, b);
   }
   float nrs = 0.f, nmu = 0.f;
   if (row < a.N) {
@@ -767,7 +781,8 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
 
   int parity = 0;
   for (int k = 0; row < a.N; row += stride, ++k) {
-    const int b = k & 1;
+    const int b = k % NB;  // this row's buffer; (k / NB) mod 2 is the parity of its fill
+    const int ph = (k / NB) & 1;
     const float r = nrs;
     const float2 r2 = splat2(r);
     const float2 b2 = splat2(LN ? -nmu * r : 0.f);
@@ -775,7 +790,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
       nrs = a.rstd[row + stride];
       if (LN) nmu = a.mean[row + stride];
     }
-    const bool ok = mbar_wait(&bar[b], (uint32_t)((k >> 1) & 1), a.err, abort_flag);
+    const bool ok = mbar_wait(&bar[b], (uint32_t)ph, a.err, abort_flag);
     const unsigned char* bx = bufs + (size_t)b * 2 * L.buf_bytes + (size_t)t * E * es;
     uint32_t xw[NWD], dw[NWD];
     if (active) {
@@ -821,15 +836,19 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
       S[0] = sgx.x + sgx.y;
     }
     group_sum<NS>(S, red, nw, wig, lane, 1, parity);
-    // Every thread has read buffer b: refill it with the row two ahead.
-    if (t == 0 && row + 2 * stride < a.N && !*abort_flag) {
+    // Every thread has read buffer b: refill it with the row NB ahead.
+    if (t == 0 && row + NB * stride < a.N && !*abort_flag) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(row + 2 * stride, b);
+      issue(row + NB * stride, b);
     }
     const float s0 = LN ? S[NS - 1] * inv_h : 0.f;
     const float c1 = LN ? S[0] * inv_h : 0.f;
     const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
-    const float2 s02 = splat2(s0), c12 = splat2(c1), nc22 = splat2(-c2);
+    // LayerNorm: dx = r*(g - c1 - c2*xc) taken as (-c2*r)*xc + (g*r - c1*r),
+    // two f32x2 instructions a pair after xc (measured 8192x5120 bf16 main
+    // kernel 50.9 -> 49.0 us).
+    const float2 s02 = splat2(s0), nc22 = splat2(-c2);
+    const float2 na2 = splat2(-c2 * r), nb2 = splat2(-c1 * r);
     if (active) {
       uint32_t out[NWD];
 #pragma unroll
@@ -842,7 +861,8 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
           const float2 d = word_pair<D>(dw, p);
           const float2 g = mul2(d, gm[h]);
           const float2 xc = LN ? sub2(xh[p], s02) : xh[p];
-          pair_word<D>(out, p, mul2(fma2(xc, nc22, LN ? sub2(g, c12) : g), r2));
+          if constexpr (LN) pair_word<D>(out, p, fma2(xc, na2, fma2(g, r2, nb2)));
+          else pair_word<D>(out, p, mul2(fma2(xc, nc22, g), r2));
           accg[p] = fma2(d, xc, accg[p]);
           if (LN) accb[p] = add2(accb[p], d);
         }
@@ -861,8 +881,8 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
     parity ^= 1;
   }
   if (t == 0) {
-    for (int b = 0; b < 2; ++b)
-      if (issued[b] > 0) mbar_wait(&bar[b], (uint32_t)((issued[b] - 1) & 1), a.err, nullptr);
+    for (int q = 0; q < NB; ++q)  // the last fill of buffer q has parity (fills - 1) mod 2
+      if ((used >> q) & 1u) mbar_wait(&bar[q], ((fills >> q) & 1u) ^ 1u, a.err, nullptr);
   }
   if (a.ws == nullptr || !active) return;
   float* pg = a.ws + (size_t)blockIdx.x * a.Hp + (size_t)t * E;
@@ -1446,7 +1466,7 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
     const bool aligned32 = al32(a.x) && al32(a.dy) && al32(a.dx) && (a.ldx * es) % 32 == 0 &&
                            (a.lddy * es) % 32 == 0 && (a.lddx * es) % 32 == 0;
     const int stpr = (a.H / kSpanCols + 31) / 32 * 32;
-    const SpanBLayout SL = spanb_layout(stpr, a.H, (int)es, NS);
+    const SpanBLayout SL = spanb_layout(stpr, a.H, (int)es, NS, spanb_bufs<KIND>());
     if (!done && dev.path == PATH_AUTO && aligned32 && a.H % kSpanCols == 0 && stpr > 256 && stpr <= 640 &&
         (size_t)SL.total <= (size_t)dev.max_smem_optin &&
         (!a.gamma || (reinterpret_cast<uintptr_t>(a.gamma) & 15u) == 0)) {
