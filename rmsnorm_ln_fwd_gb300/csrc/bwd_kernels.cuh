@@ -256,7 +256,10 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& a, int h_full, int 
     } else {
       S[0] = sgx.x + sgx.y;
     }
-    group_sum<NS>(S, sh, nw, wig, lane, bar_id, parity);
+    // Cluster parts have at most 16 warps: a compile-time butterfly for the
+    // one-value sums (measured RMSNorm 2048x16384 bf16 43.3 -> 42.1 us,
+    // 1024x32768 47.1 -> 45.5; the LayerNorm sums gain nothing).
+    group_sum<NS, (CL > 1 && NS == 1) ? 16 : 0>(S, sh, nw, wig, lane, bar_id, parity);
     if constexpr (CLUSTER) {  // identical sums in every part
       cluster_group_sum_async<NS, CL>(S, xch[parity], &xbar[parity], (it >> 1) & 1u, crank, a.err, &xabort);
       ++it;
@@ -439,7 +442,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_rows_kernel(const BwdArgs a) {
 constexpr int kSpanCols = 16;
 constexpr int kSpanSlot = kSpanCols + 4;  // floats a thread's slot occupies in the shared arrays
 
-template <int KIND, typename D, int MAXT, int MINB>
+template <int KIND, typename D, int MAXT, int MINB, int PW = 0>
 __global__ void __launch_bounds__(MAXT, MINB) bwd_span_kernel(const BwdArgs a) {
   using T = typename D::T;
   constexpr int E = kSpanCols;
@@ -561,7 +564,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_span_kernel(const BwdArgs a) {
     } else {
       S[0] = sgx.x + sgx.y;
     }
-    group_sum<NS>(S, red, nw, wig, lane, 1 + slot, parity);
+    group_sum<NS, PW>(S, red, nw, wig, lane, 1 + slot, parity);
     const float s0 = LN ? S[NS - 1] * inv_h : 0.f;
     const float c1 = LN ? S[0] * inv_h : 0.f;
     const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
@@ -677,7 +680,7 @@ __host__ __device__ inline SpanBLayout spanb_layout(int tpr, int H, int es, int 
   return L;
 }
 
-template <int KIND, typename D, int MAXT, int MINB>
+template <int KIND, typename D, int MAXT, int MINB, int PW>
 __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) {
   using T = typename D::T;
   constexpr int E = kSpanCols;
@@ -835,7 +838,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
     } else {
       S[0] = sgx.x + sgx.y;
     }
-    group_sum<NS>(S, red, nw, wig, lane, 1, parity);
+    group_sum<NS, PW>(S, red, nw, wig, lane, 1, parity);
     // Every thread has read buffer b: refill it with the row NB ahead.
     if (t == 0 && row + NB * stride < a.N && !*abort_flag) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1462,7 +1465,13 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
                            (size_t)stpr * kSpanSlot * (srpc > 1 ? 3 : 1)) * sizeof(float);
       a.tpr = stpr;
       const int p_cap = (int)std::min<int64_t>((a.N + srpc - 1) / srpc, p_max);
+      // The row reduction's cross-warp butterfly over a compile-time lane count
+      // where the row takes 2, 4 or 5..8 warps (measured LayerNorm bf16
+      // 8192x1024 17.7 -> 17.1 us, 16384x2048 40.8 -> 40.1, 8192x4096 42.5 -> 41.6).
       auto kern = bwd_span_kernel<KIND, D, 256, 2>;
+      if (stpr == 64) kern = bwd_span_kernel<KIND, D, 256, 2, 2>;
+      else if (stpr == 128) kern = bwd_span_kernel<KIND, D, 256, 2, 4>;
+      else if (stpr > 128) kern = bwd_span_kernel<KIND, D, 256, 2, 8>;
       int per_sm = 0;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
         per_sm = 1;
@@ -1483,7 +1492,10 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
     if (!done && dev.path == PATH_AUTO && aligned32 && a.H % kSpanCols == 0 && stpr > 256 && stpr <= 640 &&
         (size_t)SL.total <= (size_t)dev.max_smem_optin &&
         (!a.gamma || (reinterpret_cast<uintptr_t>(a.gamma) & 15u) == 0)) {
-      auto kern = bwd_spanb_kernel<KIND, D, 640, 1>;
+      // The row reduction's cross-warp butterfly over a compile-time lane count
+      // (measured LayerNorm 8192x5120 bf16 53.2 -> 51.9 us, 4096x8192 49.4 ->
+      // 48.2, 8192x6144 71.7 -> 69.7; the wide forward gains nothing from it).
+      auto kern = stpr <= 512 ? bwd_spanb_kernel<KIND, D, 640, 1, 16> : bwd_spanb_kernel<KIND, D, 640, 1, 32>;
       if (SL.total > 48 * 1024) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SL.total);
       }

@@ -264,8 +264,11 @@ __device__ __forceinline__ float warp_sum_scatter(const float (&v)[K], int lane)
 // barrier).  After the barrier, lane k picks up warp (k mod P)'s partial, P
 // the power of two >= nw (0 past nw), and a butterfly over groups of P lanes
 // finishes the sum in log2(P) steps, in a fixed order, identical in every
-// thread (each group of P lanes holds the same values).
-template <int K>
+// thread (each group of P lanes holds the same values).  PW > 0: a power of
+// two >= nw known at compile time, taken as P (the butterfly unrolled with no
+// per-step tests; lanes past nw add exact zeros, so the sums are those of the
+// runtime P up to the sign of a zero total).
+template <int K, int PW = 0>
 __device__ __forceinline__ void group_sum(float (&v)[K], float* sh, int nw, int wig, int lane,
                                           int bar_id, int parity) {
   float* buf = sh + parity * nw * K;
@@ -287,11 +290,22 @@ __device__ __forceinline__ void group_sum(float (&v)[K], float* sh, int nw, int 
     }
   }
   named_barrier(bar_id, nw * 32);
-  const int P = pow2_ceil(nw);
-  const int src = lane & (P - 1);
+  if constexpr (PW > 0) {
+    const int src = lane & (PW - 1);
 #pragma unroll
-  for (int k = 0; k < K; ++k) v[k] = src < nw ? buf[src * K + k] : 0.f;
-  warp_sum_pow2<K>(v, P);
+    for (int k = 0; k < K; ++k) v[k] = src < nw ? buf[src * K + k] : 0.f;
+#pragma unroll
+    for (int off = PW >> 1; off > 0; off >>= 1) {
+#pragma unroll
+      for (int k = 0; k < K; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], off);
+    }
+  } else {
+    const int P = pow2_ceil(nw);
+    const int src = lane & (P - 1);
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] = src < nw ? buf[src * K + k] : 0.f;
+    warp_sum_pow2<K>(v, P);
+  }
 }
 
 // Welford accumulator (count, mean, M2) and the parallel merge of

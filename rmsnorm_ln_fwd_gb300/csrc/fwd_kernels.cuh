@@ -863,11 +863,14 @@ template <int KIND, typename D, int NCH>
 static cudaError_t run_wide(const FwdArgs& a, int threads, int rpc, size_t smem, const DeviceInfo& dev,
                             cudaStream_t s) {
   const int64_t groups = (a.N + rpc - 1) / rpc;
-  if (a.tpr == 32)
-    return launch_rows(fwd_wide_kernel<KIND, D, NCH, 256, (KIND == KIND_LN ? 2 : 3)>, a, threads, smem, dev, groups,
-                       s);
-  if (threads <= 256) return launch_rows(fwd_wide_kernel<KIND, D, NCH, 256, 2>, a, threads, smem, dev, groups, s);
-  return launch_rows(fwd_wide_kernel<KIND, D, NCH, 640, 1>, a, threads, smem, dev, groups, s);
+  constexpr int W1_MINB = KIND == KIND_LN ? 2 : 3;
+  if constexpr (NCH == 1) {  // one chunk a lane: one-warp rows only
+    return launch_rows(fwd_wide_kernel<KIND, D, NCH, 256, W1_MINB>, a, threads, smem, dev, groups, s);
+  } else {
+    if (a.tpr == 32) return launch_rows(fwd_wide_kernel<KIND, D, NCH, 256, W1_MINB>, a, threads, smem, dev, groups, s);
+    if (threads <= 256) return launch_rows(fwd_wide_kernel<KIND, D, NCH, 256, 2>, a, threads, smem, dev, groups, s);
+    return launch_rows(fwd_wide_kernel<KIND, D, NCH, 640, 1>, a, threads, smem, dev, groups, s);
+  }
 }
 
 template <int KIND, typename D, int VPT, int CL>
