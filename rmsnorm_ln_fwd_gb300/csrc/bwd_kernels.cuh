@@ -646,14 +646,16 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_span_kernel(const BwdArgs a) {
 }
 
 // Span rows with the next rows in shared memory (half-precision LayerNorm
-// and RMSNorm from x, one row a CTA of 257..640 threads): the column
-// ownership and the arithmetic of bwd_span_kernel, but no registers hold a row
-// in flight: one thread of the CTA bulk-copies the next two rows of x and dy
-// into a double buffer in shared memory, completing on the buffer's mbarrier,
-// and refills a buffer once the row reduction's barrier has passed (every
-// thread has then read it).  That leaves room for both accumulators in
-// registers at two CTAs an SM (96 registers, no spills), where the span kernel
-// with its register prefetch had to keep dgamma in shared memory.  Measured:
+// and RMSNorm, from x or from the saved output, one row a CTA of 257..640
+// threads): the column ownership and the arithmetic of bwd_span_kernel, but
+// no registers hold a row in flight: one thread of the CTA bulk-copies the
+// next rows of x (or y) and dy into row buffers in shared memory, completing
+// on the buffer's mbarrier, and refills a buffer once the row reduction's
+// barrier has passed (every thread has then read it).  That leaves room for
+// both accumulators in registers at two CTAs an SM (at most 93 registers, no
+// spills), where the span kernel with its register prefetch had to keep
+// dgamma in shared memory.  From the output, x_hat = (y - beta)/gamma with
+// 1/gamma and beta staged next to gamma in the thread's slot.  Measured:
 // LayerNorm 8192x5120 bf16 59.5 -> 55.4 us (main kernel 56.6 -> 51.6), fp16
 // 61.3 -> 55.7, 4096x10240 62.0 -> 60.3; RMSNorm 8192x5120 48.6 -> 47.3.
 // Every wait is bounded; a wait that runs out sets the error word and stops
@@ -663,18 +665,27 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_span_kernel(const BwdArgs a) {
 // waits on memory more and gains from a third (measured 8192x5120 bf16 45.6 ->
 // 43.0 us); LayerNorm does not (53.3 -> 54.5).
 template <int KIND>
-__host__ __device__ constexpr int spanb_bufs() { return KIND == KIND_RMS ? 3 : 2; }
+__host__ __device__ constexpr int spanb_bufs() { return KIND == KIND_RMS || KIND == KIND_RMS_Y ? 3 : 2; }
+
+// Floats of a thread's parameter slot: gamma of its 16 columns, from the
+// output also 1/gamma and (LayerNorm) beta, then 4 floats of padding (the
+// 16-byte reads of eight consecutive threads then hit distinct banks: the slot
+// stride is 4 mod 32 words for 20 and 36, 20 mod 32 for 52).
+template <int KIND>
+__host__ __device__ constexpr int spanb_slot() {
+  return kind_from_y(KIND) ? (kind_is_ln(KIND) ? 3 : 2) * kSpanCols + 4 : kSpanSlot;
+}
 
 struct SpanBLayout {
   int bars, abort, red, gamma, bufs, buf_bytes, total;
 };
-__host__ __device__ inline SpanBLayout spanb_layout(int tpr, int H, int es, int NS, int NB) {
+__host__ __device__ inline SpanBLayout spanb_layout(int tpr, int H, int es, int NS, int NB, int slot) {
   SpanBLayout L;
   L.bars = 0;
   L.abort = 8 * NB;
   L.red = (L.abort + 4 + 15) & ~15;
   L.gamma = (L.red + 4 * 2 * (tpr / 32) * NS + 15) & ~15;
-  L.bufs = (L.gamma + 4 * tpr * kSpanSlot + 127) & ~127;
+  L.bufs = (L.gamma + 4 * tpr * slot + 127) & ~127;
   L.buf_bytes = (H * es + 127) & ~127;
   L.total = L.bufs + 2 * NB * L.buf_bytes;  // [buffers][x, dy]
   return L;
@@ -687,10 +698,12 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
   constexpr int NP = E / 2;
   constexpr int NWD = E * (int)sizeof(T) / 4;
   constexpr int NL = NWD / 8;
-  constexpr int SW = kSpanSlot;
-  constexpr bool LN = KIND == KIND_LN;
-  constexpr int NS = LN ? 3 : 1;
-  static_assert(KIND == KIND_LN || KIND == KIND_RMS, "from x only");
+  constexpr int SW = spanb_slot<KIND>();
+  constexpr bool LN = kind_is_ln(KIND);
+  constexpr bool FROM_Y = kind_from_y(KIND);  // x is the forward's output y
+  constexpr bool RECENTER = KIND == KIND_LN;
+  constexpr int NS = LN ? (RECENTER ? 3 : 2) : 1;
+  static_assert(KIND != KIND_FUSED, "LayerNorm/RMSNorm, from x or from the output");
   extern __shared__ __align__(128) unsigned char smem_sb[];
   const int tpr = blockDim.x;
   const int t = threadIdx.x;
@@ -703,7 +716,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
   const bool w_f32 = a.w_f32 != 0;
   const size_t es = sizeof(T);
   constexpr int NB = spanb_bufs<KIND>();
-  const SpanBLayout L = spanb_layout(tpr, H, (int)es, NS, NB);
+  const SpanBLayout L = spanb_layout(tpr, H, (int)es, NS, NB, SW);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem_sb + L.bars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_sb + L.abort);
   float* red = reinterpret_cast<float*>(smem_sb + L.red);
@@ -729,21 +742,30 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
     *abort_flag = 0;
     fence_barrier_init();
   }
-#pragma unroll
-  for (int q = 0; q < E / 4; ++q) {
-    float4 g4 = make_float4(1.f, 1.f, 1.f, 1.f);
-    if (a.gamma != nullptr && active) {
+  // Four parameters of held quad q as fp32 (p == nullptr or an idle thread: fill).
+  auto param4 = [&](const void* p, int q, float fill) {
+    float4 v = make_float4(fill, fill, fill, fill);
+    if (p != nullptr && active) {
       const int c = t * E + held_col(q);
       if (w_f32) {
-        g4 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.gamma) + c);
+        v = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p) + c);
       } else {
-        const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const T*>(a.gamma) + c);
+        const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const T*>(p) + c);
         const uint32_t w[2] = {u.x, u.y};
         const float2 lo = word_pair<D>(w, 0), hi = word_pair<D>(w, 1);
-        g4 = make_float4(lo.x, lo.y, hi.x, hi.y);
+        v = make_float4(lo.x, lo.y, hi.x, hi.y);
       }
     }
+    return v;
+  };
+#pragma unroll
+  for (int q = 0; q < E / 4; ++q) {
+    const float4 g4 = param4(a.gamma, q, 1.f);
     *reinterpret_cast<float4*>(gsh + t * SW + 4 * q) = g4;
+    if constexpr (FROM_Y) {  // 1/gamma (IEEE division: gamma = 0 gives infinity) and beta
+      *reinterpret_cast<float4*>(gsh + t * SW + E + 4 * q) = make_float4(1.f / g4.x, 1.f / g4.y, 1.f / g4.z, 1.f / g4.w);
+      if (LN) *reinterpret_cast<float4*>(gsh + t * SW + 2 * E + 4 * q) = param4(a.beta, q, 0.f);
+    }
   }
   __syncthreads();
 
@@ -772,7 +794,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
   float nrs = 0.f, nmu = 0.f;
   if (row < a.N) {
     nrs = a.rstd[row];
-    if (LN) nmu = a.mean[row];
+    if (RECENTER) nmu = a.mean[row];
   }
   char* dxp = reinterpret_cast<char*>(a.dx) + (row * a.lddx + (int64_t)t * E) * es;
   const int64_t sdx_step = stride * a.lddx * (int64_t)es;
@@ -788,10 +810,10 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
     const int ph = (k / NB) & 1;
     const float r = nrs;
     const float2 r2 = splat2(r);
-    const float2 b2 = splat2(LN ? -nmu * r : 0.f);
+    const float2 b2 = splat2(RECENTER ? -nmu * r : 0.f);
     if (row + stride < a.N) {
       nrs = a.rstd[row + stride];
-      if (LN) nmu = a.mean[row + stride];
+      if (RECENTER) nmu = a.mean[row + stride];
     }
     const bool ok = mbar_wait(&bar[b], (uint32_t)ph, a.err, abort_flag);
     const unsigned char* bx = bufs + (size_t)b * 2 * L.buf_bytes + (size_t)t * E * es;
@@ -807,10 +829,30 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
       }
     }
     float2 xh[NP];
+    if constexpr (FROM_Y) {
+      // x_hat = (y - beta) / gamma, from the forward's output.
 #pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      const float2 xv = word_pair<D>(xw, p);
-      xh[p] = LN ? fma2(xv, r2, b2) : mul2(xv, r2);
+      for (int q = 0; q < E / 4; ++q) {
+        const float4 i4 = *reinterpret_cast<const float4*>(my_g + E + 4 * q);
+        const float2 gi[2] = {make_float2(i4.x, i4.y), make_float2(i4.z, i4.w)};
+        float2 be[2] = {splat2(0.f), splat2(0.f)};
+        if constexpr (LN) {
+          const float4 b4 = *reinterpret_cast<const float4*>(my_g + 2 * E + 4 * q);
+          be[0] = make_float2(b4.x, b4.y);
+          be[1] = make_float2(b4.z, b4.w);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float2 yv = word_pair<D>(xw, 2 * q + h);
+          xh[2 * q + h] = mul2(LN ? sub2(yv, be[h]) : yv, gi[h]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        const float2 xv = word_pair<D>(xw, p);
+        xh[p] = LN ? fma2(xv, r2, b2) : mul2(xv, r2);
+      }
     }
     float2 sg = splat2(0.f), sgx = splat2(0.f), sxh = splat2(0.f);
     if (active) {
@@ -823,10 +865,8 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
           const int p = 2 * q + h;
           const float2 g = mul2(word_pair<D>(dw, p), gm[h]);
           sgx = fma2(g, xh[p], sgx);
-          if (LN) {
-            sg = add2(sg, g);
-            sxh = add2(sxh, xh[p]);
-          }
+          if (LN) sg = add2(sg, g);
+          if (RECENTER) sxh = add2(sxh, xh[p]);
         }
       }
     }
@@ -834,7 +874,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
     if (LN) {
       S[0] = sg.x + sg.y;
       S[1] = sgx.x + sgx.y;
-      S[NS - 1] = sxh.x + sxh.y;
+      if constexpr (RECENTER) S[NS - 1] = sxh.x + sxh.y;
     } else {
       S[0] = sgx.x + sgx.y;
     }
@@ -844,7 +884,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       issue(row + NB * stride, b);
     }
-    const float s0 = LN ? S[NS - 1] * inv_h : 0.f;
+    const float s0 = RECENTER ? S[NS - 1] * inv_h : 0.f;
     const float c1 = LN ? S[0] * inv_h : 0.f;
     const float c2 = LN ? fmaf(-s0, S[0], S[1]) * inv_h : S[0] * inv_h;
     // LayerNorm: dx = r*(g - c1 - c2*xc) taken as (-c2*r)*xc + (g*r - c1*r),
@@ -863,7 +903,7 @@ __global__ void __launch_bounds__(MAXT, MINB) bwd_spanb_kernel(const BwdArgs a) 
           const int p = 2 * q + h;
           const float2 d = word_pair<D>(dw, p);
           const float2 g = mul2(d, gm[h]);
-          const float2 xc = LN ? sub2(xh[p], s02) : xh[p];
+          const float2 xc = RECENTER ? sub2(xh[p], s02) : xh[p];
           if constexpr (LN) pair_word<D>(out, p, fma2(xc, na2, fma2(g, r2, nb2)));
           else pair_word<D>(out, p, mul2(fma2(xc, nc22, g), r2));
           accg[p] = fma2(d, xc, accg[p]);
@@ -1481,16 +1521,19 @@ cudaError_t launch_bwd_typed(BwdArgs a, void* dg, void* db, const DeviceInfo& de
       done = true;
     }
   }
-  // Span rows from shared memory: half-precision LayerNorm and RMSNorm rows of
-  // 257..640 threads at 16 contiguous columns a thread.
-  if constexpr ((KIND == KIND_LN || KIND == KIND_RMS) && VEC == 8) {
+  // Span rows from shared memory: half-precision LayerNorm and RMSNorm rows,
+  // from x or from the saved output (measured from the output against the
+  // interleaved register rows: LayerNorm 8192x5120 bf16 74.0 -> 54.4 us,
+  // 4096x10240 87.5 -> 63.3, RMSNorm 8192x5120 52.1 -> 46.4).
+  if constexpr (KIND != KIND_FUSED && VEC == 8) {
     auto al32 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
     const bool aligned32 = al32(a.x) && al32(a.dy) && al32(a.dx) && (a.ldx * es) % 32 == 0 &&
                            (a.lddy * es) % 32 == 0 && (a.lddx * es) % 32 == 0;
     const int stpr = (a.H / kSpanCols + 31) / 32 * 32;
-    const SpanBLayout SL = spanb_layout(stpr, a.H, (int)es, NS, spanb_bufs<KIND>());
+    const SpanBLayout SL = spanb_layout(stpr, a.H, (int)es, NS, spanb_bufs<KIND>(), spanb_slot<KIND>());
+    const bool beta_ok = !(FROM_Y && LN) || !a.beta || (reinterpret_cast<uintptr_t>(a.beta) & 15u) == 0;
     if (!done && dev.path == PATH_AUTO && aligned32 && a.H % kSpanCols == 0 && stpr > 256 && stpr <= 640 &&
-        (size_t)SL.total <= (size_t)dev.max_smem_optin &&
+        (size_t)SL.total <= (size_t)dev.max_smem_optin && beta_ok &&
         (!a.gamma || (reinterpret_cast<uintptr_t>(a.gamma) & 15u) == 0)) {
       // The row reduction's cross-warp butterfly over a compile-time lane count
       // (measured LayerNorm 8192x5120 bf16 53.2 -> 51.9 us, 4096x8192 49.4 ->

@@ -8,7 +8,8 @@ those limits (4096 = 256 threads, 4112 = 257, 10240 = 640, 10256 = 641), run
 ragged and tiny row counts (fewer rows than CTAs, a last partial wave), padded
 strides that keep 32-byte alignment (the span paths) and strides that keep
 only 16-byte alignment (the interleaved register rows), the saved statistics
-of the GPU forward, and both dgamma/dbeta requested and dx alone.
+of the GPU forward, and both dgamma/dbeta requested and dx alone; and the
+backward from the forward's saved output on the shared-memory span rows.
 """
 
 import pytest
@@ -98,3 +99,25 @@ def test_span_strides(kind, H, ld):
 @pytest.mark.parametrize("kind", ["ln", "rms"])
 def test_span_dx_only(kind, H):
     _run(kind, 500, H, BF, param_grads=False)
+
+
+# The backward from the forward's saved output on the span rows from shared
+# memory (rows of 257..640 threads): x_hat = (y - beta)/gamma from per-thread
+# 1/gamma and beta slots, next to gamma.
+from test_from_output_gpu import ln_y_case, rms_y_case  # noqa: E402
+
+
+@pytest.mark.parametrize("dt", [BF, F16], ids=["bf16", "f16"])
+@pytest.mark.parametrize("H", [4096, 4112, 5120, 8192, 10240, 10256])
+def test_span_from_output_widths(H, dt):
+    ln_y_case(300, H, dt, seed=H)
+    rms_y_case(300, H, dt, seed=H + 1)
+
+
+@pytest.mark.parametrize("N", [1, 7, 305])
+def test_span_from_output_row_counts_and_params(N):
+    ln_y_case(N, 5120, BF, seed=N)
+    rms_y_case(N, 5120, BF, seed=N + 1)
+    ln_y_case(N, 5120, BF, seed=N + 2, wdt=torch.float32)      # fp32 parameters
+    ln_y_case(N, 5120, F16, seed=N + 3, gamma=False, beta=False)  # no affine
+    rms_y_case(N, 5120, F16, seed=N + 4, gamma=False)
