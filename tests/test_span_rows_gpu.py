@@ -17,7 +17,7 @@ import torch
 
 import oracle as O
 import rmsnorm_ln_fwd_gb300 as nl
-from normtest import DT_NAME, check_out, check_param, ln_dx_scale, np64, rms_dx_scale
+from normtest import DT_NAME, check_out, check_param, ln_dx_scale, ln_y_scale, np64, rms_dx_scale
 from rmsnorm_ln_fwd_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -121,3 +121,30 @@ def test_span_from_output_row_counts_and_params(N):
     ln_y_case(N, 5120, BF, seed=N + 2, wdt=torch.float32)      # fp32 parameters
     ln_y_case(N, 5120, F16, seed=N + 3, gamma=False, beta=False)  # no affine
     rms_y_case(N, 5120, F16, seed=N + 4, gamma=False)
+
+
+@pytest.mark.parametrize("H", [5120, 8192])
+def test_span_in_place(H):
+    """y over x in the forward (wide-chunk rows) and dx over dy in the
+    backward (span rows from shared memory, from x and from the output): each
+    row's dy sits in shared memory before that row's dx is written."""
+    N, eps = 333, 1e-5
+    t = {k: v.to(DEV) for k, v in synth.norm_inputs(N, H, "bf16", seed=H).items()}
+    xn, dyn, gn, bn = np64(t["x"]), np64(t["dy"]), np64(t["gamma"]), np64(t["beta"])
+    x = t["x"].clone()
+    y, mean, rstd = nl.ln_forward(x, t["gamma"], t["beta"], eps, out=x)
+    assert y.data_ptr() == x.data_ptr()
+    dy = t["dy"].clone()
+    nl.ln_backward(dy, t["x"], mean, rstd, t["gamma"], dx=dy)
+    dy2 = t["dy"].clone()
+    _, rstd2 = nl.rms_forward(t["x"], t["gamma"], eps)
+    nl.rms_backward(dy2, t["x"], rstd2, t["gamma"], dx=dy2)
+    torch.cuda.synchronize()
+    yr, mr, rr = O.layer_norm_forward(xn, gn, bn, eps)
+    check_out(np64(x), yr, ln_y_scale(xn, mr, rr, gn, bn), BF, f"in-place y {H}")
+    dxr, _, _ = O.layer_norm_backward(dyn, xn, gn, eps)
+    check_out(np64(dy), dxr, ln_dx_scale(dyn, xn, gn, eps), BF, f"in-place ln dx {H}")
+    dxr2, _ = O.rms_norm_backward(dyn, xn, gn, eps)
+    check_out(np64(dy2), dxr2, rms_dx_scale(dyn, xn, gn, eps), BF, f"in-place rms dx {H}")
+    ln_y_case(N, H, BF, seed=H + 5, dx_into_dy=True)
+    rms_y_case(N, H, BF, seed=H + 6, dx_into_dy=True)
