@@ -16,10 +16,11 @@
 //   threads touch consecutive 16-byte chunks, so every warp-wide access is
 //   fully coalesced.  Needs 16-byte aligned rows and H a multiple of the
 //   vector width.
-// * fwd_wide_kernel -- the register rows of half-precision LayerNorm and
-//   RMSNorm whose rows are 32-byte aligned (H >= 512, a multiple of 16): the
-//   same walk, with 32-byte chunks of 16 contiguous columns as the unit and
-//   gamma/beta in a per-thread slot, for fewer instructions an element.
+// * fwd_wide_kernel -- the register rows of half-precision LayerNorm,
+//   RMSNorm and the fused add whose rows are 32-byte aligned (H >= 512, a
+//   multiple of 16): the same walk, with 32-byte chunks of 16 contiguous
+//   columns as the unit and gamma/beta in a per-thread slot, for fewer
+//   instructions an element.
 // * fwd_staged_kernel -- persistent, one CTA per SM; a producer warp streams
 //   rows through a shared-memory ring with bulk copies (see staged.cuh) and
 //   consumer row groups compute from shared memory.  Same alignment needs,
@@ -330,8 +331,8 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_rows_kernel(const FwdArgs a) {
 }
 
 
-// Wide-chunk register rows (half-precision LayerNorm and RMSNorm, rows 32-byte
-// aligned, H a multiple of 16): the row walk, prefetch and arithmetic of
+// Wide-chunk register rows (half-precision LayerNorm, RMSNorm and the fused
+// add, rows 32-byte aligned, H a multiple of 16): the row walk, prefetch and arithmetic of
 // fwd_rows_body, but a thread's unit is a 32-byte chunk of 16 contiguous
 // columns -- chunk c of thread t covers columns [16*(t + c*tpr), +16) -- so
 // one 256-bit load or store moves it, the thread reaches its chunks from one
@@ -346,7 +347,9 @@ __host__ __device__ constexpr int wide_slot() { return 2 * NCH * kWideCols + 4; 
 template <int KIND, typename D, int NCH, int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB) fwd_wide_kernel(const FwdArgs a) {
   using T = typename D::T;
-  static_assert(sizeof(T) == 2 && (KIND == KIND_LN || KIND == KIND_RMS), "half-precision LayerNorm/RMSNorm");
+  static_assert(sizeof(T) == 2, "half precision");
+  constexpr bool FUSED = KIND == KIND_FUSED;
+  constexpr int NT = FUSED ? NCH : 1;  // residual chunks held (fused add only)
   constexpr int CW = kWideCols;
   constexpr int NP = CW / 2;  // fp32 pairs (32-bit words) a chunk
   constexpr int SLOT = wide_slot<NCH>();
@@ -375,20 +378,28 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_wide_kernel(const FwdArgs a) {
   int64_t row = (int64_t)blockIdx.x * rpc + slot;
   const T* xnext = reinterpret_cast<const T*>(a.x) + row * a.ldx + t * CW;
   const int64_t xstep = stride * a.ldx;
-  uint32_t nx[NCH][NP];
+  const T* rnext = FUSED ? reinterpret_cast<const T*>(a.res) + row * a.ldr + t * CW : nullptr;
+  const int64_t rstep = FUSED ? stride * a.ldr : 0;
+  uint32_t nx[NCH][NP], nr[NT][NP];
   uint4 npv = make_uint4(0u, 0u, 0u, 0u);
   auto fetch = [&](int64_t r) {
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
       if (c < nch) {
         ld_stream32(xnext + c * cs, nx[c]);
+        if constexpr (FUSED) ld_stream32(rnext + c * cs, nr[c]);
       } else {
 #pragma unroll
         for (int k = 0; k < NP; ++k) nx[c][k] = 0u;
+        if constexpr (FUSED) {
+#pragma unroll
+          for (int k = 0; k < NP; ++k) nr[c][k] = 0u;
+        }
       }
     }
     if constexpr (KIND == KIND_LN) npv = ld_cached(reinterpret_cast<const T*>(a.x) + r * a.ldx);
     xnext += xstep;
+    if constexpr (FUSED) rnext += rstep;
   };
   auto vector_mean = [](const uint4& u) {
     float f0[VEC];
@@ -399,7 +410,7 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_wide_kernel(const FwdArgs a) {
     return sum0 * (1.f / VEC);
   };
   if (row < a.N) fetch(row);
-  constexpr bool PF = kL2PrefetchRows > 1;
+  constexpr bool PF = kL2PrefetchRows > 1 && !FUSED;
   auto l2_prefetch_row = [&](int64_t pr) {
     l2_prefetch_bulk(reinterpret_cast<const T*>(a.x) + pr * a.ldx, (uint32_t)(H * sizeof(T)));
   };
@@ -439,6 +450,8 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_wide_kernel(const FwdArgs a) {
 
   T* yrow = reinterpret_cast<T*>(a.y) + row * a.ldy + t * CW;
   const int64_t ystep = stride * a.ldy;
+  T* hrow = FUSED ? reinterpret_cast<T*>(a.h) + row * a.ldh + t * CW : nullptr;
+  const int64_t hstep = FUSED ? stride * a.ldh : 0;
   int parity = 0;
   for (; row < a.N; row += stride, yrow += ystep) {
     float2 f[NCH][NP];
@@ -446,6 +459,21 @@ __global__ void __launch_bounds__(MAXT, MINB) fwd_wide_kernel(const FwdArgs a) {
     for (int c = 0; c < NCH; ++c)
 #pragma unroll
       for (int p = 0; p < NP; ++p) f[c][p] = word_pair<D>(nx[c], p);
+    if constexpr (FUSED) {
+      // h = x + residual in fp32, stored (rounded) by the thread that read
+      // both, before the next row's loads are issued
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        uint32_t hw[NP];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          f[c][p] = add2(f[c][p], word_pair<D>(nr[c], p));
+          pair_word<D>(hw, p, f[c][p]);
+        }
+        if (c < nch) st_vec32(hrow + c * cs, hw);
+      }
+      hrow += hstep;
+    }
     const float pivot = KIND == KIND_LN ? vector_mean(npv) : 0.f;
     if (row + stride < a.N) fetch(row + stride);
     if constexpr (PF) {
@@ -864,7 +892,10 @@ static cudaError_t run_wide(const FwdArgs& a, int threads, int rpc, size_t smem,
                             cudaStream_t s) {
   const int64_t groups = (a.N + rpc - 1) / rpc;
   constexpr int W1_MINB = KIND == KIND_LN ? 2 : 3;
-  if constexpr (NCH == 1) {  // one chunk a lane: one-warp rows only
+  if constexpr (KIND == KIND_FUSED) {  // 16 columns a thread up to 640 threads, three CTAs an SM when they fit
+    if (threads <= 256) return launch_rows(fwd_wide_kernel<KIND, D, NCH, 256, 3>, a, threads, smem, dev, groups, s);
+    return launch_rows(fwd_wide_kernel<KIND, D, NCH, 640, 1>, a, threads, smem, dev, groups, s);
+  } else if constexpr (NCH == 1) {  // one chunk a lane: one-warp rows only
     return launch_rows(fwd_wide_kernel<KIND, D, NCH, 256, W1_MINB>, a, threads, smem, dev, groups, s);
   } else {
     if (a.tpr == 32) return launch_rows(fwd_wide_kernel<KIND, D, NCH, 256, W1_MINB>, a, threads, smem, dev, groups, s);
@@ -986,25 +1017,31 @@ cudaError_t launch_fwd_typed(FwdArgs a, const DeviceInfo& dev, cudaStream_t s) {
       return run_staged<KIND, D, 8>(a, c, blocks, smem, s);
     }
   }
-  // Half-precision LayerNorm/RMSNorm rows of at least 512 columns take the
-  // wide-chunk kernel where rows are 32-byte aligned (measured against the
-  // 16-byte register rows: LayerNorm 8192x5120 bf16 31.1 -> 29.4 us,
-  // 2048x16384 29.3 -> 28.7, 4096x8192 26.6 -> 25.9; RMSNorm 8192x5120
-  // 26.4 -> 25.5).
-  if constexpr (KIND != KIND_FUSED && VEC == 8) {
+  // Half-precision rows of at least 512 columns take the wide-chunk kernel
+  // where rows are 32-byte aligned (measured against the 16-byte register
+  // rows: LayerNorm 8192x5120 bf16 31.1 -> 29.4 us, 2048x16384 29.3 -> 28.7,
+  // 4096x8192 26.6 -> 25.9; RMSNorm 8192x5120 26.4 -> 25.5; the fused add
+  // 8192x1024 14.1 -> 13.6, 8192x5120 51.5 -> 49.7, 32768x1024 41.3 -> 39.7).
+  if constexpr (VEC == 8) {
     auto al32 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
-    const bool aligned32 = al32(a.x) && al32(a.y) && (a.ldx * es) % 32 == 0 && (a.ldy * es) % 32 == 0;
+    bool aligned32 = al32(a.x) && al32(a.y) && (a.ldx * es) % 32 == 0 && (a.ldy * es) % 32 == 0;
+    if (KIND == KIND_FUSED)
+      aligned32 = aligned32 && al32(a.res) && al32(a.h) && (a.ldr * es) % 32 == 0 && (a.ldh * es) % 32 == 0;
     if (use_rows && aligned32 && a.H >= 2 * kWideCols * 16 && a.H % kWideCols == 0) {
       const int hc = a.H / kWideCols;
-      const int nch = hc <= 32 ? 1 : 2;
-      const int wtpr = hc <= 64 ? 32 : ((hc + 1) / 2 + 31) / 32 * 32;
+      // The fused add keeps two tensors' next chunks in registers: one chunk a
+      // thread while the row fits 640 threads.
+      const bool one = KIND == KIND_FUSED ? true : hc <= 32;
+      const int nch = one ? 1 : 2;
+      const int wtpr = one ? (hc + 31) / 32 * 32 : (hc <= 64 ? 32 : ((hc + 1) / 2 + 31) / 32 * 32);
+      // (fused rows past 640 threads fall through to the kernels below)
       const int wrpc = wtpr <= 256 ? 256 / wtpr : 1;
       const size_t wsmem = (((size_t)wrpc * 2 * (wtpr / 32) * 3 + 3) & ~(size_t)3) * sizeof(float) +
                            (size_t)wtpr * (nch == 1 ? wide_slot<1>() : wide_slot<2>()) * sizeof(float);
       if (wtpr <= kRowsAutoMaxThreads && wsmem <= (size_t)dev.max_smem_optin) {
         a.tpr = wtpr;
         if (nch == 1) return run_wide<KIND, D, 1>(a, wrpc * wtpr, wrpc, wsmem, dev, s);
-        return run_wide<KIND, D, 2>(a, wrpc * wtpr, wrpc, wsmem, dev, s);
+        if constexpr (KIND != KIND_FUSED) return run_wide<KIND, D, 2>(a, wrpc * wtpr, wrpc, wsmem, dev, s);
       }
     }
   }
