@@ -3,10 +3,12 @@
 //
 // Forward kernels: LayerNorm, RMSNorm and fused residual-add + RMSNorm.
 //
-// Three kernel families (launch_fwd_typed picks one per call: register rows
-// while a row needs at most 640 threads, then the bulk-copy pipeline, then
-// register rows shared by a cluster of 2, 4 or 8 CTAs, then register rows of
-// up to 1024 threads for widths no cluster split divides, then the loop):
+// Kernel families (launch_fwd_typed picks one per call: register rows --
+// wide-chunk rows where half-precision rows are 32-byte aligned, else 16-byte
+// vector rows -- while a row needs at most 640 threads, then the bulk-copy
+// pipeline, then register rows shared by a cluster of 2, 4 or 8 CTAs, then
+// register rows of up to 1024 threads for widths no cluster split divides,
+// then the loop):
 //
 // * fwd_rows_kernel -- the row lives in registers.  A "row group" of `tpr`
 //   threads (one warp for narrow rows, up to 1024 threads for wide rows) owns
