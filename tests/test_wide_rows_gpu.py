@@ -9,15 +9,17 @@ and the first width past it (20496, which takes the cluster rows).  They run
 tiny and ragged row counts, padded strides that keep 32-byte alignment and
 ones that keep only 16-byte alignment (the 16-byte register rows), fp32
 parameters, missing gamma/beta, and rows whose shift sits far from the mean
-(the exact second pass).
+(the exact second pass).  The fused add takes one chunk a thread: its widths,
+h written over x or the residual, and padded strides, h checked bit for bit.
 """
 
+import numpy as np
 import pytest
 import torch
 
 import oracle as O
 import rmsnorm_ln_fwd_gb300 as nl
-from normtest import DT_NAME, check_mean, check_out, check_rstd, ln_y_scale, np64, rms_y_scale
+from normtest import DT_NAME, DT_ORACLE, check_mean, check_out, check_rstd, ln_y_scale, np64, rms_y_scale
 from rmsnorm_ln_fwd_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -109,3 +111,38 @@ def test_wide_fp32_params_and_no_affine(kind, H):
 @pytest.mark.parametrize("dt", [BF, F16], ids=["bf16", "f16"])
 def test_wide_pivot_far_from_mean(H, dt):
     _run("ln", 48, H, dt, far_pivot=True)
+
+
+def _fused(N, H, dt, inplace=None, ld=None, seed=11):
+    eps = 1e-6
+    t = {k: v.to(DEV) for k, v in synth.norm_inputs(N, H, DT_NAME[dt], seed=seed, with_beta=False, with_dy=False,
+                                                     with_residual=True).items()}
+    x0, r0 = t["x"].clone(), t["residual"].clone()
+    x, r = (_strided(t["x"], ld), _strided(t["residual"], ld)) if ld is not None else (t["x"], t["residual"])
+    h_out = {"x": x, "residual": r, None: None}[inplace]
+    if ld is not None and inplace is None:
+        h_out = _strided(torch.zeros_like(x0), ld)
+    y, h, rstd = nl.fused_add_rms_forward(x, r, t["gamma"], eps, h_out=h_out)
+    torch.cuda.synchronize()
+    xn, rn, gn = np64(x0), np64(r0), np64(t["gamma"])
+    yr, hr, rr = O.fused_add_rms_norm_forward(xn, rn, gn, eps, DT_ORACLE[dt])
+    assert np.array_equal(np64(h), hr), f"fused h {N}x{H} ld={ld} inplace={inplace}: not bit-exact"
+    check_out(np64(y), yr, rms_y_scale(xn + rn, rr, gn), dt, f"fused y {N}x{H}")
+    check_rstd(np64(rstd), rr, f"fused rstd {N}x{H}")
+
+
+@pytest.mark.parametrize("dt", [BF, F16], ids=["bf16", "f16"])
+@pytest.mark.parametrize("H", [512, 528, 1040, 5120, 10240, 10256])
+def test_wide_fused_widths(H, dt):
+    _fused(300, H, dt)
+
+
+@pytest.mark.parametrize("inplace", ["x", "residual"])
+@pytest.mark.parametrize("H", [1024, 5120])
+def test_wide_fused_in_place(H, inplace):
+    _fused(257, H, BF, inplace=inplace)
+
+
+@pytest.mark.parametrize("H,ld", [(1024, 1040), (1024, 1032), (5120, 5136)])
+def test_wide_fused_strides(H, ld):
+    _fused(97, H, BF, ld=ld)
