@@ -111,7 +111,7 @@ def check_rstd(got, ref, what):
 
 
 def check_mean(got, ref, x, what):
-    """The saved mean is judged against the scale of its row, RMS(x_row): a
+    """The saved mean is checked against the scale of its row, RMS(x_row): a
     mean near 0 has no relative accuracy of its own to speak of."""
     scale = np.sqrt(np.mean(np.asarray(x, dtype=np.float64) ** 2, axis=1))
     rel = np.max(np.abs(got - ref) / np.maximum(scale, 1e-30)) if ref.size else 0.0
