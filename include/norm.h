@@ -26,7 +26,9 @@
  * eps.  Added INSIDE the square root: rstd = 1/sqrt(var + eps).  eps must be
  *   finite and > 0.
  * Alignment.  Rows whose pointers and strides are 16-byte aligned take the
- *   128-bit vector path; anything else is still correct (scalar path).
+ *   128-bit vector path; half-precision rows that are 32-byte aligned with H
+ *   a multiple of 16 take the faster 256-bit paths; anything else is still
+ *   correct (scalar path).
  * Errors.  Arguments are validated on the host before anything is enqueued;
  *   an invalid call returns an error and enqueues nothing.  A failed launch
  *   returns NORM_ERR_CUDA.  No entry point aborts, throws or prints.
